@@ -1,0 +1,409 @@
+"""Benchmark of the packed prefix-tree attention path on one GB300 (or N, one per rank).
+
+One step = the whole hot path over one synthetic batch:
+  plan (host C++ planner) -> plan upload -> tree RoPE -> tree attention -> readout/calibration.
+
+Default workload: the Llama-1B-shaped batch -- 8 rows, each a 128-token resident
+template -> 512-token document -> 4 question blocks of 48 -> 2 option leaves of
+40 (depth 4), 8192 forward tokens, 32 q heads / 8 kv heads, head dim 64, RoPE
+theta 500000, 4-6 letters per question, T in {0.7, 1.0, 1.3}.
+
+Printed (rank 0, one JSON line): tokens/s of the whole job, the attention
+kernel's TFLOP/s against the measured tensor peak (roofline), an end-to-end
+figure with host<->device copies inside the timed region, SM clocks sampled
+during the timed region, and the CPU oracle timed on the host as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "packed tree-attention tokens/s & TFLOP/s (8192-tok forward), % of f16 TC peak"
+UNIT = "tokens/s"
+N_SETS = 4  # rotating input sets: 4 x ~81 MB > 129 MB L2
+
+# DRAM bytes per attention launch from one ncu capture, valid only for the
+# kernel source it was taken on (sha256 of csrc/attn.cu, first 16 hex digits).
+ATTN_TRAFFIC = {}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return dict(hbm=float(m["hbm_gbs"]), tc=float(m["bf16_tflops_sustained"]),
+                    tc_burst=float(m["bf16_tflops"]), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, tc=1700.0, tc_burst=1900.0, src="fallback")
+
+
+def _src_hash(name):
+    with open(os.path.join(ROOT, "prefix_tree_packed_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class Batch:
+    """One workload resident on the device (N_SETS rotating copies of Q/K/V/O)."""
+
+    def __init__(self, lib, torch, w: synth.Workload, dev):
+        self.lib, self.torch, self.w, self.dev = lib, torch, w, dev
+        kw = dict(leaf1=w.leaf1, leaf2=w.leaf2) if w.leaf1 is not None else {}
+        self.kw = kw
+        self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, **kw)
+        i = self.plan.info
+        self.info = i
+        self.pdev = torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev)
+        q, k, v = synth.draw_qkv(i.n_fwd, i.n_tot, w.hq, w.hkv, w.d, w.seed)
+        self.host = dict(q=q, k=k, v=v)
+        self.sets = []
+        for s in range(N_SETS):
+            self.sets.append(dict(q=torch.from_numpy(q).to(dev), k=torch.from_numpy(k).to(dev),
+                                  v=torch.from_numpy(v).to(dev),
+                                  o=torch.empty((i.n_fwd, w.hq, w.d), dtype=torch.float16, device=dev)))
+        self.tab = torch.from_numpy(lib.rope_table(i.max_pos, w.d, w.theta)).to(dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.nq = i.n_questions
+        if self.nq:
+            stride = w.letter_stride
+            logits = synth.draw_logits(i.n_slots, stride, w.logit_sigma, w.seed)
+            self.host.update(logits=logits, n=w.n_letters, T=w.temperature)
+            self.logits = torch.from_numpy(logits).to(dev)
+            self.nl = torch.from_numpy(w.n_letters).to(dev)
+            self.T = torch.from_numpy(w.temperature).to(dev)
+            self.p_cal = torch.empty((self.nq, stride), device=dev)
+            self.choice = torch.empty(self.nq, dtype=torch.int32, device=dev)
+        self.chunks = [self.plan.chunk(c) for c in range(i.n_chunks)]
+
+    def step(self, s, stream, replan=True, ev=None, bufs=None):
+        """Enqueue one whole-path step on `stream` using input set s (or `bufs`).
+
+        ev: optional list that receives one (start, end) CUDA event pair per
+        attention launch, recorded on `stream` around the launch.
+        """
+        lib, w, i = self.lib, self.w, self.info
+        torch = self.torch
+        if replan:
+            self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, **self.kw)
+        self.plan.upload(self.pdev, i.dev_bytes, stream)
+        b = bufs if bufs is not None else self.sets[s]
+        for c, ci in enumerate(self.chunks):
+            r0, r1 = ci.q0 - i.n_res, ci.q1 - i.n_res
+            qv, ov = b["q"][r0:r1], b["o"][r0:r1]
+            lib.tree_rope(self.plan, self.pdev, c, qv, b["k"], w.hq, w.hkv, w.d, self.tab, i.max_pos, stream)
+            if ev is not None:
+                pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                pair[0].record(stream)
+            lib.tree_attn_fwd(self.plan, self.pdev, c, qv, b["k"], b["v"], ov, None, w.hq, w.hkv, w.d,
+                              status=self.status, stream=stream)
+            if ev is not None:
+                pair[1].record(stream)
+                ev.append(pair)
+        if self.nq:
+            base = self.pdev.data_ptr()
+            lib.readout_decide(self.logits, w.letter_stride, base + i.off_r1, base + i.off_r2, self.nl, self.T,
+                               self.nq, self.p_cal, None, self.choice, self.status, stream)
+
+    def launches_per_step(self):
+        return 2 * len(self.chunks) + (1 if self.nq else 0)
+
+
+def run_gpu(args):
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import prefix_tree_packed_gb300 as lib
+
+    # every rank packs and runs its own batch: rows are independent, no data exchange
+    w = synth.workload(args.workload, seed=args.workload + 101 * rank)
+    B = Batch(lib, torch, w, dev)
+    i = B.info
+    stream = torch.cuda.current_stream()
+    for s in range(args.warmup):
+        B.step(s % N_SETS, stream)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region (events around every attention launch)
+    evs = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(args.steps):
+        B.step(s % N_SETS, stream, ev=evs)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    clk = clocks.stop()
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    assert int(B.status.item()) == 0, "device status word set"
+
+    # ---- end to end: inputs from pinned host memory, decisions back to the host
+    h = B.host
+    pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in h.items()}
+    e2e_bufs = dict(q=torch.empty_like(B.sets[0]["q"]), k=torch.empty_like(B.sets[0]["k"]),
+                    v=torch.empty_like(B.sets[0]["v"]), o=torch.empty_like(B.sets[0]["o"]))
+    out_pc = torch.empty(tuple(B.p_cal.shape), dtype=torch.float32).pin_memory() if B.nq else None
+    out_ch = torch.empty(B.nq, dtype=torch.int32).pin_memory() if B.nq else None
+    h2d = sum(v.numel() * v.element_size() for v in pin.values()) + i.dev_bytes
+    d2h = (out_pc.numel() * 4 + out_ch.numel() * 4) if B.nq else 0
+
+    def e2e_step():
+        e2e_bufs["q"].copy_(pin["q"], non_blocking=True)
+        e2e_bufs["k"].copy_(pin["k"], non_blocking=True)
+        e2e_bufs["v"].copy_(pin["v"], non_blocking=True)
+        if B.nq:
+            B.logits.copy_(pin["logits"], non_blocking=True)
+            B.nl.copy_(pin["n"], non_blocking=True)
+            B.T.copy_(pin["T"], non_blocking=True)
+        B.step(0, stream, bufs=e2e_bufs)
+        if B.nq:
+            out_pc.copy_(B.p_cal, non_blocking=True)
+            out_ch.copy_(B.choice, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b)
+
+    # ---- max over ranks
+    ms = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(ms[0]), float(ms[1])
+    toks_step = i.n_fwd
+    value = toks_step * world * args.steps / (total_ms / 1e3)
+    e2e_value = toks_step * world * args.steps / (e2e_ms / 1e3)
+
+    peaks = _peaks()
+    flops = 4.0 * w.d * w.hq * i.pairs                      # QK^T + PV on visible pairs only
+    attn_launch_ms = statistics.mean(attn_ms)
+    flops_launch = flops / len(B.chunks)
+    achieved = flops_launch / (attn_launch_ms / 1e3) / 1e12
+    h_attn = _src_hash("attn.cu")
+    traffic = ATTN_TRAFFIC.get((args.workload, h_attn))
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 (f32 accumulate)",
+        "data": "synthetic (seeded N(0,1) Q/K/V, N(0,sigma) letter logits)",
+        "config": {"workload": w.name, "forward_tokens": i.n_fwd, "resident_tokens": i.n_res,
+                   "rows": 8 if args.workload == 2 else None, "q_heads": w.hq, "kv_heads": w.hkv,
+                   "head_dim": w.d, "visible_pairs_per_head": i.pairs, "chunks": len(B.chunks),
+                   "questions": B.nq, "l2": f"{N_SETS} rotating input sets (> L2)",
+                   "step": "plan + upload + rope + attention + readout", "parallelism": f"dp{world} (rows)"},
+        "tflops_attention": round(achieved, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tc"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["tc"], 4), "traffic": traffic,
+                     "kernel": "tree_attn_fwd", "peak_source": f"{peaks['src']} bf16 sustained x 1 (f16 = bf16 rate)",
+                     "launch_ms": round(attn_launch_ms, 5)},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4)},
+        "gpu_launches": B.launches_per_step() * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+def _oracle_step(w, rows=None):
+    """The oracle's whole path over the workload, or over forward rows `rows` of it.
+
+    With `rows`, RoPE is applied to those query rows and to the key rows their
+    prompts reach, attention is computed for those rows only, and the readout
+    runs on the workload's questions.
+    """
+    from oracle import attention as oatt
+    from oracle import plan as oplan
+    from oracle import readout as ordo
+    from oracle import rope as orope
+    f = w.forest
+    kw = dict(leaf1=w.leaf1, leaf2=w.leaf2) if w.leaf1 is not None else {}
+    p, qm = oplan.plan_forest(f, max_fwd=w.max_fwd, **kw)
+    q, k, v = synth.draw_qkv(p.n_fwd, p.n_tot, w.hq, w.hkv, w.d, w.seed)
+    if rows is None:
+        qr, kr = orope.apply_plan(p, q, k, w.theta)
+        oatt.attend_paths(p, qr, kr, v)
+        n_tok = p.n_fwd
+    else:
+        need = np.zeros(p.n_tot, bool)
+        blk = np.searchsorted(p.blk_start, np.arange(p.n_tot), side="right") - 1
+        for r in rows:
+            b = int(blk[r + p.n_res])
+            while b >= 0:
+                need[p.blk_start[b]:p.blk_start[b] + p.blk_len[b]] = True
+                b = int(p.blk_parent[b])
+        fwd = np.nonzero(need[p.n_res:])[0] + p.n_res
+        qr = q.copy()
+        kr = k.copy()
+        qr[rows] = orope.rope_f16(q[rows], p.pos[rows + p.n_res], w.theta)
+        kr[fwd] = orope.rope_f16(k[fwd], p.pos[fwd], w.theta)
+        oatt.attend_rows(p, qr, kr, v, rows)
+        n_tok = len(rows)
+    if qm:
+        logits = synth.draw_logits(p.n_slots, w.letter_stride, w.logit_sigma, w.seed)
+        ordo.decide(logits, qm["r1"], qm["r2"], w.n_letters, w.temperature, w.letter_stride)
+    return n_tok
+
+
+def _threads():
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def cpu_baseline(w, budget_s=20.0):
+    t = time.perf_counter()
+    n = _oracle_step(w)
+    dt = time.perf_counter() - t
+    reps = 1
+    while time.perf_counter() - t + dt < budget_s and reps < 3:
+        n += _oracle_step(w)
+        reps += 1
+    dt = time.perf_counter() - t
+    return {"value": round(n / dt, 2), "unit": UNIT, "cores": _threads(), "kind": "oracle",
+            "sample": f"{reps} x the whole workload ({w.name}): host plan, f64 RoPE, per-prompt dense "
+                      f"attention, readout; numpy float64, BLAS threads = cores",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = synth.workload(args.workload)
+    # each step: the oracle on the first row's worth of forward tokens (one prompt tree)
+    from oracle import plan as oplan
+    p, _ = oplan.plan_forest(w.forest, max_fwd=w.max_fwd)
+    rows = np.arange(min(p.n_fwd, 256))
+    for _ in range(args.warmup):
+        _oracle_step(w, rows)
+    t = time.perf_counter()
+    n = 0
+    for _ in range(args.steps):
+        n += _oracle_step(w, rows)
+    dt = time.perf_counter() - t
+    value = n / dt
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "sample_rows": int(len(rows))},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": _threads(), "kind": "oracle",
+                             "sample": f"per step: plan, f64 RoPE and per-row attention of the first "
+                                       f"{len(rows)} forward rows (and the keys of their prompts), readout "
+                                       f"({w.name})"},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,281 @@
+/*
+ * tree_attn.h -- C ABI of the packed prefix-tree attention library (GB300, sm_103a).
+ *
+ * The library computes the data-parallel hot path of a Llama forward over a
+ * batch of prompts packed as prefix trees, as the basal-rs Architecture page
+ * describes it:
+ *
+ *   tree_pack_plan  -- prompts -> per-row prefix trees -> one packed token row
+ *                      ("01 / Request path: Batch and prefix tree";
+ *                       "03 / Packing: Attention over tree blocks")
+ *   tree_rope       -- rotary embedding at tree positions: a token's position
+ *                      is its position in its own prompt ("03 / Packing")
+ *   tree_attn_fwd   -- attention over tree blocks: a token sees the earlier
+ *                      tokens of its own block and all tokens of its ancestor
+ *                      blocks; sibling branches are masked ("03 / Packing";
+ *                      f16 storage, f32 accumulation per "01 / Request path:
+ *                      GPU forward pass")
+ *   readout_decide  -- letter probabilities for both option orders, order 2
+ *                      put back, averaged, calibrated with
+ *                      p_cal = softmax(log(max(p, 1e-12)) / T)
+ *                      ("02 / Basal protocol: Two option orders and calibration")
+ *
+ * Conventions for every call:
+ *   - The return value is a status code (TREE_OK = 0 on success).  On failure
+ *     tree_last_error() returns a message for the calling thread.
+ *   - The caller owns all device memory; the library never allocates device
+ *     memory.  Plans live in host memory owned by the library
+ *     (tree_pack_plan / tree_plan_free).
+ *   - GPU work is enqueued on the caller's stream (NULL = legacy default
+ *     stream) and never synchronised inside the library.  Launch errors are
+ *     returned; errors found on the device (a bounded wait that gave up) are
+ *     written to the caller's int32 `status` word in device memory, which the
+ *     caller clears before the call and reads after synchronising.
+ *   - f16 tensors are IEEE binary16, row-major, densely packed.
+ */
+#ifndef TREE_ATTN_H
+#define TREE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TREE_API __attribute__((visibility("default")))
+#else
+#define TREE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st *tree_stream_t;
+
+enum tree_status {
+  TREE_OK = 0,
+  TREE_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size, question block not a leaf, ... */
+  TREE_ERR_BAD_TREE = 2,      /* parent out of range, cycle, block length <= 0 */
+  TREE_ERR_DEPTH = 3,         /* a tree deeper than max_depth blocks */
+  TREE_ERR_ROW_TOO_LONG = 4,  /* a row (one tree) longer than max_row tokens */
+  TREE_ERR_UNSUPPORTED = 5,   /* head dim not 64/128, hq % hkv != 0, misaligned pointer, > 255 letters */
+  TREE_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed */
+  TREE_ERR_TIMEOUT = 7        /* written to `status` by a device wait that gave up */
+};
+
+/* Message describing the last error of the calling thread ("" if none). */
+TREE_API const char *tree_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+TREE_API int tree_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Planner (host only)                                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * One batch as a forest of prompt blocks ("01 / Request path: Batch and prefix
+ * tree": the prompts of a batch are arranged into rows, each row a tree whose
+ * shared prefixes are computed once).
+ *
+ *   parent[b]   parent block of input block b, -1 for a root
+ *   length[b]   tokens in block b, > 0
+ *   key[b]      content key, NULL = every block unique.  Sibling blocks (same
+ *               parent after merging) with equal non-zero key and equal
+ *               length are one block: identical prompts share one block and
+ *               one readout ("Batch and prefix tree").  Their children pool.
+ *   resident[b] NULL = none.  1 = the block's K/V are already in the cache
+ *               (e.g. the template, computed once at startup, "03 / Packing").
+ *               Resident tokens must come first in the packed order.
+ *   leaf1/leaf2 per question, the input blocks whose last token reads out the
+ *               order-1 and order-2 letters; each must be a leaf after merging.
+ * All arrays are host memory, read during the call only.
+ */
+typedef struct {
+  int32_t n_blocks;
+  const int32_t *parent;
+  const int32_t *length;
+  const uint64_t *key;
+  const uint8_t *resident;
+  int32_t n_questions;
+  const int32_t *leaf1;
+  const int32_t *leaf2;
+} tree_spec_t;
+
+/* Planner options; a zero field takes the default in brackets. */
+typedef struct {
+  int32_t max_fwd;   /* tokens per forward chunk, multiple of 128 [8192] */
+  int32_t max_depth; /* blocks on a root-to-leaf path [8] */
+  int32_t max_row;   /* tokens in one tree [32768] */
+} tree_plan_opts_t;
+
+typedef struct tree_plan tree_plan_t;
+
+/*
+ * Build a plan: merge identical sibling blocks, pack blocks in depth-first
+ * pre-order (children in input order, roots in input order), give each token
+ * its position in its own prompt and the end of its block's subtree, split the
+ * forward tokens into chunks of max_fwd, list for every 128-row query tile the
+ * 128-key tiles it sees (full or partial), and number the readout slots (the
+ * last token of every leaf block, in packed order).
+ *
+ * Visibility in packed order: key j is visible to query i iff
+ *     j <= i  and  i < send[j]
+ * where send[j] is the end of the subtree of j's block.
+ *
+ * On success *out holds a new plan (free with tree_plan_free).  Errors:
+ * TREE_ERR_INVALID_ARG, TREE_ERR_BAD_TREE, TREE_ERR_DEPTH,
+ * TREE_ERR_ROW_TOO_LONG, TREE_ERR_UNSUPPORTED (max_fwd not a multiple of 128).
+ */
+TREE_API int tree_pack_plan(const tree_spec_t *spec, const tree_plan_opts_t *opts, tree_plan_t **out);
+
+/* Free a plan (NULL is accepted). */
+TREE_API int tree_plan_free(tree_plan_t *plan);
+
+typedef struct {
+  int32_t n_input_blocks;
+  int32_t n_blocks;      /* blocks after merging */
+  int32_t n_tot;         /* packed tokens, resident included */
+  int32_t n_res;         /* leading resident tokens */
+  int32_t n_fwd;         /* n_tot - n_res: tokens whose Q/K/V the forward computes */
+  int32_t n_chunks;
+  int32_t n_qtiles;      /* over all chunks */
+  int32_t n_entries;     /* (query tile, key tile) pairs that see anything */
+  int32_t n_slots;       /* readout slots */
+  int32_t n_questions;
+  int32_t max_fwd;
+  int32_t bm, bn;        /* query / key tile rows (128 / 128) */
+  int32_t max_pos;       /* 1 + largest position: rows needed in the RoPE table */
+  int64_t pairs;         /* visible (query, key) pairs over all forward tokens */
+  size_t dev_bytes;      /* size of the device image (tree_plan_upload) */
+  /* byte offsets of the device image's arrays (int32 each) */
+  size_t off_pos, off_send, off_qtile, off_ent, off_order, off_chunk, off_slot_tok, off_r1, off_r2;
+} tree_plan_info_t;
+
+TREE_API int tree_plan_query(const tree_plan_t *plan, tree_plan_info_t *info);
+
+typedef struct {
+  int32_t q0, q1;        /* packed token range of the chunk's queries */
+  int32_t t0, t1;        /* its query tiles */
+  int64_t pairs;         /* visible pairs of its queries */
+  int32_t n_entries;     /* tile pairs the kernel visits */
+} tree_chunk_info_t;
+
+TREE_API int tree_plan_chunk(const tree_plan_t *plan, int32_t chunk, tree_chunk_info_t *info);
+
+/*
+ * Read-only host view of the plan's tables (valid until tree_plan_free).
+ * Blocks are in packed order.  ent[e] = (key_tile << 1) | partial.
+ */
+typedef struct {
+  const int32_t *block_map;                       /* [n_input_blocks] input block -> packed block */
+  const int32_t *blk_start, *blk_len, *blk_parent, *blk_depth, *blk_pos0, *blk_send, *blk_resident,
+      *blk_slot;                                  /* [n_blocks] */
+  const int32_t *pos;                             /* [n_tot] */
+  const int32_t *send;                            /* [ceil(n_tot/128)*128], 0 past n_tot */
+  const int32_t *chunk_q0, *chunk_q1, *chunk_t0, *chunk_t1; /* [n_chunks] */
+  const int32_t *qt_row0, *qt_row1, *qt_ent0, *qt_ent1;     /* [n_qtiles] */
+  const int32_t *ent;                             /* [n_entries] */
+  const int32_t *qt_order;                        /* [n_qtiles] per chunk, most entries first */
+  const int32_t *slot_tok;                        /* [n_slots] */
+  const int32_t *r1, *r2;                         /* [n_questions] readout slots of each question */
+  const void *image;                              /* the device image, host copy */
+  size_t image_bytes;
+} tree_plan_host_view_t;
+
+TREE_API int tree_plan_tables(const tree_plan_t *plan, tree_plan_host_view_t *view);
+
+/*
+ * Copy the plan's device image (info.dev_bytes bytes) into caller-owned device
+ * memory `dev_buf` (16-byte aligned, `bytes` >= dev_bytes) on `stream`.  The
+ * host copy is pageable; the plan may be freed once this returns.
+ */
+TREE_API int tree_plan_upload(const tree_plan_t *plan, void *dev_buf, size_t bytes, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Rotary embedding at tree positions                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Fill host_out[max_pos][d/2][2] with {cos, sin} of pos * theta^(-2i/d),
+ * evaluated in double and rounded to float (the table form of the AstrAI
+ * inference page, "Rotary Embedding Backend").  d even, max_pos > 0.
+ */
+TREE_API int tree_rope_table(float *host_out, int32_t max_pos, int32_t d, double theta);
+
+/*
+ * Rotate, in place, the queries and keys of forward chunk `chunk`, pair
+ * (i, i + d/2) by the angle of the token's tree position (plan pos table):
+ *
+ *   q   f16 [q1-q0, hq, d]   the chunk's query rows (row r = packed token q0 + r)
+ *   k   f16 [n_tot, hkv, d]  the whole KV space; rows [q0, q1) are rotated
+ *   cos_sin  f32 [max_pos][d/2][2] device table from tree_rope_table,
+ *            max_pos >= info.max_pos
+ *
+ * Arithmetic in f32, stored f16 (round to nearest even).  plan_dev is the
+ * device image from tree_plan_upload.  d even and <= 256; q and k 16-byte
+ * aligned; hq*d and hkv*d multiples of 8.
+ */
+TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev, int32_t chunk, void *q, void *k,
+              int32_t hq, int32_t hkv, int32_t d, const float *cos_sin, int32_t max_pos,
+              tree_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Attention over tree blocks                                                */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  int32_t hq, hkv, d;  /* query heads, kv heads (hq % hkv == 0, q head h reads kv head h/(hq/hkv)), d in {64,128} */
+  float scale;         /* scores are q.k * scale; 0 = 1/sqrt(d) (AstrAI inference page, "KV Cache") */
+} tree_attn_params_t;
+
+/*
+ * Attention of forward chunk `chunk` over tree blocks:
+ *
+ *   O[i, h] = sum_{j visible to i} softmax_j(scale * Q[i,h] . K[j,g]) V[j,g],
+ *   g = h / (hq/hkv), visible = j <= i and i < send[j]
+ *
+ *   q    f16 [q1-q0, hq, d]   post-RoPE queries of the chunk
+ *   k, v f16 [n_tot, hkv, d]  post-RoPE keys and values of the whole KV space
+ *                             (resident tokens, earlier chunks and this chunk)
+ *   o    f16 [q1-q0, hq, d]   output, normalised
+ *   lse  f32 [q1-q0, hq] or NULL: natural-log sum of exp of the scaled scores
+ *
+ * Scores, softmax and accumulation in f32; probabilities rounded to f16 for
+ * the P.V product.  All tensors 16-byte aligned.  `status` (device int32, may
+ * be NULL) receives TREE_ERR_TIMEOUT if a pipeline wait gave up.
+ */
+TREE_API int tree_attn_fwd(const tree_plan_t *plan, const void *plan_dev, int32_t chunk, const void *q,
+                  const void *k, const void *v, void *o, float *lse, const tree_attn_params_t *params,
+                  int32_t *status, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Letter readout and calibration                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For each question q (one warp per question):
+ *   l1 = logits[r1[q], 0:n], l2 = logits[r2[q], 0:n], n = n_letters[q] in 1..255
+ *   p     = (softmax(l1) + reverse(softmax(l2))) / 2       reverse: k -> n-1-k
+ *   p_cal = softmax(log(max(p, 1e-12)) / T[q])             T[q] > 0
+ *   choice[q] = argmax p_cal (lowest index on ties), taken as argmax of p
+ *
+ *   logits      f32 [n_slots, stride] device
+ *   r1, r2, n_letters  int32 [n_q] device;  temperature f32 [n_q] device
+ *   p_cal       f32 [n_q, stride] device, zero past n
+ *   p_avg       f32 [n_q, stride] device or NULL, zero past n
+ *   choice      int32 [n_q] device or NULL
+ *   status      device int32 or NULL: TREE_ERR_INVALID_ARG if some n is out
+ *               of 1..min(stride,255) or some T <= 0 (that question's
+ *               outputs are zero, choice -1)
+ * All arithmetic in f32.  n_q == 0 is a no-op.
+ */
+TREE_API int readout_decide(const float *logits, int32_t stride, const int32_t *r1, const int32_t *r2,
+                   const int32_t *n_letters, const float *temperature, int32_t n_q, float *p_cal,
+                   float *p_avg, int32_t *choice, int32_t *status, tree_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREE_ATTN_H */

@@ -132,6 +132,28 @@ def attend_rows(plan: Plan, q_rot, k_rot, v, rows) -> np.ndarray:
     return out
 
 
+def lse_rows(plan: Plan, q_rot, k_rot, rows) -> np.ndarray:
+    """[len(rows), hq] natural log of sum_j exp(q.k_j / sqrt(d)) over each row's own keys."""
+    q = np.asarray(q_rot)
+    n_fwd, hq, d = q.shape
+    groups = hq // k_rot.shape[1]
+    out = np.empty((len(rows), hq), np.float64)
+    for n, r in enumerate(rows):
+        t = int(r) + plan.n_res
+        b = int(np.searchsorted(plan.blk_start, t, side="right") - 1)
+        keys = [np.arange(plan.blk_start[b], t + 1)]
+        x = plan.blk_parent[b]
+        while x >= 0:
+            keys.append(np.arange(plan.blk_start[x], plan.blk_start[x] + plan.blk_len[x]))
+            x = plan.blk_parent[x]
+        kk = np.asarray(k_rot[np.concatenate(keys)], np.float64)
+        for h in range(hq):
+            s = (kk[:, h // groups, :] @ np.asarray(q[int(r), h], np.float64)) / np.sqrt(d)
+            m = s.max()
+            out[n, h] = m + np.log(np.exp(s - m).sum())
+    return out
+
+
 def brute_force(plan: Plan, q_rot, k_rot, v) -> np.ndarray:
     """Masked softmax attention over the whole packed row (tiny inputs only)."""
     m = brute_mask(plan)[plan.n_res:]                          # forward queries x all keys

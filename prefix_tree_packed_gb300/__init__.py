@@ -1,0 +1,238 @@
+"""Python binding of the packed prefix-tree attention library (``libtreeattn.so``).
+
+Argument marshalling only: every step of the path (planning, RoPE, attention,
+readout) runs inside the C-ABI library, declared in ``include/tree_attn.h``.
+Tensors are passed as raw device pointers (any object with ``data_ptr()``, or
+an int) and streams as raw ``cudaStream_t`` handles; PyTorch is used by callers
+for device memory and streams only.
+
+Importing this package raises if the compiled library is missing: there is no
+other implementation to fall back to.  Build it with
+``python prefix_tree_packed_gb300/build.py``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtreeattn.so")
+
+TREE_OK = 0
+TREE_ERR_INVALID_ARG = 1
+TREE_ERR_BAD_TREE = 2
+TREE_ERR_DEPTH = 3
+TREE_ERR_ROW_TOO_LONG = 4
+TREE_ERR_UNSUPPORTED = 5
+TREE_ERR_CUDA = 6
+TREE_ERR_TIMEOUT = 7
+
+# every symbol the header declares
+EXPORTS = (
+    "tree_last_error", "tree_version", "tree_pack_plan", "tree_plan_free", "tree_plan_query",
+    "tree_plan_chunk", "tree_plan_tables", "tree_plan_upload", "tree_rope_table", "tree_rope",
+    "tree_attn_fwd", "readout_decide",
+)
+
+
+class TreeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run `python prefix_tree_packed_gb300/build.py`")
+_lib = C.CDLL(LIB_PATH)
+
+_i32p = C.POINTER(C.c_int32)
+
+
+class _Spec(C.Structure):
+    _fields_ = [("n_blocks", C.c_int32), ("parent", _i32p), ("length", _i32p),
+                ("key", C.POINTER(C.c_uint64)), ("resident", C.POINTER(C.c_uint8)),
+                ("n_questions", C.c_int32), ("leaf1", _i32p), ("leaf2", _i32p)]
+
+
+class _Opts(C.Structure):
+    _fields_ = [("max_fwd", C.c_int32), ("max_depth", C.c_int32), ("max_row", C.c_int32)]
+
+
+class PlanInfo(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in (
+        "n_input_blocks", "n_blocks", "n_tot", "n_res", "n_fwd", "n_chunks", "n_qtiles",
+        "n_entries", "n_slots", "n_questions", "max_fwd", "bm", "bn", "max_pos")] + [
+        ("pairs", C.c_int64), ("dev_bytes", C.c_size_t)] + [(n, C.c_size_t) for n in (
+        "off_pos", "off_send", "off_qtile", "off_ent", "off_order", "off_chunk", "off_slot_tok",
+        "off_r1", "off_r2")]
+
+
+class ChunkInfo(C.Structure):
+    _fields_ = [("q0", C.c_int32), ("q1", C.c_int32), ("t0", C.c_int32), ("t1", C.c_int32),
+                ("pairs", C.c_int64), ("n_entries", C.c_int32)]
+
+
+_VIEW_FIELDS = ("block_map", "blk_start", "blk_len", "blk_parent", "blk_depth", "blk_pos0",
+                "blk_send", "blk_resident", "blk_slot", "pos", "send", "chunk_q0", "chunk_q1",
+                "chunk_t0", "chunk_t1", "qt_row0", "qt_row1", "qt_ent0", "qt_ent1", "ent",
+                "qt_order", "slot_tok", "r1", "r2")
+
+
+class _View(C.Structure):
+    _fields_ = [(n, _i32p) for n in _VIEW_FIELDS] + [("image", C.c_void_p), ("image_bytes", C.c_size_t)]
+
+
+class AttnParams(C.Structure):
+    _fields_ = [("hq", C.c_int32), ("hkv", C.c_int32), ("d", C.c_int32), ("scale", C.c_float)]
+
+
+_vp = C.c_void_p
+_lib.tree_last_error.restype = C.c_char_p
+_lib.tree_version.restype = C.c_int
+_lib.tree_pack_plan.argtypes = [C.POINTER(_Spec), C.POINTER(_Opts), C.POINTER(_vp)]
+_lib.tree_plan_free.argtypes = [_vp]
+_lib.tree_plan_query.argtypes = [_vp, C.POINTER(PlanInfo)]
+_lib.tree_plan_chunk.argtypes = [_vp, C.c_int32, C.POINTER(ChunkInfo)]
+_lib.tree_plan_tables.argtypes = [_vp, C.POINTER(_View)]
+_lib.tree_plan_upload.argtypes = [_vp, _vp, C.c_size_t, _vp]
+_lib.tree_rope_table.argtypes = [_vp, C.c_int32, C.c_int32, C.c_double]
+_lib.tree_rope.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, _vp,
+                           C.c_int32, _vp]
+_lib.tree_attn_fwd.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp, C.POINTER(AttnParams),
+                               _vp, _vp]
+_lib.readout_decide.argtypes = [_vp, C.c_int32, _vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp]
+for _f in ("tree_pack_plan", "tree_plan_free", "tree_plan_query", "tree_plan_chunk", "tree_plan_tables",
+           "tree_plan_upload", "tree_rope_table", "tree_rope", "tree_attn_fwd", "readout_decide"):
+    getattr(_lib, _f).restype = C.c_int
+
+
+def _check(rc: int):
+    if rc != TREE_OK:
+        raise TreeError(rc, _lib.tree_last_error().decode(errors="replace"))
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def version() -> int:
+    return _lib.tree_version()
+
+
+class Plan:
+    """A packed batch: owns the library's host plan (``tree_pack_plan``)."""
+
+    def __init__(self, parent, length, key=None, resident=None, leaf1=None, leaf2=None,
+                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0):
+        self._keep = []
+        par = np.ascontiguousarray(parent, np.int32)
+        ln = np.ascontiguousarray(length, np.int32)
+        spec = _Spec()
+        spec.n_blocks = par.shape[0]
+        spec.parent = par.ctypes.data_as(_i32p)
+        spec.length = ln.ctypes.data_as(_i32p)
+        self._keep += [par, ln]
+        if key is not None:
+            k = np.ascontiguousarray(key, np.uint64)
+            spec.key = k.ctypes.data_as(C.POINTER(C.c_uint64))
+            self._keep.append(k)
+        if resident is not None:
+            r = np.ascontiguousarray(resident, np.uint8)
+            spec.resident = r.ctypes.data_as(C.POINTER(C.c_uint8))
+            self._keep.append(r)
+        if leaf1 is not None:
+            l1 = np.ascontiguousarray(leaf1, np.int32)
+            l2 = np.ascontiguousarray(leaf2, np.int32)
+            spec.n_questions = l1.shape[0]
+            spec.leaf1 = l1.ctypes.data_as(_i32p)
+            spec.leaf2 = l2.ctypes.data_as(_i32p)
+            self._keep += [l1, l2]
+        opts = _Opts(max_fwd, max_depth, max_row)
+        h = _vp()
+        _check(_lib.tree_pack_plan(C.byref(spec), C.byref(opts), C.byref(h)))
+        self._keep = []
+        self.handle = h
+        self.info = PlanInfo()
+        _check(_lib.tree_plan_query(self.handle, C.byref(self.info)))
+
+    @classmethod
+    def from_forest(cls, forest, **kw):
+        return cls(forest.parent, forest.length, forest.key, forest.resident, **kw)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            _lib.tree_plan_free(h)
+            self.handle = None
+
+    def chunk(self, c: int) -> ChunkInfo:
+        ci = ChunkInfo()
+        _check(_lib.tree_plan_chunk(self.handle, c, C.byref(ci)))
+        return ci
+
+    def tables(self) -> dict:
+        """Copies of every host table as numpy arrays (plus the device image bytes)."""
+        v = _View()
+        _check(_lib.tree_plan_tables(self.handle, C.byref(v)))
+        i = self.info
+        n_kvt = -(-i.n_tot // i.bn)
+        sizes = dict(block_map=i.n_input_blocks, pos=i.n_tot, send=n_kvt * i.bn, ent=i.n_entries,
+                     qt_order=i.n_qtiles, slot_tok=i.n_slots, r1=i.n_questions, r2=i.n_questions)
+        for n in ("blk_start", "blk_len", "blk_parent", "blk_depth", "blk_pos0", "blk_send",
+                  "blk_resident", "blk_slot"):
+            sizes[n] = i.n_blocks
+        for n in ("chunk_q0", "chunk_q1", "chunk_t0", "chunk_t1"):
+            sizes[n] = i.n_chunks
+        for n in ("qt_row0", "qt_row1", "qt_ent0", "qt_ent1"):
+            sizes[n] = i.n_qtiles
+        out = {}
+        for n in _VIEW_FIELDS:
+            cnt = sizes[n]
+            p = getattr(v, n)
+            out[n] = np.ctypeslib.as_array(p, shape=(cnt,)).copy() if cnt > 0 else np.zeros(0, np.int32)
+        out["image"] = np.ctypeslib.as_array(C.cast(v.image, C.POINTER(C.c_uint8)),
+                                             shape=(v.image_bytes,)).copy()
+        return out
+
+    def upload(self, dev_buf, nbytes: int, stream=None):
+        _check(_lib.tree_plan_upload(self.handle, _ptr(dev_buf), nbytes, _stream(stream)))
+
+
+def rope_table(max_pos: int, d: int, theta: float) -> np.ndarray:
+    out = np.empty((max_pos, d // 2, 2), np.float32)
+    _check(_lib.tree_rope_table(out.ctypes.data, max_pos, d, theta))
+    return out
+
+
+def tree_rope(plan: Plan, plan_dev, chunk: int, q, k, hq: int, hkv: int, d: int, cos_sin,
+              max_pos: int, stream=None):
+    _check(_lib.tree_rope(plan.handle, _ptr(plan_dev), chunk, _ptr(q), _ptr(k), hq, hkv, d,
+                          _ptr(cos_sin), max_pos, _stream(stream)))
+
+
+def tree_attn_fwd(plan: Plan, plan_dev, chunk: int, q, k, v, o, lse, hq: int, hkv: int, d: int,
+                  scale: float = 0.0, status=None, stream=None):
+    p = AttnParams(hq, hkv, d, scale)
+    _check(_lib.tree_attn_fwd(plan.handle, _ptr(plan_dev), chunk, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                              _ptr(lse), C.byref(p), _ptr(status), _stream(stream)))
+
+
+def readout_decide(logits, stride: int, r1, r2, n_letters, temperature, n_q: int, p_cal, p_avg=None,
+                   choice=None, status=None, stream=None):
+    _check(_lib.readout_decide(_ptr(logits), stride, _ptr(r1), _ptr(r2), _ptr(n_letters),
+                               _ptr(temperature), n_q, _ptr(p_cal), _ptr(p_avg), _ptr(choice),
+                               _ptr(status), _stream(stream)))

@@ -1,0 +1,475 @@
+// Host planner: a batch's prompt blocks -> prefix trees -> one packed token row.
+//
+// Follows the basal-rs Architecture page: "01 / Request path: Batch and prefix
+// tree" (rows are trees whose shared prefixes are computed once; at most
+// 32,768 tokens per row, 8192 per forward, 8 blocks deep; identical prompts
+// share one readout) and "03 / Packing: Attention over tree blocks" (the tree
+// becomes one row of tokens; a token sees earlier tokens of its block and all
+// tokens of ancestor blocks; its rotary position is its position in its own
+// prompt).  The long-request lane of "04 / Scheduling" runs a long row as
+// several forwards, each resuming with the earlier tensors: here, chunks.
+//
+// Packing is depth-first pre-order, so the subtree of every block is one
+// contiguous token interval [start, send); key j is then visible to query i
+// exactly when j <= i < send[j].  Tiles of 128 queries x 128 keys are sorted
+// into empty (dropped), full (no mask needed) and partial (per-element mask).
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <numeric>
+#include <utility>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace tree {
+
+static thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+namespace {
+
+constexpr int32_t kTile = 128;
+
+size_t align4(size_t words) { return (words + 3) & ~size_t(3); }
+
+int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_row, Plan &P) {
+  const int32_t nb = s.n_blocks;
+  P.n_input_blocks = nb;
+  P.max_fwd = max_fwd;
+  // ---- validation of the input forest
+  for (int32_t b = 0; b < nb; ++b) {
+    const int32_t p = s.parent[b];
+    if (p < -1 || p >= nb || p == b)
+      return fail(TREE_ERR_BAD_TREE, "block %d: parent %d out of range", b, p);
+    if (s.length[b] <= 0) return fail(TREE_ERR_BAD_TREE, "block %d: length %d <= 0", b, s.length[b]);
+  }
+  {
+    // depth of every block by walking up; a chain longer than nb is a cycle
+    for (int32_t b = 0; b < nb; ++b) {
+      int32_t d = 0;
+      for (int32_t x = b; x != -1; x = s.parent[x]) {
+        if (++d > nb) return fail(TREE_ERR_BAD_TREE, "block %d: parent chain has a cycle", b);
+      }
+      if (d > max_depth) return fail(TREE_ERR_DEPTH, "block %d: depth %d > %d", b, d, max_depth);
+    }
+  }
+  // ---- children lists of the input forest (input order)
+  std::vector<std::vector<int32_t>> kids(nb);
+  std::vector<int32_t> roots;
+  for (int32_t b = 0; b < nb; ++b) (s.parent[b] < 0 ? roots : kids[s.parent[b]]).push_back(b);
+
+  auto key_of = [&](int32_t b) -> uint64_t { return s.key ? s.key[b] : 0; };
+  auto res_of = [&](int32_t b) -> int32_t { return s.resident ? (s.resident[b] ? 1 : 0) : 0; };
+
+  // ---- merge identical siblings top-down.  A sibling set is the sorted list
+  // of input children of all members of one merged block.
+  std::vector<int32_t> canon(nb, -1);
+  std::vector<std::vector<int32_t>> ckids(nb);  // canonical -> canonical children, in order
+  std::vector<int32_t> top;
+  struct Work {
+    int32_t owner;  // canonical parent, -1 = the forest
+    std::vector<int32_t> members;
+  };
+  std::vector<Work> work;
+  work.push_back({-1, roots});
+  while (!work.empty()) {
+    Work w = std::move(work.back());
+    work.pop_back();
+    std::sort(w.members.begin(), w.members.end());
+    std::map<std::pair<int32_t, uint64_t>, int32_t> seen;
+    std::vector<int32_t> order;
+    std::map<int32_t, std::vector<int32_t>> pooled;
+    for (int32_t b : w.members) {
+      const uint64_t k = key_of(b);
+      int32_t c = b;
+      if (k != 0) {
+        auto it = seen.find({s.length[b], k});
+        if (it != seen.end()) {
+          c = it->second;
+          if (res_of(b) != res_of(c))
+            return fail(TREE_ERR_INVALID_ARG, "blocks %d and %d merge but disagree on residency", c, b);
+        } else {
+          seen.emplace(std::make_pair(s.length[b], k), b);
+        }
+      }
+      canon[b] = c;
+      if (c == b) order.push_back(b);
+      auto &pl = pooled[c];
+      pl.insert(pl.end(), kids[b].begin(), kids[b].end());
+    }
+    if (w.owner < 0)
+      top = order;
+    else
+      ckids[w.owner] = order;
+    for (auto &kv : pooled)
+      if (!kv.second.empty()) work.push_back({kv.first, std::move(kv.second)});
+  }
+
+  // ---- depth-first pre-order of canonical blocks
+  std::vector<int32_t> packed;
+  {
+    std::vector<int32_t> st(top.rbegin(), top.rend());
+    while (!st.empty()) {
+      const int32_t c = st.back();
+      st.pop_back();
+      packed.push_back(c);
+      const auto &ch = ckids[c];
+      for (auto it = ch.rbegin(); it != ch.rend(); ++it) st.push_back(*it);
+    }
+  }
+  const int32_t nbc = (int32_t)packed.size();
+  P.n_blocks = nbc;
+  std::vector<int32_t> pidx(nb, -1);
+  for (int32_t i = 0; i < nbc; ++i) pidx[packed[i]] = i;
+  P.block_map.resize(nb);
+  for (int32_t b = 0; b < nb; ++b) P.block_map[b] = pidx[canon[b]];
+
+  P.blk_start.assign(nbc, 0);
+  P.blk_len.assign(nbc, 0);
+  P.blk_parent.assign(nbc, -1);
+  P.blk_depth.assign(nbc, 0);
+  P.blk_pos0.assign(nbc, 0);
+  P.blk_send.assign(nbc, 0);
+  P.blk_resident.assign(nbc, 0);
+  P.blk_slot.assign(nbc, -1);
+  for (int32_t i = 0; i < nbc; ++i) {
+    const int32_t c = packed[i];
+    P.blk_len[i] = s.length[c];
+    P.blk_parent[i] = s.parent[c] >= 0 ? pidx[canon[s.parent[c]]] : -1;
+    P.blk_resident[i] = res_of(c);
+  }
+  std::vector<int64_t> sub(nbc);
+  for (int32_t i = 0; i < nbc; ++i) {  // parents come first in pre-order
+    const int32_t p = P.blk_parent[i];
+    P.blk_depth[i] = p < 0 ? 1 : P.blk_depth[p] + 1;
+    sub[i] = P.blk_len[i];
+  }
+  for (int32_t i = nbc - 1; i >= 0; --i)
+    if (P.blk_parent[i] >= 0) sub[P.blk_parent[i]] += sub[i];
+  int64_t tot = 0;
+  for (int32_t i = 0; i < nbc; ++i) {
+    if (P.blk_parent[i] < 0 && sub[i] > max_row)
+      return fail(TREE_ERR_ROW_TOO_LONG, "row of %lld tokens > %d", (long long)sub[i], max_row);
+    tot += P.blk_len[i];
+  }
+  if (tot > INT32_MAX / 2) return fail(TREE_ERR_INVALID_ARG, "%lld tokens: too many", (long long)tot);
+  P.n_tot = (int32_t)tot;
+  tot = 0;
+  for (int32_t i = 0; i < nbc; ++i) {
+    P.blk_start[i] = (int32_t)tot;
+    tot += P.blk_len[i];
+    const int32_t p = P.blk_parent[i];
+    P.blk_pos0[i] = p < 0 ? 0 : P.blk_pos0[p] + P.blk_len[p];
+    P.blk_send[i] = P.blk_start[i] + (int32_t)sub[i];
+  }
+  // ---- resident tokens lead the packed row
+  int32_t n_res = 0;
+  bool fwd_seen = false;
+  for (int32_t i = 0; i < nbc; ++i) {
+    if (P.blk_resident[i]) {
+      if (fwd_seen)
+        return fail(TREE_ERR_INVALID_ARG, "resident block %d follows a forward block in packed order", i);
+      n_res += P.blk_len[i];
+    } else {
+      fwd_seen = true;
+    }
+  }
+  if (n_res == P.n_tot) return fail(TREE_ERR_INVALID_ARG, "no forward tokens");
+  P.n_res = n_res;
+
+  // ---- per-token tables
+  const int32_t n_kvt = (P.n_tot + kTile - 1) / kTile;
+  P.pos.assign(P.n_tot, 0);
+  P.send.assign((size_t)n_kvt * kTile, 0);
+  int32_t maxpos = 0;
+  for (int32_t i = 0; i < nbc; ++i) {
+    for (int32_t t = 0; t < P.blk_len[i]; ++t) {
+      P.pos[P.blk_start[i] + t] = P.blk_pos0[i] + t;
+      P.send[P.blk_start[i] + t] = P.blk_send[i];
+    }
+    maxpos = std::max(maxpos, P.blk_pos0[i] + P.blk_len[i]);
+  }
+  P.max_pos = maxpos;
+  P.pairs = 0;
+  for (int32_t t = P.n_res; t < P.n_tot; ++t) P.pairs += (int64_t)P.pos[t] + 1;
+
+  // per key tile: smallest and largest subtree end (padding keys count as 0)
+  std::vector<int32_t> kt_min(n_kvt), kt_max(n_kvt);
+  for (int32_t kt = 0; kt < n_kvt; ++kt) {
+    int32_t mn = INT32_MAX, mx = INT32_MIN;
+    for (int32_t j = kt * kTile; j < (kt + 1) * kTile; ++j) {
+      mn = std::min(mn, P.send[j]);
+      mx = std::max(mx, P.send[j]);
+    }
+    kt_min[kt] = mn;
+    kt_max[kt] = mx;
+  }
+
+  // ---- chunks, query tiles, tile lists
+  const int32_t n_fwd = P.n_tot - P.n_res;
+  P.n_chunks = (n_fwd + max_fwd - 1) / max_fwd;
+  for (int32_t c = 0; c < P.n_chunks; ++c) {
+    const int32_t q0 = P.n_res + c * max_fwd, q1 = std::min(q0 + max_fwd, P.n_tot);
+    P.chunk_q0.push_back(q0);
+    P.chunk_q1.push_back(q1);
+    P.chunk_t0.push_back((int32_t)P.qt_row0.size());
+    int64_t cp = 0;
+    for (int32_t t = q0; t < q1; ++t) cp += (int64_t)P.pos[t] + 1;
+    P.chunk_pairs.push_back(cp);
+    const int32_t e_begin = (int32_t)P.ent.size();
+    for (int32_t i0 = q0; i0 < q1; i0 += kTile) {
+      const int32_t i1 = std::min(i0 + kTile, q1);
+      P.qt_row0.push_back(i0);
+      P.qt_row1.push_back(i1);
+      P.qt_ent0.push_back((int32_t)P.ent.size());
+      const int32_t last = (i1 - 1) / kTile;
+      for (int32_t kt = 0; kt <= last; ++kt) {
+        const int32_t j0 = kt * kTile, j1 = j0 + kTile;
+        // some query sees some key: a key j < i1 whose subtree reaches past i0
+        bool any;
+        if (j1 <= i1) {
+          any = kt_max[kt] > i0;
+        } else {
+          any = false;
+          for (int32_t j = j0; j < i1 && !any; ++j) any = P.send[j] > i0;
+        }
+        if (!any) continue;
+        // every query sees every key: the tile is whole, lies before the
+        // first query, and every key's subtree reaches past the last query
+        const bool full = (j1 <= P.n_tot) && (j1 - 1 <= i0) && (i1 - 1 < kt_min[kt]);
+        P.ent.push_back((kt << 1) | (full ? 0 : 1));
+      }
+      P.qt_ent1.push_back((int32_t)P.ent.size());
+    }
+    P.chunk_t1.push_back((int32_t)P.qt_row0.size());
+    P.chunk_nent.push_back((int32_t)P.ent.size() - e_begin);
+    // longest-first order of the chunk's tiles; equal work keeps tile order
+    std::vector<int32_t> ord(P.chunk_t1[c] - P.chunk_t0[c]);
+    std::iota(ord.begin(), ord.end(), P.chunk_t0[c]);
+    std::stable_sort(ord.begin(), ord.end(), [&](int32_t a, int32_t b) {
+      return P.qt_ent1[a] - P.qt_ent0[a] > P.qt_ent1[b] - P.qt_ent0[b];
+    });
+    P.qt_order.insert(P.qt_order.end(), ord.begin(), ord.end());
+  }
+
+  // ---- readout slots: last token of every leaf, packed order
+  std::vector<char> has_child(nbc, 0);
+  for (int32_t i = 0; i < nbc; ++i)
+    if (P.blk_parent[i] >= 0) has_child[P.blk_parent[i]] = 1;
+  for (int32_t i = 0; i < nbc; ++i) {
+    if (has_child[i]) continue;
+    P.blk_slot[i] = (int32_t)P.slot_tok.size();
+    P.slot_tok.push_back(P.blk_start[i] + P.blk_len[i] - 1);
+  }
+  P.n_questions = s.n_questions;
+  for (int32_t q = 0; q < s.n_questions; ++q) {
+    const int32_t l[2] = {s.leaf1[q], s.leaf2[q]};
+    for (int32_t o = 0; o < 2; ++o) {
+      if (l[o] < 0 || l[o] >= nb) return fail(TREE_ERR_INVALID_ARG, "question %d: block %d out of range", q, l[o]);
+      const int32_t slot = P.blk_slot[P.block_map[l[o]]];
+      if (slot < 0) return fail(TREE_ERR_INVALID_ARG, "question %d: block %d is not a leaf", q, l[o]);
+      (o == 0 ? P.r1 : P.r2).push_back(slot);
+    }
+  }
+
+  // ---- device image
+  size_t w = 16;  // header words
+  P.off_pos = w;
+  w = align4(w + P.pos.size());
+  P.off_send = w;
+  w = align4(w + P.send.size());
+  P.off_qtile = w;
+  w = align4(w + 4 * P.qt_row0.size());
+  P.off_ent = w;
+  w = align4(w + P.ent.size());
+  P.off_order = w;
+  w = align4(w + P.qt_order.size());
+  P.off_chunk = w;
+  w = align4(w + 4 * (size_t)P.n_chunks);
+  P.off_slot_tok = w;
+  w = align4(w + P.slot_tok.size());
+  P.off_r1 = w;
+  w = align4(w + P.r1.size());
+  P.off_r2 = w;
+  w = align4(w + P.r2.size());
+  P.image.assign(w, 0);
+  int32_t *im = P.image.data();
+  im[0] = 0x4C505254;  // "TRPL"
+  im[1] = P.n_tot;
+  im[2] = P.n_res;
+  im[3] = P.n_chunks;
+  im[4] = (int32_t)P.qt_row0.size();
+  im[5] = (int32_t)P.ent.size();
+  im[6] = (int32_t)P.slot_tok.size();
+  im[7] = P.n_questions;
+  std::copy(P.pos.begin(), P.pos.end(), im + P.off_pos);
+  std::copy(P.send.begin(), P.send.end(), im + P.off_send);
+  for (size_t t = 0; t < P.qt_row0.size(); ++t) {
+    int32_t *r = im + P.off_qtile + 4 * t;
+    r[0] = P.qt_row0[t];
+    r[1] = P.qt_row1[t];
+    r[2] = P.qt_ent0[t];
+    r[3] = P.qt_ent1[t];
+  }
+  std::copy(P.ent.begin(), P.ent.end(), im + P.off_ent);
+  std::copy(P.qt_order.begin(), P.qt_order.end(), im + P.off_order);
+  for (int32_t c = 0; c < P.n_chunks; ++c) {
+    int32_t *r = im + P.off_chunk + 4 * c;
+    r[0] = P.chunk_q0[c];
+    r[1] = P.chunk_q1[c];
+    r[2] = P.chunk_t0[c];
+    r[3] = P.chunk_t1[c];
+  }
+  std::copy(P.slot_tok.begin(), P.slot_tok.end(), im + P.off_slot_tok);
+  std::copy(P.r1.begin(), P.r1.end(), im + P.off_r1);
+  std::copy(P.r2.begin(), P.r2.end(), im + P.off_r2);
+  return TREE_OK;
+}
+
+}  // namespace
+}  // namespace tree
+
+extern "C" {
+
+const char *tree_last_error(void) { return tree::g_err.c_str(); }
+
+int tree_version(void) { return 100; }
+
+int tree_pack_plan(const tree_spec_t *spec, const tree_plan_opts_t *opts, tree_plan_t **out) {
+  if (!spec || !out) return tree::fail(TREE_ERR_INVALID_ARG, "tree_pack_plan: NULL spec or out");
+  *out = nullptr;
+  if (spec->n_blocks <= 0 || !spec->parent || !spec->length)
+    return tree::fail(TREE_ERR_INVALID_ARG, "tree_pack_plan: empty forest or NULL parent/length");
+  if (spec->n_questions < 0 || (spec->n_questions > 0 && (!spec->leaf1 || !spec->leaf2)))
+    return tree::fail(TREE_ERR_INVALID_ARG, "tree_pack_plan: bad question arrays");
+  int32_t max_fwd = 8192, max_depth = 8, max_row = 32768;
+  if (opts) {
+    if (opts->max_fwd) max_fwd = opts->max_fwd;
+    if (opts->max_depth) max_depth = opts->max_depth;
+    if (opts->max_row) max_row = opts->max_row;
+  }
+  if (max_fwd <= 0 || max_fwd % 128 != 0)
+    return tree::fail(TREE_ERR_UNSUPPORTED, "max_fwd %d is not a positive multiple of 128", max_fwd);
+  if (max_depth <= 0 || max_row <= 0) return tree::fail(TREE_ERR_INVALID_ARG, "bad limits");
+  auto *pl = new (std::nothrow) tree_plan;
+  if (!pl) return tree::fail(TREE_ERR_INVALID_ARG, "out of host memory");
+  const int rc = tree::build(*spec, max_fwd, max_depth, max_row, pl->p);
+  if (rc != TREE_OK) {
+    delete pl;
+    return rc;
+  }
+  *out = pl;
+  return TREE_OK;
+}
+
+int tree_plan_free(tree_plan_t *plan) {
+  delete plan;
+  return TREE_OK;
+}
+
+int tree_plan_query(const tree_plan_t *plan, tree_plan_info_t *info) {
+  if (!plan || !info) return tree::fail(TREE_ERR_INVALID_ARG, "tree_plan_query: NULL argument");
+  const tree::Plan &P = plan->p;
+  std::memset(info, 0, sizeof *info);
+  info->n_input_blocks = P.n_input_blocks;
+  info->n_blocks = P.n_blocks;
+  info->n_tot = P.n_tot;
+  info->n_res = P.n_res;
+  info->n_fwd = P.n_tot - P.n_res;
+  info->n_chunks = P.n_chunks;
+  info->n_qtiles = (int32_t)P.qt_row0.size();
+  info->n_entries = (int32_t)P.ent.size();
+  info->n_slots = (int32_t)P.slot_tok.size();
+  info->n_questions = P.n_questions;
+  info->max_fwd = P.max_fwd;
+  info->bm = P.bm;
+  info->bn = P.bn;
+  info->max_pos = P.max_pos;
+  info->pairs = P.pairs;
+  info->dev_bytes = P.image.size() * sizeof(int32_t);
+  info->off_pos = P.off_pos * 4;
+  info->off_send = P.off_send * 4;
+  info->off_qtile = P.off_qtile * 4;
+  info->off_ent = P.off_ent * 4;
+  info->off_order = P.off_order * 4;
+  info->off_chunk = P.off_chunk * 4;
+  info->off_slot_tok = P.off_slot_tok * 4;
+  info->off_r1 = P.off_r1 * 4;
+  info->off_r2 = P.off_r2 * 4;
+  return TREE_OK;
+}
+
+int tree_plan_chunk(const tree_plan_t *plan, int32_t chunk, tree_chunk_info_t *info) {
+  if (!plan || !info) return tree::fail(TREE_ERR_INVALID_ARG, "tree_plan_chunk: NULL argument");
+  const tree::Plan &P = plan->p;
+  if (chunk < 0 || chunk >= P.n_chunks)
+    return tree::fail(TREE_ERR_INVALID_ARG, "chunk %d out of range [0, %d)", chunk, P.n_chunks);
+  info->q0 = P.chunk_q0[chunk];
+  info->q1 = P.chunk_q1[chunk];
+  info->t0 = P.chunk_t0[chunk];
+  info->t1 = P.chunk_t1[chunk];
+  info->pairs = P.chunk_pairs[chunk];
+  info->n_entries = P.chunk_nent[chunk];
+  return TREE_OK;
+}
+
+int tree_plan_tables(const tree_plan_t *plan, tree_plan_host_view_t *v) {
+  if (!plan || !v) return tree::fail(TREE_ERR_INVALID_ARG, "tree_plan_tables: NULL argument");
+  const tree::Plan &P = plan->p;
+  v->block_map = P.block_map.data();
+  v->blk_start = P.blk_start.data();
+  v->blk_len = P.blk_len.data();
+  v->blk_parent = P.blk_parent.data();
+  v->blk_depth = P.blk_depth.data();
+  v->blk_pos0 = P.blk_pos0.data();
+  v->blk_send = P.blk_send.data();
+  v->blk_resident = P.blk_resident.data();
+  v->blk_slot = P.blk_slot.data();
+  v->pos = P.pos.data();
+  v->send = P.send.data();
+  v->chunk_q0 = P.chunk_q0.data();
+  v->chunk_q1 = P.chunk_q1.data();
+  v->chunk_t0 = P.chunk_t0.data();
+  v->chunk_t1 = P.chunk_t1.data();
+  v->qt_row0 = P.qt_row0.data();
+  v->qt_row1 = P.qt_row1.data();
+  v->qt_ent0 = P.qt_ent0.data();
+  v->qt_ent1 = P.qt_ent1.data();
+  v->ent = P.ent.data();
+  v->qt_order = P.qt_order.data();
+  v->slot_tok = P.slot_tok.data();
+  v->r1 = P.r1.data();
+  v->r2 = P.r2.data();
+  v->image = P.image.data();
+  v->image_bytes = P.image.size() * sizeof(int32_t);
+  return TREE_OK;
+}
+
+int tree_plan_upload(const tree_plan_t *plan, void *dev_buf, size_t bytes, tree_stream_t stream) {
+  if (!plan || !dev_buf) return tree::fail(TREE_ERR_INVALID_ARG, "tree_plan_upload: NULL argument");
+  const size_t need = plan->p.image.size() * sizeof(int32_t);
+  if (bytes < need)
+    return tree::fail(TREE_ERR_INVALID_ARG, "tree_plan_upload: buffer of %zu bytes < %zu", bytes, need);
+  if (reinterpret_cast<uintptr_t>(dev_buf) % 16)
+    return tree::fail(TREE_ERR_UNSUPPORTED, "tree_plan_upload: device buffer not 16-byte aligned");
+  const cudaError_t e = cudaMemcpyAsync(dev_buf, plan->p.image.data(), need, cudaMemcpyHostToDevice,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return tree::fail(TREE_ERR_CUDA, "tree_plan_upload: %s", cudaGetErrorString(e));
+  return TREE_OK;
+}
+
+}  // extern "C"

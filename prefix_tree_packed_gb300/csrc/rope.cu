@@ -1,0 +1,122 @@
+// tree_rope: rotary embedding at tree positions, in place on Q and K.
+//
+// The rotary position of a token is its position in its own prompt (basal-rs
+// Architecture page, "03 / Packing: Attention over tree blocks"); the planner's
+// pos table holds it.  Pairs (i, i + d/2) are rotated by pos * theta^(-2i/d)
+// (the Llama "rotate half" layout):
+//
+//   y_i       = x_i cos - x_{i+d/2} sin
+//   y_{i+d/2} = x_{i+d/2} cos + x_i sin
+//
+// cos/sin come from an f32 table [max_pos][d/2][2] that the host fills in
+// double precision (tree_rope_table), the table form of the AstrAI inference
+// page ("Rotary Embedding Backend"); evaluating pos * inv_freq in f32 instead
+// would put ~2e-3 rad of error on the angle at position 32k.
+//
+// The kernel is a streaming pass over the chunk's Q rows and K rows: one
+// thread rotates 8 pairs of one head (two 16-byte loads and stores), threads of
+// a warp cover consecutive pairs and heads of a row, so every access is a full
+// 32-byte sector; the table stays in L1/L2.  Grid-stride over a grid of
+// (SMs x 8) blocks.
+
+#include <cmath>
+
+#include "common.cuh"
+
+namespace tree {
+namespace {
+
+__device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float4 *cs) {
+  // lo holds x_i .. x_{i+7}, hi holds x_{i+d/2} .. x_{i+d/2+7}; cs: 8 x {cos, sin}
+  __half2 *l = reinterpret_cast<__half2 *>(&lo);
+  __half2 *h = reinterpret_cast<__half2 *>(&hi);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const float4 c = __ldg(cs + p);  // {cos_a, sin_a, cos_b, sin_b} for pairs 2p, 2p+1
+    const float2 x1 = __half22float2(l[p]);
+    const float2 x2 = __half22float2(h[p]);
+    const float y1a = x1.x * c.x - x2.x * c.y;
+    const float y2a = x2.x * c.x + x1.x * c.y;
+    const float y1b = x1.y * c.z - x2.y * c.w;
+    const float y2b = x2.y * c.z + x1.y * c.w;
+    l[p] = __floats2half2_rn(y1a, y1b);
+    h[p] = __floats2half2_rn(y2a, y2b);
+  }
+}
+
+__global__ void __launch_bounds__(256) rope_kernel(__half *__restrict__ q, __half *__restrict__ k,
+                                                   const int32_t *__restrict__ pos, int32_t q0, int32_t nrows,
+                                                   int hq, int hkv, int d, const float *__restrict__ cos_sin,
+                                                   int32_t max_pos) {
+  const int per_head = d / 16;  // threads per head: 8 pairs each
+  const int64_t q_items = (int64_t)nrows * hq * per_head;
+  const int64_t total = q_items + (int64_t)nrows * hkv * per_head;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    __half *base;
+    int64_t r, rem;
+    if (t < q_items) {
+      r = t / (hq * per_head);
+      rem = t - r * (hq * per_head);
+      base = q + (size_t)r * hq * d;
+    } else {
+      const int64_t u = t - q_items;
+      r = u / (hkv * per_head);
+      rem = u - r * (hkv * per_head);
+      base = k + (size_t)(q0 + r) * hkv * d;
+    }
+    const int head = (int)(rem / per_head);
+    const int c = (int)(rem - (int64_t)head * per_head);
+    const int p = pos[q0 + r];
+    if (p < 0 || p >= max_pos) continue;  // the host checked the table against the plan
+    __half *x = base + (size_t)head * d + 8 * c;
+    uint4 lo = *reinterpret_cast<const uint4 *>(x);
+    uint4 hi = *reinterpret_cast<const uint4 *>(x + d / 2);
+    const float4 *cs = reinterpret_cast<const float4 *>(cos_sin + ((size_t)p * (d / 2) + 8 * c) * 2);
+    rotate8(lo, hi, cs);
+    *reinterpret_cast<uint4 *>(x) = lo;
+    *reinterpret_cast<uint4 *>(x + d / 2) = hi;
+  }
+}
+
+}  // namespace
+}  // namespace tree
+
+extern "C" TREE_API int tree_rope_table(float *host_out, int32_t max_pos, int32_t d, double theta) {
+  using namespace tree;
+  if (!host_out || max_pos <= 0 || d <= 0 || d % 2 || !(theta > 0))
+    return fail(TREE_ERR_INVALID_ARG, "tree_rope_table: max_pos %d, d %d, theta %g", max_pos, d, theta);
+  const int h = d / 2;
+  for (int32_t p = 0; p < max_pos; ++p)
+    for (int i = 0; i < h; ++i) {
+      const double a = (double)p * std::pow(theta, -2.0 * i / d);
+      host_out[((size_t)p * h + i) * 2 + 0] = (float)std::cos(a);
+      host_out[((size_t)p * h + i) * 2 + 1] = (float)std::sin(a);
+    }
+  return TREE_OK;
+}
+
+extern "C" TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev, int32_t chunk, void *q,
+                                  void *k, int32_t hq, int32_t hkv, int32_t d, const float *cos_sin,
+                                  int32_t max_pos, tree_stream_t stream) {
+  using namespace tree;
+  if (!plan || !plan_dev || !q || !k || !cos_sin) return fail(TREE_ERR_INVALID_ARG, "tree_rope: NULL argument");
+  const Plan &P = plan->p;
+  if (chunk < 0 || chunk >= P.n_chunks) return fail(TREE_ERR_INVALID_ARG, "tree_rope: chunk %d out of range", chunk);
+  if (hq <= 0 || hkv <= 0 || d <= 0 || d % 16 || d > 256)
+    return fail(TREE_ERR_UNSUPPORTED, "tree_rope: hq %d hkv %d d %d (d must be a multiple of 16, <= 256)", hq,
+                hkv, d);
+  if (max_pos < P.max_pos)
+    return fail(TREE_ERR_INVALID_ARG, "tree_rope: table has %d positions, plan needs %d", max_pos, P.max_pos);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(cos_sin) || !aligned16(plan_dev))
+    return fail(TREE_ERR_UNSUPPORTED, "tree_rope: pointers must be 16-byte aligned");
+  const int32_t q0 = P.chunk_q0[chunk], n = P.chunk_q1[chunk] - q0;
+  const int64_t total = (int64_t)n * (hq + hkv) * (d / 16);
+  const int threads = 256;
+  const int64_t need = (total + threads - 1) / threads;
+  const int blocks = (int)std::min<int64_t>(need, (int64_t)sm_count() * 8);
+  const int32_t *pos = reinterpret_cast<const int32_t *>(plan_dev) + P.off_pos;
+  rope_kernel<<<blocks, threads, 0, as_stream(stream)>>>(reinterpret_cast<__half *>(q), reinterpret_cast<__half *>(k),
+                                                         pos, q0, n, hq, hkv, d, cos_sin, max_pos);
+  return launch_status("tree_rope");
+}

@@ -1,0 +1,133 @@
+"""The C-ABI library loads, exports every declared symbol, and its planner
+matches the oracle planner table for table, bit for bit (CPU only)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import plan as oplan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import prefix_tree_packed_gb300 as lib
+    return lib
+
+
+def test_exports_every_declared_symbol(lib):
+    with open(os.path.join(ROOT, "include", "tree_attn.h")) as f:
+        hdr = f.read()
+    declared = set(re.findall(r"^TREE_API\s+[\w\s\*]*?\*?\s*(\w+)\s*\(", hdr, flags=re.M))
+    assert declared == set(lib.EXPORTS)
+    for name in declared:
+        getattr(lib._lib, name)          # raises if the shared object lacks it
+    assert lib.version() >= 100
+
+
+def _compare(p_or: oplan.Plan, q_or: dict, pl):
+    t = pl.tables()
+    i = pl.info
+    assert (i.n_blocks, i.n_tot, i.n_res, i.n_chunks, i.n_slots) == (
+        p_or.n_blocks, p_or.n_tot, p_or.n_res, p_or.n_chunks, p_or.n_slots)
+    assert i.pairs == p_or.pairs
+    pairs = [("block_map", p_or.block_map), ("blk_start", p_or.blk_start), ("blk_len", p_or.blk_len),
+             ("blk_parent", p_or.blk_parent), ("blk_depth", p_or.blk_depth), ("blk_pos0", p_or.blk_pos0),
+             ("blk_send", p_or.blk_send), ("blk_resident", p_or.blk_resident), ("blk_slot", p_or.blk_slot),
+             ("pos", p_or.pos), ("send", p_or.send), ("chunk_q0", p_or.chunk_q0), ("chunk_q1", p_or.chunk_q1),
+             ("chunk_t0", p_or.chunk_t0), ("chunk_t1", p_or.chunk_t1), ("qt_row0", p_or.qt_row0),
+             ("qt_row1", p_or.qt_row1), ("qt_ent0", p_or.qt_ent0), ("qt_ent1", p_or.qt_ent1),
+             ("ent", p_or.ent), ("qt_order", p_or.qt_order), ("slot_tok", p_or.slot_tok)]
+    if q_or:
+        pairs += [("r1", q_or["r1"]), ("r2", q_or["r2"])]
+    for name, ref in pairs:
+        assert np.array_equal(t[name].astype(np.int64), np.asarray(ref, np.int64)), name
+    assert i.max_pos == int(p_or.pos.max()) + 1
+    for c in range(i.n_chunks):
+        ci = pl.chunk(c)
+        q0, q1 = int(p_or.chunk_q0[c]), int(p_or.chunk_q1[c])
+        assert ci.pairs == int((p_or.pos[q0:q1] + 1).sum())
+    # the device image holds the same arrays at the advertised offsets
+    img = t["image"].view(np.int32)
+    assert np.array_equal(img[i.off_pos // 4: i.off_pos // 4 + i.n_tot], t["pos"])
+    assert np.array_equal(img[i.off_send // 4: i.off_send // 4 + len(t["send"])], t["send"])
+    qt = img[i.off_qtile // 4: i.off_qtile // 4 + 4 * i.n_qtiles].reshape(-1, 4)
+    assert np.array_equal(qt[:, 0], t["qt_row0"]) and np.array_equal(qt[:, 3], t["qt_ent1"])
+    assert np.array_equal(img[i.off_ent // 4: i.off_ent // 4 + i.n_entries], t["ent"])
+    assert np.array_equal(img[i.off_order // 4: i.off_order // 4 + i.n_qtiles], t["qt_order"])
+    for off in (i.off_pos, i.off_send, i.off_qtile, i.off_ent, i.off_order, i.off_chunk, i.off_slot_tok,
+                i.off_r1, i.off_r2):
+        assert off % 16 == 0
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_workloads_match_oracle(lib, n):
+    w = synth.workload(n)
+    f = w.forest
+    kw = dict(leaf1=w.leaf1, leaf2=w.leaf2) if w.leaf1 is not None else {}
+    p_or, q_or = oplan.plan_forest(f, max_fwd=w.max_fwd, **kw)
+    pl = lib.Plan.from_forest(f, max_fwd=w.max_fwd, **kw)
+    _compare(p_or, q_or, pl)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_forests_match_oracle(lib, seed):
+    rng = np.random.default_rng(1000 + seed)
+    f = synth.random_forest(rng, n_roots=int(rng.integers(1, 5)), max_blocks=int(rng.integers(2, 40)),
+                            max_len=int(rng.integers(1, 300)), dup_prob=0.25, resident_root=bool(seed % 4 == 0))
+    max_fwd = int(rng.choice([128, 256, 8192]))
+    try:
+        p_or, _ = oplan.plan_forest(f, max_fwd=max_fwd)
+    except oplan.PlanError as e:
+        with pytest.raises(lib.TreeError) as ei:
+            lib.Plan.from_forest(f, max_fwd=max_fwd)
+        assert ei.value.code == e.code
+        return
+    pl = lib.Plan.from_forest(f, max_fwd=max_fwd)
+    _compare(p_or, {}, pl)
+
+
+def test_error_codes_match_oracle(lib):
+    cases = [
+        ([-1] + list(range(8)), [1] * 9, None, {}),           # depth 9
+        ([-1], [32769], None, {}),                             # row too long
+        ([-1, 0, 0], [20000, 10000, 3000], None, {}),          # row too long across blocks
+        ([-1, 2, 1], [1, 1, 1], None, {}),                     # cycle
+        ([-1, 5], [1, 1], None, {}),                           # orphan
+        ([-1, 0], [1, 0], None, {}),                           # empty block
+        ([-1, 0], [1, -3], None, {}),                          # negative length
+        ([-1, -1], [4, 4], [0, 1], {}),                        # resident after a forward block
+        ([-1], [4], [1], {}),                                  # nothing to compute
+        ([-1], [4], None, {"max_fwd": 100}),                   # chunk not a multiple of 128
+    ]
+    for par, ln, res, kw in cases:
+        with pytest.raises(oplan.PlanError) as eo:
+            oplan.make_plan(par, ln, np.zeros(len(par), np.uint64), res or [0] * len(par), **kw)
+        with pytest.raises(lib.TreeError) as ec:
+            lib.Plan(par, ln, None, res, **kw)
+        assert ec.value.code == eo.value.code, (par, ln, res, kw)
+        assert str(ec.value)
+
+
+def test_question_errors(lib):
+    # a question naming a non-leaf block
+    with pytest.raises(lib.TreeError) as e:
+        lib.Plan([-1, 0, 0], [4, 2, 2], leaf1=[0], leaf2=[1])
+    assert e.value.code == lib.TREE_ERR_INVALID_ARG
+    with pytest.raises(lib.TreeError):
+        lib.Plan([-1, 0, 0], [4, 2, 2], leaf1=[1], leaf2=[7])
+
+
+def test_rope_table_matches_double_precision(lib):
+    tab = lib.rope_table(40000, 128, 500000.0)
+    from oracle import rope
+    a = rope.angles(np.arange(40000), 128, 500000.0)
+    # both evaluate in double and round once to float: at most one float ulp apart
+    # (the two libraries' pow/cos/sin may differ in the last double bit)
+    np.testing.assert_array_max_ulp(tab[..., 0], np.cos(a).astype(np.float32), maxulp=1)
+    np.testing.assert_array_max_ulp(tab[..., 1], np.sin(a).astype(np.float32), maxulp=1)
+    with pytest.raises(lib.TreeError):
+        lib.rope_table(0, 64, 1e4)

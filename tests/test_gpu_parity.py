@@ -1,0 +1,294 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Tolerances:
+  plan tables, readout slots, choices      bit-exact
+  RoPE outputs (f16)                       within 1 f16 ulp, almost all equal
+  attention outputs (f16)                  max-abs 2e-3 against the float64 oracle
+  LSE (f32)                                max-abs 1e-3 (natural log units)
+  decision probabilities (f32)             max-abs 1e-5
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import attention as oatt
+from oracle import plan as oplan
+from oracle import readout as ordo
+from oracle import rope as orope
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ATOL_O = 2e-3
+ATOL_P = 1e-5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import prefix_tree_packed_gb300 as lib
+    return lib
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+class Run:
+    """A plan on the device plus helpers to call the library."""
+
+    def __init__(self, lib, forest, max_fwd=8192, leaf1=None, leaf2=None):
+        self.lib = lib
+        kw = dict(leaf1=leaf1, leaf2=leaf2) if leaf1 is not None else {}
+        self.plan = lib.Plan.from_forest(forest, max_fwd=max_fwd, **kw)
+        self.oplan, self.oq = oplan.plan_forest(forest, max_fwd=max_fwd, **kw)
+        i = self.plan.info
+        self.dev = torch.empty(i.dev_bytes, dtype=torch.uint8, device="cuda")
+        self.plan.upload(self.dev, i.dev_bytes, torch.cuda.current_stream())
+
+    def rope(self, q, k, hq, hkv, d, theta, chunk):
+        i = self.plan.info
+        tab = _dev(self.lib.rope_table(i.max_pos, d, theta))
+        self.lib.tree_rope(self.plan, self.dev, chunk, q, k, hq, hkv, d, tab, i.max_pos,
+                           torch.cuda.current_stream())
+
+    def attn(self, q, k, v, hq, hkv, d, chunk, lse=None, status=None):
+        ci = self.plan.chunk(chunk)
+        o = torch.empty((ci.q1 - ci.q0, hq, d), dtype=torch.float16, device="cuda")
+        self.lib.tree_attn_fwd(self.plan, self.dev, chunk, q, k, v, o, lse, hq, hkv, d,
+                               status=status, stream=torch.cuda.current_stream())
+        return o
+
+
+def _f16_ulp(x):
+    x = np.abs(x.astype(np.float32))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -14)))
+    return 2.0 ** (e - 10)
+
+
+# ---------------------------------------------------------------- readout
+
+def _check_readout(lib, logits, r1, r2, n, T, stride):
+    nq = len(r1)
+    pc = torch.full((nq, stride), -7.0, device="cuda")
+    pa = torch.full((nq, stride), -7.0, device="cuda")
+    ch = torch.full((nq,), -9, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.readout_decide(_dev(logits), stride, _dev(np.int32(r1)), _dev(np.int32(r2)), _dev(np.int32(n)),
+                       _dev(np.float32(T)), nq, pc, pa, ch, st, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_pc, ref_pa, _ = ordo.decide(logits, r1, r2, n, T, stride)
+    assert np.abs(pc.cpu().numpy() - ref_pc).max() <= ATOL_P
+    assert np.abs(pa.cpu().numpy() - ref_pa).max() <= ATOL_P
+    got = ch.cpu().numpy()
+    want = ordo.choice_f32(logits, r1, r2, n)
+    diff = np.nonzero(got != want)[0]
+    # an f32 near-tie may legitimately resolve either way; both must be maxima of p
+    for q in diff:
+        top = np.sort(ref_pa[q])[::-1]
+        assert top[0] - top[1] < 1e-6 and abs(ref_pa[q, got[q]] - top[0]) < 1e-6
+    assert len(diff) <= max(1, nq // 10000)
+
+
+def test_readout_worked_example(lib):
+    logits = np.array([[3.2, 0.9, -0.4], [0.4, 1.1, 2.6]], np.float32)
+    _check_readout(lib, logits, [0], [1], [3], [1.0], 3)
+
+
+def test_readout_workload_one_and_two(lib):
+    for n in (1, 2):
+        w = synth.workload(n)
+        p, q = oplan.plan_forest(w.forest, leaf1=w.leaf1, leaf2=w.leaf2)
+        logits = synth.draw_logits(p.n_slots, w.letter_stride, w.logit_sigma, w.seed)
+        _check_readout(lib, logits, q["r1"], q["r2"], w.n_letters, w.temperature, w.letter_stride)
+
+
+def test_readout_65536_questions(lib):
+    b = synth.draw_readout_batch()
+    _check_readout(lib, b["logits"], b["r1"], b["r2"], b["n_letters"], b["temperature"], b["stride"])
+
+
+@pytest.mark.parametrize("stride,nmax", [(1, 1), (16, 16), (17, 17), (40, 33), (255, 255), (300, 255)])
+def test_readout_sizes(lib, stride, nmax):
+    rng = np.random.default_rng(stride)
+    nq = 333
+    logits = (rng.standard_normal((2 * nq, stride)) * 3).astype(np.float32)
+    n = rng.integers(1, nmax + 1, nq)
+    n[0] = nmax
+    T = rng.choice([0.5, 1.0, 2.0], nq)
+    _check_readout(lib, logits, 2 * np.arange(nq), 2 * np.arange(nq) + 1, n, T, stride)
+
+
+def test_readout_bad_arguments_flagged(lib):
+    logits = np.zeros((4, 6), np.float32)
+    pc = torch.full((2, 6), -7.0, device="cuda")
+    ch = torch.full((2,), -9, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.readout_decide(_dev(logits), 6, _dev(np.int32([0, 2])), _dev(np.int32([1, 3])), _dev(np.int32([3, 7])),
+                       _dev(np.float32([1.0, 1.0])), 2, pc, None, ch, st, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert int(st.item()) == lib.TREE_ERR_INVALID_ARG
+    assert ch.cpu().tolist() == [0, -1]           # equal logits: lowest index; bad question: -1
+    assert np.all(pc.cpu().numpy()[1] == 0)
+    st.zero_()
+    lib.readout_decide(_dev(logits), 6, _dev(np.int32([0])), _dev(np.int32([1])), _dev(np.int32([3])),
+                       _dev(np.float32([0.0])), 1, pc, None, ch, st, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert int(st.item()) == lib.TREE_ERR_INVALID_ARG
+    lib.readout_decide(0, 6, 0, 0, 0, 0, 0, 0)    # no questions: no-op
+    with pytest.raises(lib.TreeError):
+        lib.readout_decide(_dev(logits), 0, 0, 0, 0, 0, 1, pc)
+
+
+# ---------------------------------------------------------------- RoPE
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_rope_workloads(lib, n):
+    w = synth.workload(n)
+    r = Run(lib, w.forest, w.max_fwd)
+    p = r.oplan
+    q, k, v = synth.draw_qkv(p.n_fwd, p.n_tot, w.hq, w.hkv, w.d, w.seed)
+    qr_ref, kr_ref = orope.apply_plan(p, q, k, w.theta)
+    kd = _dev(k)
+    qr = np.empty_like(q)
+    for c in range(p.n_chunks):
+        ci = r.plan.chunk(c)
+        qd = _dev(q[ci.q0 - p.n_res: ci.q1 - p.n_res])
+        r.rope(qd, kd, w.hq, w.hkv, w.d, w.theta, c)
+        torch.cuda.synchronize()
+        qr[ci.q0 - p.n_res: ci.q1 - p.n_res] = qd.cpu().numpy()
+    kr = kd.cpu().numpy()
+    for got, ref, x in ((qr, qr_ref, q), (kr, kr_ref, k)):
+        d = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+        # the kernel evaluates x1*cos - x2*sin in f32 from an f32 table: before the
+        # final f16 rounding it is within a few f32 ulps of (|x1| + |x2|) of the
+        # exact value, so after rounding it may differ by one f16 ulp plus that
+        xa = np.abs(x.astype(np.float64))
+        h = x.shape[-1] // 2
+        partner = np.concatenate([xa[..., h:], xa[..., :h]], axis=-1)
+        bound = _f16_ulp(ref) + 2.0 ** -20 * (xa + partner)
+        assert np.all(d <= bound), f"worst excess {(d - bound).max()}"
+        assert (d > 0).mean() < 1e-3
+    assert np.array_equal(kr[: p.n_res], k[: p.n_res])     # resident rows untouched
+
+
+# ---------------------------------------------------------------- attention
+
+def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per_chunk=48, lse=True):
+    r = Run(lib, forest, max_fwd)
+    p = r.oplan
+    q, k, v = synth.draw_qkv(p.n_fwd, p.n_tot, hq, hkv, d, seed)
+    qr, kr = orope.apply_plan(p, q, k, 500000.0)     # oracle RoPE output is the attention input
+    kd, vd = _dev(kr), _dev(v)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs, lses = [], []
+    for c in range(p.n_chunks):
+        ci = r.plan.chunk(c)
+        qd = _dev(qr[ci.q0 - p.n_res: ci.q1 - p.n_res])
+        ld = torch.full((ci.q1 - ci.q0, hq), np.nan, device="cuda") if lse else None
+        o = r.attn(qd, kd, vd, hq, hkv, d, c, lse=ld, status=st)
+        torch.cuda.synchronize()
+        outs.append(o.float().cpu().numpy())
+        if lse:
+            lses.append(ld.cpu().numpy())
+    assert int(st.item()) == 0
+    got = np.concatenate(outs)
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(seed + 7)
+    if full:
+        ref = oatt.attend_paths(p, qr, kr, v)
+        err = np.abs(got - ref)
+        assert err.max() <= ATOL_O, f"max err {err.max()} at {np.unravel_index(err.argmax(), err.shape)}"
+        rows = rng.choice(p.n_fwd, min(p.n_fwd, 64), replace=False)
+    else:
+        rows = []
+        for c in range(p.n_chunks):
+            a, b = int(p.chunk_q0[c]) - p.n_res, int(p.chunk_q1[c]) - p.n_res
+            rows += [a, b - 1] + list(rng.integers(a, b, rows_per_chunk - 2))
+        rows = np.array(rows)
+        ref = oatt.attend_rows(p, qr, kr, v, rows)
+        err = np.abs(got[rows] - ref)
+        assert err.max() <= ATOL_O, f"max err {err.max()}"
+    if lse:
+        lg = np.concatenate(lses)[rows]
+        lr = oatt.lse_rows(p, qr, kr, rows)
+        assert np.abs(lg - lr).max() <= 1e-3
+    return got
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5])
+def test_attention_workloads_full(lib, n):
+    w = synth.workload(n)
+    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=True)
+
+
+def test_attention_long_row_four_chunks_sampled(lib):
+    w = synth.workload(4)
+    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=False, rows_per_chunk=40)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_attention_random_forests(lib, seed):
+    rng = np.random.default_rng(500 + seed)
+    f = synth.random_forest(rng, n_roots=int(rng.integers(1, 4)), max_blocks=int(rng.integers(3, 30)),
+                            max_len=int(rng.integers(1, 200)), dup_prob=0.2, resident_root=bool(seed % 2))
+    try:
+        oplan.plan_forest(f, max_fwd=256)
+    except oplan.PlanError:
+        pytest.skip("forest has no forward tokens")
+    hq, hkv, d = [(4, 4, 64), (8, 2, 128), (4, 1, 64), (6, 3, 128)][seed % 4]
+    _attn_check(lib, f, hq, hkv, d, seed, max_fwd=int(rng.choice([128, 256, 8192])))
+
+
+def test_attention_chunked_equals_unchunked(lib):
+    rng = np.random.default_rng(42)
+    f = synth.random_forest(rng, n_roots=2, max_blocks=20, max_len=150, resident_root=True)
+    a = _attn_check(lib, f, 8, 2, 64, 3, max_fwd=128, lse=False)
+    b = _attn_check(lib, f, 8, 2, 64, 3, max_fwd=8192, lse=False)
+    assert np.abs(a - b).max() <= 2 * ATOL_O
+
+
+def test_attention_rejects_bad_shapes(lib):
+    w = synth.workload(1)
+    r = Run(lib, w.forest)
+    x = torch.zeros((96, 4, 64), dtype=torch.float16, device="cuda")
+    for hq, hkv, d in ((4, 3, 64), (4, 4, 96), (4, 4, 256)):
+        with pytest.raises(lib.TreeError) as e:
+            lib.tree_attn_fwd(r.plan, r.dev, 0, x, x, x, x, None, hq, hkv, d)
+        assert e.value.code == lib.TREE_ERR_UNSUPPORTED
+    with pytest.raises(lib.TreeError) as e:
+        lib.tree_attn_fwd(r.plan, r.dev, 1, x, x, x, x, None, 4, 4, 64)
+    assert e.value.code == lib.TREE_ERR_INVALID_ARG
+    with pytest.raises(lib.TreeError) as e:
+        lib.tree_attn_fwd(r.plan, r.dev, 0, x.data_ptr() + 2, x, x, x, None, 4, 4, 64)
+    assert e.value.code == lib.TREE_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- whole path
+
+def test_pipeline_workload_two(lib):
+    """Plan -> RoPE -> attention -> readout on the GPU against the oracle chain."""
+    w = synth.workload(2)
+    r = Run(lib, w.forest, leaf1=w.leaf1, leaf2=w.leaf2)
+    p = r.oplan
+    q, k, v = synth.draw_qkv(p.n_fwd, p.n_tot, w.hq, w.hkv, w.d, w.seed)
+    qd, kd, vd = _dev(q), _dev(k), _dev(v)
+    r.rope(qd, kd, w.hq, w.hkv, w.d, w.theta, 0)
+    o = r.attn(qd, kd, vd, w.hq, w.hkv, w.d, 0)
+    logits = synth.draw_logits(p.n_slots, w.letter_stride, w.logit_sigma, w.seed)
+    i = r.plan.info
+    nq = i.n_questions
+    pc = torch.empty((nq, w.letter_stride), device="cuda")
+    ch = torch.empty(nq, dtype=torch.int32, device="cuda")
+    base = r.dev.data_ptr()
+    lib.readout_decide(_dev(logits), w.letter_stride, base + i.off_r1, base + i.off_r2, _dev(w.n_letters),
+                       _dev(w.temperature), nq, pc, None, ch, None, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    qr, kr = orope.apply_plan(p, q, k, w.theta)
+    ref = oatt.attend_paths(p, qr, kr, v)
+    assert np.abs(o.float().cpu().numpy() - ref).max() <= ATOL_O
+    ref_pc, _, _ = ordo.decide(logits, r.oq["r1"], r.oq["r2"], w.n_letters, w.temperature, w.letter_stride)
+    assert np.abs(pc.cpu().numpy() - ref_pc).max() <= ATOL_P
+    assert np.array_equal(ch.cpu().numpy(), ordo.choice_f32(logits, r.oq["r1"], r.oq["r2"], w.n_letters))

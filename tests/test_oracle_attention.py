@@ -118,3 +118,18 @@ def test_sampled_rows_match_paths_on_workload_two():
     a = oatt.attend_paths(p, q, k, v)
     b = oatt.attend_rows(p, q, k, v, rows)
     np.testing.assert_allclose(a[rows], b, rtol=0, atol=1e-12)
+
+
+def test_lse_rows_is_library_logsumexp_over_the_brute_mask():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(14)
+    f = synth.random_forest(rng, n_roots=2, max_blocks=9, max_len=7)
+    p, _ = oplan.plan_forest(f)
+    q, k, v = _rand_qkv(p, 4, 2, 16, 15)
+    m = oplan.brute_mask(p)[p.n_res:]
+    ours = oatt.lse_rows(p, q, k, np.arange(p.n_fwd))
+    for i in range(p.n_fwd):
+        keys = np.nonzero(m[i])[0]
+        for h in range(4):
+            s = k[keys, h // 2].astype(np.float64) @ q[i, h].astype(np.float64) / 4.0
+            assert abs(ours[i, h] - logsumexp(s)) < 1e-12
