@@ -1,4 +1,4 @@
-// tree_attn_fwd: attention over tree blocks for one forward chunk.
+// tree_attn_fwd: attention over tree blocks for one forward chunk, sm_103a.
 //
 // A token sees the earlier tokens of its own block and every token of its
 // ancestor blocks; sibling branches are masked, so each prompt's result equals
@@ -8,252 +8,436 @@
 // (AstrAI inference page, "KV Cache"); f16 storage, f32 softmax and
 // accumulation ("01 / Request path: GPU forward pass").
 //
-// Work decomposition: one CTA per (query tile of 128 rows, q head), CTAs
-// ordered longest tile first from the planner's per-chunk order.  The CTA walks
-// the tile's list of 128-key tiles (empty tiles never appear in the list);
-// full tiles skip the mask, partial tiles apply j <= i < send[j] per element.
-// Online softmax in the log2 domain keeps one running max and sum per row.
+// Work decomposition.  One CTA per (128-row query tile, kv head, pair of q
+// heads that share that kv head); CTAs are ordered longest tile first from the
+// planner's per-chunk order.  The CTA walks the tile's list of 128-key tiles
+// (empty tiles never appear in it); full tiles skip the mask, partial tiles
+// apply j <= i < send[j] per element.  Each K/V tile is loaded once and serves
+// both q heads.
 //
-// This file is the register-tile tensor-core version (mma.sync m16n8k16, f16
-// in, f32 accumulate): 8 warps x 16 query rows, K/V/send tiles staged in
-// shared memory with cp.async, XOR-swizzled 16-byte chunks for conflict-free
-// ldmatrix.
+// Roles (warp specialisation):
+//   softmax warpgroup h (warps 4h..4h+3), one per q head: thread = query row;
+//       reads its S row from tensor memory, masks, keeps a running max and sum
+//       in the log2 domain, writes P (f16) back into tensor memory over its S
+//       columns, and rescales O in tensor memory when the running max grows by
+//       more than 2^8 (so rescales are rare); at the end normalises O and stores it.
+//   producer warp: TMA loads of the Q tiles and of K, V (and the 128 subtree
+//       ends of the key tile) into a ring of shared-memory stages.
+//   MMA warp: one thread issues tcgen05.mma: S_h = Q_h K^T (A and B from shared
+//       memory, 128 x 128 x d) and O_h += P_h V (A = P from tensor memory,
+//       B = V from shared memory, 128 x d x 128), each followed by a commit to
+//       an mbarrier.  Per head the chain is S -> softmax -> PV -> next S, and the
+//       two heads interleave, so one head's softmax overlaps the other head's MMAs.
+// Tensor memory: S_h (128 columns, P_h aliased on its first 64), O_h (d columns).
+//
+// Every wait on an mbarrier gives up after ~2 s, sets TREE_ERR_TIMEOUT in the
+// caller's status word, and the CTA winds down: pending copies are awaited
+// (bounded), tensor memory is freed, and the kernel returns.
 
 #include <cmath>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "sm103.cuh"
 
 namespace tree {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int kWarps = 8;
+using namespace sm103;
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+constexpr int BN = 128;  // keys per tile (queries per tile: 128, one per TMEM lane)
+constexpr uint32_t BOX_BYTES = 128 * 128;  // one 128-row x 64-column f16 box (128-byte rows)
+constexpr uint64_t kWaitNs = 2000000000ull;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
+struct AttnArgs {
+  const int32_t *send;
+  const QTile *qtiles;
+  const int32_t *ent;
+  const int32_t *order;
+  __half *o;
+  float *lse;
+  int32_t *status;
+  int32_t t0, q0, n_tot, hq, hkv, ratio;
+  float scale_log2;
+};
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
+template <int D, int NH>
+struct Cfg {
+  static constexpr int CB = D / 64;                  // 64-column boxes per row of a tile
+  static constexpr int STAGES = D == 64 ? 3 : 2;     // K/V ring depth
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t K_OFF = Q_OFF + NH * CB * BOX_BYTES;
+  static constexpr uint32_t V_OFF = K_OFF + STAGES * CB * BOX_BYTES;
+  static constexpr uint32_t SEND_OFF = V_OFF + STAGES * CB * BOX_BYTES;
+  static constexpr uint32_t SMEM = SEND_OFF + STAGES * 512 + 1024;  // + alignment slack
+  static constexpr int THREADS = 128 * NH + 64;
+  static constexpr int PROD_WARP = 4 * NH;
+  static constexpr int MMA_WARP = 4 * NH + 1;
+  static constexpr uint32_t TMEM_COLS = (128 * NH + D * NH) <= 256 ? 256 : 512;
+  static constexpr uint32_t S_COL = 0;           // S_h at column 128 h
+  static constexpr uint32_t O_COL = 128 * NH;    // O_h at column O_COL + D h
+};
 
-__device__ __forceinline__ void mma16816(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
+// registers per thread: with 10 warps (two heads) one SM sub-partition holds 3
+// warps, whose 16384 registers allow 168 each
+template <int NH>
+constexpr int kMaxReg = NH == 2 ? 168 : 255;
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[3], v_full[3], kv_empty[3];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint32_t tmem;
+  int32_t abort;
+};
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// byte offset of 16-byte chunk c of row r in a swizzled tile with CH chunks per row
-template <int CH>
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return (uint32_t)(r * CH * 16 + ((c ^ (r & 7)) * 16));
-}
-
-template <int D>
-__global__ void __launch_bounds__(kWarps * 32) attn_mma_kernel(
-    const __half *__restrict__ q, const __half *__restrict__ k, const __half *__restrict__ v,
-    __half *__restrict__ o, float *__restrict__ lse, const int32_t *__restrict__ send,
-    const QTile *__restrict__ qtiles, const int32_t *__restrict__ ent, const int32_t *__restrict__ order,
-    int32_t t0, int32_t q0, int32_t n_tot, int hq, int hkv, float scale_log2) {
-  constexpr int CH = D / 8;  // 16-byte chunks per row
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *sQ = smem;
-  uint8_t *sK = sQ + BM * D * 2;
-  uint8_t *sV = sK + BN * D * 2;
-  int32_t *sSend = reinterpret_cast<int32_t *>(sV + BN * D * 2);
-
-  const int h = blockIdx.x % hq;
-  const int g = h / (hq / hkv);
-  const QTile qt = qtiles[order[t0 + blockIdx.x / hq]];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // ---- Q tile
-  for (int x = tid; x < BM * CH; x += kWarps * 32) {
-    const int r = x / CH, c = x % CH;
-    const int row = qt.row0 + r;
-    const bool ok = row < qt.row1;
-    const __half *src = q + ((size_t)(ok ? row - q0 : 0) * hq + h) * D + c * 8;
-    cp_async16(smem_u32(sQ) + swz<CH>(r, c), src, ok);
+// Wait for the phase with the given parity; false (and the CTA's abort flag
+// set) if it has not completed within kWaitNs, or, with honor_abort, as soon
+// as another thread of the CTA has given up.
+TREE_DEV bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *status,
+                       bool honor_abort = true, uint64_t limit_ns = kWaitNs) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try(bar, parity)) return true;
+    if ((n & 255) == 0) {
+      if (honor_abort && *abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort = 1;
+        if (status) atomicExch(status, TREE_ERR_TIMEOUT);
+        return false;
+      }
+    }
   }
-  cp_async_commit();
+}
 
-  float acc[D / 8][4];
-#pragma unroll
-  for (int j = 0; j < D / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  const int qi0 = qt.row0 + warp * 16 + (lane >> 2);  // global query of c0/c1; +8 for c2/c3
-  uint32_t qa[D / 16][4];
+// Warp-uniform form for the softmax warps, whose next steps are warp-collective.
+TREE_DEV bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *status) {
+  const bool ok = wait_bar(bar, parity, abort, status);
+  return __all_sync(0xffffffffu, ok);
+}
 
-  for (int e = qt.ent0; e < qt.ent1; ++e) {
-    const int code = ent[e];
-    const int kt = code >> 1;
-    const bool partial = code & 1;
-    const int j0 = kt * BN;
-    for (int x = tid; x < BN * CH; x += kWarps * 32) {
-      const int r = x / CH, c = x % CH;
-      const int key = j0 + r;
-      const bool ok = key < n_tot;
-      const size_t off = ((size_t)(ok ? key : 0) * hkv + g) * D + c * 8;
-      cp_async16(smem_u32(sK) + swz<CH>(r, c), k + off, ok);
-      cp_async16(smem_u32(sV) + swz<CH>(r, c), v + off, ok);
+// Bounded wait used while winding down: ignores the abort flag, gives up after 0.5 s.
+constexpr uint64_t kDrainNs = 500000000ull;
+
+template <int D, int NH>
+__global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
+    tree_attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                 const __grid_constant__ CUtensorMap mv, const AttnArgs a) {
+  using C = Cfg<D, NH>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Bars bars;
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = smem_u32(sm);
+  const int32_t *sSend = reinterpret_cast<const int32_t *>(sm + C::SEND_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pairs = a.ratio / NH;
+  const int per_tile = a.hkv * pairs;
+  const int rank = blockIdx.x / per_tile;
+  const int rem = blockIdx.x - rank * per_tile;
+  const int g = rem / pairs;
+  const int h0 = g * a.ratio + (rem - g * pairs) * NH;
+  const QTile qt = a.qtiles[__ldg(a.order + a.t0 + rank)];
+  const int n = qt.ent1 - qt.ent0;
+  volatile int32_t *abort = &bars.abort;
+
+  const uint32_t b_q = smem_u32(&bars.q_full);
+  auto b_k = [&](int s) { return smem_u32(&bars.k_full[s]); };
+  auto b_v = [&](int s) { return smem_u32(&bars.v_full[s]); };
+  auto b_e = [&](int s) { return smem_u32(&bars.kv_empty[s]); };
+  auto b_s = [&](int h) { return smem_u32(&bars.s_full[h]); };
+  auto b_p = [&](int h) { return smem_u32(&bars.p_full[h]); };
+  auto b_o = [&](int h) { return smem_u32(&bars.o_done[h]); };
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(b_k(s), 1);
+      mbar_init(b_v(s), 1);
+      mbar_init(b_e(s), 1);
     }
-    if (tid < BN / 4) cp_async16(smem_u32(sSend) + tid * 16, send + j0 + tid * 4, true);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
-    if (e == qt.ent0) {
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int r = warp * 16 + (lane & 15), c = kk * 2 + (lane >> 4);
-        ldsm_x4(smem_u32(sQ) + swz<CH>(r, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+    for (int h = 0; h < NH; ++h) {
+      mbar_init(b_s(h), 1);
+      mbar_init(b_p(h), 128);
+      mbar_init(b_o(h), 1);
+    }
+    bars.abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == C::MMA_WARP) tmem_alloc(smem_u32(&bars.tmem), C::TMEM_COLS);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = bars.tmem;
+
+  if (warp == C::PROD_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      prefetch_map(&mq);
+      prefetch_map(&mk);
+      prefetch_map(&mv);
+      mbar_expect_tx(b_q, NH * C::CB * BOX_BYTES);
+      for (int h = 0; h < NH; ++h)
+        for (int c = 0; c < C::CB; ++c)
+          tma_load_2d(s_base + C::Q_OFF + (h * C::CB + c) * BOX_BYTES, &mq, (h0 + h) * D + 64 * c, qt.row0 - a.q0,
+                      b_q);
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % C::STAGES;
+        if (i >= C::STAGES && !wait_bar(b_e(st), ((i / C::STAGES) - 1) & 1, abort, a.status)) break;
+        const int j0 = (__ldg(a.ent + qt.ent0 + i) >> 1) * BN;
+        mbar_expect_tx(b_k(st), C::CB * BOX_BYTES + 512);
+        for (int c = 0; c < C::CB; ++c)
+          tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES, &mk, g * D + 64 * c, j0, b_k(st));
+        bulk_load(s_base + C::SEND_OFF + st * 512, a.send + j0, 512, b_k(st));
+        mbar_expect_tx(b_v(st), C::CB * BOX_BYTES);
+        for (int c = 0; c < C::CB; ++c)
+          tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, g * D + 64 * c, j0, b_v(st));
+        issued = i + 1;
+      }
+      // wind down: every copy issued must have landed before the CTA exits
+      wait_bar(b_q, 0, abort, nullptr, false, kDrainNs);
+      for (int i = (issued > C::STAGES ? issued - C::STAGES : 0); i < issued; ++i) {
+        wait_bar(b_k(i % C::STAGES), (i / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
+        wait_bar(b_v(i % C::STAGES), (i / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
       }
     }
-    // ---- S = Q K^T for this warp's 16 rows x 128 keys
-    float s[BN / 8][4];
-#pragma unroll
-    for (int n = 0; n < BN / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-      for (int np = 0; np < BN / 16; ++np) {
-        const int m = lane >> 3;
-        const int r = np * 16 + (m >> 1) * 8 + (lane & 7), c = kk * 2 + (m & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(sK) + swz<CH>(r, c), b0, b1, b2, b3);
-        mma16816(s[2 * np], qa[kk], b0, b1);
-        mma16816(s[2 * np + 1], qa[kk], b2, b3);
-      }
-    }
-    // ---- scale (log2 domain), mask, running max
-    float mt[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int n = 0; n < BN / 8; ++n) {
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        float val = s[n][x] * scale_log2;
-        if (partial) {
-          const int jl = n * 8 + (lane & 3) * 2 + (x & 1);
-          const int i = qi0 + (x >> 1) * 8;
-          const int j = j0 + jl;
-          if (!(j <= i && i < sSend[jl])) val = -INFINITY;
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(128, 128, false);
+      constexpr uint32_t idesc_pv = idesc_f16(128, D, true);
+      auto issue_qk = [&](int h, int st) {
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+          const uint64_t da = sdesc_sw128(s_base + C::Q_OFF + h * C::CB * BOX_BYTES + off, 16, 1024);
+          const uint64_t db = sdesc_sw128(s_base + C::K_OFF + st * C::CB * BOX_BYTES + off, 16, 1024);
+          mma_ss(tmem + C::S_COL + 128 * h, da, db, idesc_qk, kk > 0);
         }
-        s[n][x] = val;
-        mt[x >> 1] = fmaxf(mt[x >> 1], val);
+        mma_commit(b_s(h));
+      };
+      bool ok = wait_bar(b_q, 0, abort, a.status) && wait_bar(b_k(0), 0, abort, a.status);
+      int last_o = -1, last_h = 0;  // iteration and head of the last PV commit issued
+      if (ok) {
+        fence_after();
+        for (int h = 0; h < NH; ++h) issue_qk(h, 0);
+        for (int i = 0; i < n && ok; ++i) {
+          const int st = i % C::STAGES;
+          if (!(ok = wait_bar(b_v(st), (i / C::STAGES) & 1, abort, a.status))) break;
+          for (int h = 0; h < NH && ok; ++h) {
+            if (!(ok = wait_bar(b_p(h), i & 1, abort, a.status))) break;
+            fence_after();
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t db = sdesc_sw128(s_base + C::V_OFF + st * C::CB * BOX_BYTES + kk * 2048, BOX_BYTES, 1024);
+              mma_ts(tmem + C::O_COL + D * h, tmem + C::S_COL + 128 * h + 8 * kk, db, idesc_pv, (i > 0 || kk > 0));
+            }
+            mma_commit(b_o(h));
+            last_o = i;
+            last_h = h;
+            if (h == NH - 1 && i + C::STAGES < n) mma_commit(b_e(st));
+            if (i + 1 < n) {
+              const int st2 = (i + 1) % C::STAGES;
+              if (h == 0 && !(ok = wait_bar(b_k(st2), ((i + 1) / C::STAGES) & 1, abort, a.status))) break;
+              // P_h shares S_h's columns: the next S_h waits until this PV has read P_h
+              if (!(ok = wait_bar(b_o(h), i & 1, abort, a.status))) break;
+              fence_after();
+              issue_qk(h, st2);
+            }
+          }
+        }
+      }
+      // wind down: all issued MMAs complete before tensor memory is freed
+      if (last_o >= 0) wait_bar(b_o(last_h), last_o & 1, abort, nullptr, false, kDrainNs);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int h = warp >> 2;
+    const int r = 32 * (warp & 3) + lane;
+    const int iq = qt.row0 + r;
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t tS = t_lane + C::S_COL + 128 * h;
+    const uint32_t tO = t_lane + C::O_COL + D * h;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    int done = 0;
+    for (int i = 0; i < n; ++i) {
+      const int st = i % C::STAGES;
+      const int e = __ldg(a.ent + qt.ent0 + i);
+      if (!(ok = wait_bar_warp(b_s(h), i & 1, abort, a.status))) break;
+      fence_after();
+      const bool partial = e & 1;
+      const int cmax = iq - (e >> 1) * BN;  // keys c <= cmax are not after the query
+      const int32_t *sd = sSend + st * 128;
+      if (partial && !(ok = wait_bar_warp(b_k(st), (i / C::STAGES) & 1, abort, a.status))) break;
+      // S row streams through registers 32 columns at a time (two passes: max, then exp)
+      uint32_t sa[32], sb[32];
+      float mx = -INFINITY;
+      tmem_ld32(tS, sa);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t *cur = (k & 1) ? sb : sa;
+        uint32_t *nxt = (k & 1) ? sa : sb;
+        if (k < 3) tmem_ld32(tS + 32 * (k + 1), nxt);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int c = 32 * k + u;
+          float x = __uint_as_float(cur[u]);
+          if (partial && !((c <= cmax) && (iq < sd[c]))) x = -INFINITY;
+          mx = fmaxf(mx, x);
+        }
+        tmem_wait_ld();
+      }
+      const float mt = mx * a.scale_log2;  // -inf stays -inf (scale > 0)
+      const bool grow = mt > m + 8.f;      // also true for the first finite maximum
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m - mt);  // 0 when m is -inf
+        m = mt;
+      }
+      const float mu = (m == -INFINITY) ? 0.f : m;
+      float sum = 0.f;
+      tmem_ld32(tS, sa);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t *cur = (k & 1) ? sb : sa;
+        uint32_t *nxt = (k & 1) ? sa : sb;
+        if (k < 3) tmem_ld32(tS + 32 * (k + 1), nxt);
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int c = 32 * k + 2 * u;
+          float x0 = __uint_as_float(cur[2 * u]), x1 = __uint_as_float(cur[2 * u + 1]);
+          if (partial) {
+            if (!((c <= cmax) && (iq < sd[c]))) x0 = -INFINITY;
+            if (!((c + 1 <= cmax) && (iq < sd[c + 1]))) x1 = -INFINITY;
+          }
+          const float p0 = ex2(fmaf(x0, a.scale_log2, -mu));
+          const float p1 = ex2(fmaf(x1, a.scale_log2, -mu));
+          sum += p0 + p1;
+          pk[u] = pack_f16x2(p0, p1);
+        }
+        // P columns [16k, 16k+16) cover S columns already consumed
+        tmem_st16(tS + 16 * k, pk);
+        tmem_wait_ld();
+      }
+      l = l * alpha + sum;
+      if (i > 0 && __any_sync(0xffffffffu, grow)) {
+        // O_h holds earlier tiles' sums: PV(i-1) is complete once S(i) was issued
+        if (!(ok = wait_bar_warp(b_o(h), (i - 1) & 1, abort, a.status))) break;
+        fence_after();
+        for (int c = 0; c < D / 32; ++c) {
+          tmem_ld32(tO + 32 * c, sa);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) sa[u] = __float_as_uint(__uint_as_float(sa[u]) * alpha);
+          tmem_st32(tO + 32 * c, sa);
+        }
+      }
+      tmem_wait_st();
+      fence_before();
+      mbar_arrive(b_p(h));
+      done = i + 1;
+    }
+    // ---- epilogue: O / l -> f16 rows of the chunk's output
+    if (ok && done == n && n > 0 && wait_bar_warp(b_o(h), (n - 1) & 1, abort, a.status)) {
+      fence_after();
+      const bool valid = iq < qt.row1;
+      const float inv = 1.f / l;
+      __half *dst = a.o + ((size_t)(iq - a.q0) * a.hq + (h0 + h)) * D;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          pk[u] = pack_f16x2(__uint_as_float(o[2 * u]) * inv, __uint_as_float(o[2 * u + 1]) * inv);
+        if (valid) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      if (valid && a.lse) {
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        a.lse[(size_t)(iq - a.q0) * a.hq + h0 + h] = (mu + __log2f(l)) * 0.69314718055994531f;
       }
     }
-    float alpha[2], mref[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mt[r] = fmaxf(mt[r], __shfl_xor_sync(0xffffffffu, mt[r], 1));
-      mt[r] = fmaxf(mt[r], __shfl_xor_sync(0xffffffffu, mt[r], 2));
-      const float mnew = fmaxf(mrow[r], mt[r]);
-      mref[r] = mnew == -INFINITY ? 0.f : mnew;
-      alpha[r] = ex2(mrow[r] - mref[r]);  // 0 when the old max is -inf
-      mrow[r] = mnew;
-      lrow[r] *= alpha[r];
-    }
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      acc[j][0] *= alpha[0];
-      acc[j][1] *= alpha[0];
-      acc[j][2] *= alpha[1];
-      acc[j][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int n = 0; n < BN / 8; ++n) {
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const float p = ex2(s[n][x] - mref[x >> 1]);
-        s[n][x] = p;
-        lrow[x >> 1] += p;
-      }
-    }
-    // ---- O += P V
-#pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk) {
-      uint32_t a[4];
-      a[0] = pack_half2(s[2 * kk][0], s[2 * kk][1]);
-      a[1] = pack_half2(s[2 * kk][2], s[2 * kk][3]);
-      a[2] = pack_half2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      a[3] = pack_half2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-      for (int jp = 0; jp < D / 16; ++jp) {
-        const int m = lane >> 3;
-        const int r = kk * 16 + (m & 1) * 8 + (lane & 7), c = jp * 2 + (m >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(sV) + swz<CH>(r, c), b0, b1, b2, b3);
-        mma16816(acc[2 * jp], a, b0, b1);
-        mma16816(acc[2 * jp + 1], a, b2, b3);
-      }
-    }
-    __syncthreads();
   }
-  // ---- normalise and store
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-  }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int i = qi0 + r * 8;
-    if (i >= qt.row1) continue;
-    const float inv = 1.f / lrow[r];
-    __half *dst = o + ((size_t)(i - q0) * hq + h) * D + (lane & 3) * 2;
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      *reinterpret_cast<__half2 *>(dst + j * 8) =
-          __floats2half2_rn(acc[j][2 * r] * inv, acc[j][2 * r + 1] * inv);
-    }
-    if (lse && (lane & 3) == 0) {
-      const float mr = mrow[r] == -INFINITY ? 0.f : mrow[r];
-      lse[(size_t)(i - q0) * hq + h] = (mr + log2f(lrow[r])) * 0.69314718055994531f;
-    }
+  fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
-template <int D>
-int launch_mma(const Plan &P, const int32_t *img, int chunk, const void *q, const void *k, const void *v,
-               void *o, float *lse, int hq, int hkv, float scale, cudaStream_t s) {
-  const size_t smem = (size_t)(BM + 2 * BN) * D * 2 + BN * 4;
-  auto kern = attn_mma_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd: %s", cudaGetErrorString(e));
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a [rows, cols] f16 matrix with 128-row x 64-column boxes, 128-byte swizzle.
+int make_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(TREE_ERR_CUDA, "tree_attn_fwd: cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TREE_ERR_CUDA, "tree_attn_fwd: tensor map encode failed (%d)", (int)r);
+  return TREE_OK;
+}
+
+template <int D, int NH>
+int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const void *k, const void *v, void *o,
+              float *lse, int hq, int hkv, float scale, int32_t *status, cudaStream_t s) {
+  using C = Cfg<D, NH>;
+  static bool attr_set = false;
+  auto kern = tree_attn_tc<D, NH>;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd: %s", cudaGetErrorString(e));
+    attr_set = true;
+  }
+  const int32_t q0 = P.chunk_q0[chunk], nq = P.chunk_q1[chunk] - q0;
+  CUtensorMap mq, mk, mv;
+  int rc;
+  if ((rc = make_map(&mq, q, (int64_t)hq * D, nq)) || (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot)) ||
+      (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot)))
+    return rc;
+  AttnArgs a;
+  a.send = img + P.off_send;
+  a.qtiles = reinterpret_cast<const QTile *>(img + P.off_qtile);
+  a.ent = img + P.off_ent;
+  a.order = img + P.off_order;
+  a.o = reinterpret_cast<__half *>(o);
+  a.lse = lse;
+  a.status = status;
+  a.t0 = P.chunk_t0[chunk];
+  a.q0 = q0;
+  a.n_tot = P.n_tot;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.ratio = hq / hkv;
+  a.scale_log2 = scale * 1.4426950408889634f;
   const int tiles = P.chunk_t1[chunk] - P.chunk_t0[chunk];
-  const dim3 grid((unsigned)(tiles * hq));
-  kern<<<grid, kWarps * 32, smem, s>>>(
-      reinterpret_cast<const __half *>(q), reinterpret_cast<const __half *>(k),
-      reinterpret_cast<const __half *>(v), reinterpret_cast<__half *>(o), lse, img + P.off_send,
-      reinterpret_cast<const QTile *>(img + P.off_qtile), img + P.off_ent, img + P.off_order,
-      P.chunk_t0[chunk], P.chunk_q0[chunk], P.n_tot, hq, hkv, scale * 1.4426950408889634f);
+  const dim3 grid((unsigned)(tiles * hkv * (a.ratio / NH)));
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(mq, mk, mv, a);
   return launch_status("tree_attn_fwd");
 }
 
@@ -264,7 +448,6 @@ extern "C" TREE_API int tree_attn_fwd(const tree_plan_t *plan, const void *plan_
                                       const void *q, const void *k, const void *v, void *o, float *lse,
                                       const tree_attn_params_t *params, int32_t *status, tree_stream_t stream) {
   using namespace tree;
-  (void)status;
   if (!plan || !plan_dev || !q || !k || !v || !o || !params)
     return fail(TREE_ERR_INVALID_ARG, "tree_attn_fwd: NULL argument");
   const Plan &P = plan->p;
@@ -278,6 +461,10 @@ extern "C" TREE_API int tree_attn_fwd(const tree_plan_t *plan, const void *plan_
   const float scale = params->scale > 0.f ? params->scale : 1.f / std::sqrt((float)d);
   const int32_t *img = reinterpret_cast<const int32_t *>(plan_dev);
   const cudaStream_t s = as_stream(stream);
-  if (d == 64) return launch_mma<64>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, s);
-  return launch_mma<128>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, s);
+  const bool pair = (hq / hkv) % 2 == 0;
+  if (d == 64)
+    return pair ? launch_tc<64, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, status, s)
+                : launch_tc<64, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, status, s);
+  return pair ? launch_tc<128, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, status, s)
+              : launch_tc<128, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, status, s);
 }
