@@ -15,24 +15,30 @@
 // apply j <= i < send[j] per element.  Each K/V tile is loaded once and serves
 // both q heads.
 //
-// Roles (warp specialisation):
-//   softmax warpgroup h (warps 4h..4h+3), one per q head: thread = query row;
-//       reads its S row from tensor memory, masks, keeps a running max and sum
-//       in the log2 domain, writes P (f16) back into tensor memory over its S
-//       columns, and rescales O in tensor memory when the running max grows by
-//       more than 2^8 (so rescales are rare); at the end normalises O and stores it.
-//   producer warp: TMA loads of the Q tiles and of K, V (and the 128 subtree
+// Roles (warp specialisation, 12 warps for two heads):
+//   softmax warpgroup h (warps 4h..4h+3), one per q head: thread = query row.
+//       Reads its whole S row (128 f32) from tensor memory in one pass, masks,
+//       keeps a running max and sum in the log2 domain, writes P (f16) to
+//       tensor memory, and rescales O in tensor memory only when the running
+//       max grows by more than 2^8 (rare); at the end normalises O and stores
+//       it.  These warps raise their register budget to 208 (setmaxnreg).
+//   producer warp: TMA loads of the Q tiles and of K, V (plus the 128 subtree
 //       ends of the key tile) into a ring of shared-memory stages.
-//   MMA warp: one thread issues tcgen05.mma: S_h = Q_h K^T (A and B from shared
-//       memory, 128 x 128 x d) and O_h += P_h V (A = P from tensor memory,
-//       B = V from shared memory, 128 x d x 128), each followed by a commit to
-//       an mbarrier.  Per head the chain is S -> softmax -> PV -> next S, and the
-//       two heads interleave, so one head's softmax overlaps the other head's MMAs.
-// Tensor memory: S_h (128 columns, P_h aliased on its first 64), O_h (d columns).
+//   MMA warp: one thread issues tcgen05.mma: S_h = Q_h K^T (A, B in shared
+//       memory, 128 x 128 x d) and O_h += P_h V (A = P_h in tensor memory,
+//       B = V in shared memory, 128 x d x 128), each followed by a commit to an
+//       mbarrier.  The producer/MMA warpgroup lowers its budget to 88 registers.
+// Tensor memory (512 columns for two heads):
+//   d = 64 : S_h at 128h, P_h at 256 + 64h, O_h at 384 + 64h.  S_h is free as
+//            soon as the softmax has read it, so S_h(i+1) is computed while the
+//            softmax still works on tile i.
+//   d = 128: S_h at 128h with P_h over its first 64 columns, O_h at 256 + 128h;
+//            S_h(i+1) waits until PV_h(i) has read P_h, and the two heads'
+//            chains interleave on the tensor core.
 //
 // Every wait on an mbarrier gives up after ~2 s, sets TREE_ERR_TIMEOUT in the
-// caller's status word, and the CTA winds down: pending copies are awaited
-// (bounded), tensor memory is freed, and the kernel returns.
+// caller's status word, and the CTA winds down: pending copies and MMAs are
+// awaited (bounded), tensor memory is freed, and the kernel returns.
 
 #include <cmath>
 
@@ -46,9 +52,10 @@ namespace {
 
 using namespace sm103;
 
-constexpr int BN = 128;  // keys per tile (queries per tile: 128, one per TMEM lane)
+constexpr int BN = 128;                    // keys per tile (queries per tile: 128, one per TMEM lane)
 constexpr uint32_t BOX_BYTES = 128 * 128;  // one 128-row x 64-column f16 box (128-byte rows)
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 500000000ull;
 
 struct AttnArgs {
   const int32_t *send;
@@ -64,36 +71,37 @@ struct AttnArgs {
 
 template <int D, int NH>
 struct Cfg {
-  static constexpr int CB = D / 64;                  // 64-column boxes per row of a tile
-  static constexpr int STAGES = D == 64 ? 3 : 2;     // K/V ring depth
+  static constexpr int CB = D / 64;               // 64-column boxes per row of a tile
+  static constexpr int STAGES = D == 64 ? 3 : 2;  // K/V ring depth
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t K_OFF = Q_OFF + NH * CB * BOX_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + STAGES * CB * BOX_BYTES;
   static constexpr uint32_t SEND_OFF = V_OFF + STAGES * CB * BOX_BYTES;
   static constexpr uint32_t SMEM = SEND_OFF + STAGES * 512 + 1024;  // + alignment slack
-  static constexpr int THREADS = 128 * NH + 64;
+  static constexpr int WARPS = 4 * NH + 4;        // softmax warpgroups + producer/MMA warpgroup
+  static constexpr int THREADS = 32 * WARPS;
   static constexpr int PROD_WARP = 4 * NH;
   static constexpr int MMA_WARP = 4 * NH + 1;
-  static constexpr uint32_t TMEM_COLS = (128 * NH + D * NH) <= 256 ? 256 : 512;
-  static constexpr uint32_t S_COL = 0;           // S_h at column 128 h
-  static constexpr uint32_t O_COL = 128 * NH;    // O_h at column O_COL + D h
+  static constexpr bool PSEP = D == 64;           // P in its own columns
+  static constexpr uint32_t P_COL = 128 * NH;     // P_h at P_COL + 64h (PSEP only)
+  static constexpr uint32_t O_COL = PSEP ? 128 * NH + 64 * NH : 128 * NH;
+  static constexpr uint32_t TMEM_USED = O_COL + D * NH;
+  static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+  // 12 warps launch at 168 registers (3 per SM sub-partition of 16384); setmaxnreg moves them
+  static constexpr int SOFTMAX_REGS = 208;       // 2 x 208 + 88 = 504 <= 512 per sub-partition
+  static constexpr int SERVICE_REGS = 88;
 };
-
-// registers per thread: with 10 warps (two heads) one SM sub-partition holds 3
-// warps, whose 16384 registers allow 168 each
-template <int NH>
-constexpr int kMaxReg = NH == 2 ? 168 : 255;
 
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[3], v_full[3], kv_empty[3];
-  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
   uint32_t tmem;
   int32_t abort;
 };
 
 // Wait for the phase with the given parity; false (and the CTA's abort flag
-// set) if it has not completed within kWaitNs, or, with honor_abort, as soon
+// set) if it has not completed within limit_ns, or, with honor_abort, as soon
 // as another thread of the CTA has given up.
 TREE_DEV bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *status,
                        bool honor_abort = true, uint64_t limit_ns = kWaitNs) {
@@ -118,11 +126,8 @@ TREE_DEV bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int32_t *abo
   return __all_sync(0xffffffffu, ok);
 }
 
-// Bounded wait used while winding down: ignores the abort flag, gives up after 0.5 s.
-constexpr uint64_t kDrainNs = 500000000ull;
-
 template <int D, int NH>
-__global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
+__global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     tree_attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const AttnArgs a) {
   using C = Cfg<D, NH>;
@@ -148,6 +153,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
   auto b_v = [&](int s) { return smem_u32(&bars.v_full[s]); };
   auto b_e = [&](int s) { return smem_u32(&bars.kv_empty[s]); };
   auto b_s = [&](int h) { return smem_u32(&bars.s_full[h]); };
+  auto b_f = [&](int h) { return smem_u32(&bars.s_free[h]); };
   auto b_p = [&](int h) { return smem_u32(&bars.p_full[h]); };
   auto b_o = [&](int h) { return smem_u32(&bars.o_done[h]); };
 
@@ -160,6 +166,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
     }
     for (int h = 0; h < NH; ++h) {
       mbar_init(b_s(h), 1);
+      mbar_init(b_f(h), 128);
       mbar_init(b_p(h), 128);
       mbar_init(b_o(h), 1);
     }
@@ -172,29 +179,40 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
   fence_after();
   const uint32_t tmem = bars.tmem;
 
-  if (warp == C::PROD_WARP) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
-      prefetch_map(&mq);
-      prefetch_map(&mk);
-      prefetch_map(&mv);
-      mbar_expect_tx(b_q, NH * C::CB * BOX_BYTES);
-      for (int h = 0; h < NH; ++h)
-        for (int c = 0; c < C::CB; ++c)
-          tma_load_2d(s_base + C::Q_OFF + (h * C::CB + c) * BOX_BYTES, &mq, (h0 + h) * D + 64 * c, qt.row0 - a.q0,
-                      b_q);
+  if (warp >= 4 * NH) {
+    if (NH == 2) regs_dec<C::SERVICE_REGS>();
+    if (warp == C::PROD_WARP && n > 0) {
+      // ---------------------------------------------------------- producer (whole warp, one lane issues)
+      if (elect_one()) {
+        prefetch_map(&mq);
+        prefetch_map(&mk);
+        prefetch_map(&mv);
+        mbar_expect_tx(b_q, NH * C::CB * BOX_BYTES);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+#pragma unroll
+          for (int c = 0; c < C::CB; ++c)
+            tma_load_2d(s_base + C::Q_OFF + (h * C::CB + c) * BOX_BYTES, &mq, (h0 + h) * D + 64 * c, qt.row0 - a.q0,
+                        b_q);
+      }
+      __syncwarp();
       int issued = 0;
       for (int i = 0; i < n; ++i) {
         const int st = i % C::STAGES;
-        if (i >= C::STAGES && !wait_bar(b_e(st), ((i / C::STAGES) - 1) & 1, abort, a.status)) break;
+        if (i >= C::STAGES && !wait_bar_warp(b_e(st), ((i / C::STAGES) - 1) & 1, abort, a.status)) break;
         const int j0 = (__ldg(a.ent + qt.ent0 + i) >> 1) * BN;
-        mbar_expect_tx(b_k(st), C::CB * BOX_BYTES + 512);
-        for (int c = 0; c < C::CB; ++c)
-          tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES, &mk, g * D + 64 * c, j0, b_k(st));
-        bulk_load(s_base + C::SEND_OFF + st * 512, a.send + j0, 512, b_k(st));
-        mbar_expect_tx(b_v(st), C::CB * BOX_BYTES);
-        for (int c = 0; c < C::CB; ++c)
-          tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, g * D + 64 * c, j0, b_v(st));
+        if (elect_one()) {
+          mbar_expect_tx(b_k(st), C::CB * BOX_BYTES + 512);
+#pragma unroll
+          for (int c = 0; c < C::CB; ++c)
+            tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES, &mk, g * D + 64 * c, j0, b_k(st));
+          bulk_load(s_base + C::SEND_OFF + st * 512, a.send + j0, 512, b_k(st));
+          mbar_expect_tx(b_v(st), C::CB * BOX_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::CB; ++c)
+            tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, g * D + 64 * c, j0, b_v(st));
+        }
+        __syncwarp();
         issued = i + 1;
       }
       // wind down: every copy issued must have landed before the CTA exits
@@ -203,47 +221,86 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
         wait_bar(b_k(i % C::STAGES), (i / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
         wait_bar(b_v(i % C::STAGES), (i / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
       }
-    }
-  } else if (warp == C::MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
+    } else if (warp == C::MMA_WARP && n > 0) {
+      // ---------------------------------------------------------- MMA issuer (whole warp, one lane issues)
       constexpr uint32_t idesc_qk = idesc_f16(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, D, true);
       auto issue_qk = [&](int h, int st) {
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          const uint64_t da = sdesc_sw128(s_base + C::Q_OFF + h * C::CB * BOX_BYTES + off, 16, 1024);
-          const uint64_t db = sdesc_sw128(s_base + C::K_OFF + st * C::CB * BOX_BYTES + off, 16, 1024);
-          mma_ss(tmem + C::S_COL + 128 * h, da, db, idesc_qk, kk > 0);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+            const uint64_t da = sdesc_sw128(s_base + C::Q_OFF + h * C::CB * BOX_BYTES + off, 16, 1024);
+            const uint64_t db = sdesc_sw128(s_base + C::K_OFF + st * C::CB * BOX_BYTES + off, 16, 1024);
+            mma_ss(tmem + 128 * h, da, db, idesc_qk, kk > 0);
+          }
+          mma_commit(b_s(h));
         }
-        mma_commit(b_s(h));
+        __syncwarp();
       };
-      bool ok = wait_bar(b_q, 0, abort, a.status) && wait_bar(b_k(0), 0, abort, a.status);
+      auto issue_pv = [&](int h, int st, int i) {
+        const uint32_t p_col = C::PSEP ? C::P_COL + 64 * h : 128 * h;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t db =
+                sdesc_sw128(s_base + C::V_OFF + st * C::CB * BOX_BYTES + kk * 2048, BOX_BYTES, 1024);
+            mma_ts(tmem + C::O_COL + D * h, tmem + p_col + 8 * kk, db, idesc_pv, (i > 0 || kk > 0));
+          }
+          mma_commit(b_o(h));
+        }
+        __syncwarp();
+      };
+      bool ok = wait_bar_warp(b_q, 0, abort, a.status) && wait_bar_warp(b_k(0), 0, abort, a.status);
       int last_o = -1, last_h = 0;  // iteration and head of the last PV commit issued
       if (ok) {
         fence_after();
         for (int h = 0; h < NH; ++h) issue_qk(h, 0);
         for (int i = 0; i < n && ok; ++i) {
           const int st = i % C::STAGES;
-          if (!(ok = wait_bar(b_v(st), (i / C::STAGES) & 1, abort, a.status))) break;
-          for (int h = 0; h < NH && ok; ++h) {
-            if (!(ok = wait_bar(b_p(h), i & 1, abort, a.status))) break;
-            fence_after();
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t db = sdesc_sw128(s_base + C::V_OFF + st * C::CB * BOX_BYTES + kk * 2048, BOX_BYTES, 1024);
-              mma_ts(tmem + C::O_COL + D * h, tmem + C::S_COL + 128 * h + 8 * kk, db, idesc_pv, (i > 0 || kk > 0));
-            }
-            mma_commit(b_o(h));
-            last_o = i;
-            last_h = h;
-            if (h == NH - 1 && i + C::STAGES < n) mma_commit(b_e(st));
+          const int st2 = (i + 1) % C::STAGES;
+          if (C::PSEP) {
+            // next S first: S_h is free once the softmax has read it into registers
             if (i + 1 < n) {
-              const int st2 = (i + 1) % C::STAGES;
-              if (h == 0 && !(ok = wait_bar(b_k(st2), ((i + 1) / C::STAGES) & 1, abort, a.status))) break;
-              // P_h shares S_h's columns: the next S_h waits until this PV has read P_h
-              if (!(ok = wait_bar(b_o(h), i & 1, abort, a.status))) break;
+              if (!(ok = wait_bar_warp(b_k(st2), ((i + 1) / C::STAGES) & 1, abort, a.status))) break;
+              for (int h = 0; h < NH && ok; ++h) {
+                if (!(ok = wait_bar_warp(b_f(h), i & 1, abort, a.status))) break;
+                fence_after();
+                issue_qk(h, st2);
+              }
+              if (!ok) break;
+            }
+            if (!(ok = wait_bar_warp(b_v(st), (i / C::STAGES) & 1, abort, a.status))) break;
+            for (int h = 0; h < NH && ok; ++h) {
+              if (!(ok = wait_bar_warp(b_p(h), i & 1, abort, a.status))) break;
               fence_after();
-              issue_qk(h, st2);
+              issue_pv(h, st, i);
+              last_o = i;
+              last_h = h;
+            }
+            if (ok && i + C::STAGES < n) {
+              if (elect_one()) mma_commit(b_e(st));
+              __syncwarp();
+            }
+          } else {
+            // P_h shares S_h's columns: per head, PV(i) then (once it is done) S(i+1)
+            if (!(ok = wait_bar_warp(b_v(st), (i / C::STAGES) & 1, abort, a.status))) break;
+            for (int h = 0; h < NH && ok; ++h) {
+              if (!(ok = wait_bar_warp(b_p(h), i & 1, abort, a.status))) break;
+              fence_after();
+              issue_pv(h, st, i);
+              last_o = i;
+              last_h = h;
+              if (h == NH - 1 && i + C::STAGES < n) {
+                if (elect_one()) mma_commit(b_e(st));
+                __syncwarp();
+              }
+              if (i + 1 < n) {
+                if (h == 0 && !(ok = wait_bar_warp(b_k(st2), ((i + 1) / C::STAGES) & 1, abort, a.status))) break;
+                if (!(ok = wait_bar_warp(b_o(h), i & 1, abort, a.status))) break;
+                fence_after();
+                issue_qk(h, st2);
+              }
             }
           }
         }
@@ -253,11 +310,13 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
+    if (NH == 2) regs_inc<C::SOFTMAX_REGS>();
     const int h = warp >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int iq = qt.row0 + r;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const uint32_t tS = t_lane + C::S_COL + 128 * h;
+    const uint32_t tS = t_lane + 128 * h;
+    const uint32_t tP = C::PSEP ? t_lane + C::P_COL + 64 * h : tS;
     const uint32_t tO = t_lane + C::O_COL + D * h;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
@@ -267,29 +326,39 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
       const int e = __ldg(a.ent + qt.ent0 + i);
       if (!(ok = wait_bar_warp(b_s(h), i & 1, abort, a.status))) break;
       fence_after();
-      const bool partial = e & 1;
-      const int cmax = iq - (e >> 1) * BN;  // keys c <= cmax are not after the query
-      const int32_t *sd = sSend + st * 128;
-      if (partial && !(ok = wait_bar_warp(b_k(st), (i / C::STAGES) & 1, abort, a.status))) break;
-      // S row streams through registers 32 columns at a time (two passes: max, then exp)
-      uint32_t sa[32], sb[32];
-      float mx = -INFINITY;
-      tmem_ld32(tS, sa);
+      uint32_t s[128];
+      tmem_ld32(tS + 0, s);
+      tmem_ld32(tS + 32, s + 32);
+      tmem_ld32(tS + 64, s + 64);
+      tmem_ld32(tS + 96, s + 96);
       tmem_wait_ld();
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t *cur = (k & 1) ? sb : sa;
-        uint32_t *nxt = (k & 1) ? sa : sb;
-        if (k < 3) tmem_ld32(tS + 32 * (k + 1), nxt);
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const int c = 32 * k + u;
-          float x = __uint_as_float(cur[u]);
-          if (partial && !((c <= cmax) && (iq < sd[c]))) x = -INFINITY;
-          mx = fmaxf(mx, x);
-        }
-        tmem_wait_ld();
+      if (C::PSEP) {
+        fence_before();
+        mbar_arrive(b_f(h));  // S_h may be overwritten by the next QK
       }
+      if (e & 1) {
+        // partial tile: key j = j0 + c is visible iff j <= iq < send[j]
+        if (!(ok = wait_bar_warp(b_k(st), (i / C::STAGES) & 1, abort, a.status))) break;
+        const int cmax = iq - (e >> 1) * BN;  // keys c <= cmax are not after the query
+        const int4 *sd = reinterpret_cast<const int4 *>(sSend + st * 128);
+#pragma unroll
+        for (int c4 = 0; c4 < 32; ++c4) {
+          const int4 se = sd[c4];
+          const int sv[4] = {se.x, se.y, se.z, se.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = 4 * c4 + u;
+            if (!((c <= cmax) && (iq < sv[u]))) s[c] = __float_as_uint(-INFINITY);
+          }
+        }
+      }
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mt = mx * a.scale_log2;  // -inf stays -inf (scale > 0)
       const bool grow = mt > m + 8.f;      // also true for the first finite maximum
       float alpha = 1.f;
@@ -298,43 +367,33 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
         m = mt;
       }
       const float mu = (m == -INFINITY) ? 0.f : m;
-      float sum = 0.f;
-      tmem_ld32(tS, sa);
-      tmem_wait_ld();
+      float sum8[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t *cur = (k & 1) ? sb : sa;
-        uint32_t *nxt = (k & 1) ? sa : sb;
-        if (k < 3) tmem_ld32(tS + 32 * (k + 1), nxt);
-        uint32_t pk[16];
+      for (int u = 0; u < 8; ++u) sum8[u] = 0.f;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int c = 32 * k + 2 * u;
-          float x0 = __uint_as_float(cur[2 * u]), x1 = __uint_as_float(cur[2 * u + 1]);
-          if (partial) {
-            if (!((c <= cmax) && (iq < sd[c]))) x0 = -INFINITY;
-            if (!((c + 1 <= cmax) && (iq < sd[c + 1]))) x1 = -INFINITY;
-          }
-          const float p0 = ex2(fmaf(x0, a.scale_log2, -mu));
-          const float p1 = ex2(fmaf(x1, a.scale_log2, -mu));
-          sum += p0 + p1;
-          pk[u] = pack_f16x2(p0, p1);
-        }
-        // P columns [16k, 16k+16) cover S columns already consumed
-        tmem_st16(tS + 16 * k, pk);
-        tmem_wait_ld();
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = ex2(fmaf(__uint_as_float(s[c]), a.scale_log2, -mu));
+        const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), a.scale_log2, -mu));
+        sum8[(c >> 1) & 7] += p0 + p1;
+        s[c >> 1] = pack_f16x2(p0, p1);
       }
-      l = l * alpha + sum;
-      if (i > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_h holds earlier tiles' sums: PV(i-1) is complete once S(i) was issued
+      l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+      // PV_h(i-1) must be done before P_h is rewritten (separate P) or O_h is rescaled
+      const bool need_o = i > 0 && __any_sync(0xffffffffu, grow);
+      if (i > 0 && (C::PSEP || need_o)) {
         if (!(ok = wait_bar_warp(b_o(h), (i - 1) & 1, abort, a.status))) break;
         fence_after();
+      }
+      tmem_st32(tP + 0, s);
+      tmem_st32(tP + 32, s + 32);
+      if (need_o) {
         for (int c = 0; c < D / 32; ++c) {
-          tmem_ld32(tO + 32 * c, sa);
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 32; ++u) sa[u] = __float_as_uint(__uint_as_float(sa[u]) * alpha);
-          tmem_st32(tO + 32 * c, sa);
+          for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+          tmem_st32(tO + 32 * c, o);
         }
       }
       tmem_wait_st();
@@ -348,6 +407,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS) __maxnreg__(kMaxReg<NH>)
       const bool valid = iq < qt.row1;
       const float inv = 1.f / l;
       __half *dst = a.o + ((size_t)(iq - a.q0) * a.hq + (h0 + h)) * D;
+#pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + 32 * c, o);

@@ -13,6 +13,16 @@ namespace sm103 {
 
 TREE_DEV uint32_t smem_u32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
+// One lane of a converged warp (elect.sync); single-thread instructions such as
+// tcgen05.mma or TMA copies are issued by that lane while the whole warp runs
+// the surrounding code, which keeps their operands warp-uniform.
+TREE_DEV bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .pred p;\n .reg .b32 r;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier
 TREE_DEV void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -132,6 +142,16 @@ TREE_DEV void tmem_st16(uint32_t taddr, const uint32_t *r) {
       : "memory");
 }
 TREE_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Warpgroup register budget changes (all four warps of a warpgroup execute them).
+template <uint32_t N>
+TREE_DEV void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+TREE_DEV void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // ---------------------------------------------------------------- math
 TREE_DEV float ex2(float x) {
