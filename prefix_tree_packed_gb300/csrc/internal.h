@@ -22,7 +22,7 @@ struct Plan {
   std::vector<int32_t> block_map;
   std::vector<int32_t> blk_start, blk_len, blk_parent, blk_depth, blk_pos0, blk_send, blk_resident,
       blk_slot;
-  std::vector<int32_t> pos, send;
+  // pos [n_tot] and send [ceil(n_tot/128)*128] live inside the device image
   std::vector<int32_t> chunk_q0, chunk_q1, chunk_t0, chunk_t1, chunk_nent;
   std::vector<int64_t> chunk_pairs;
   std::vector<int32_t> qt_row0, qt_row1, qt_ent0, qt_ent1, ent, qt_order;

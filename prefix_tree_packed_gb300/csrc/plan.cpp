@@ -57,78 +57,105 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
       return fail(TREE_ERR_BAD_TREE, "block %d: parent %d out of range", b, p);
     if (s.length[b] <= 0) return fail(TREE_ERR_BAD_TREE, "block %d: length %d <= 0", b, s.length[b]);
   }
-  {
-    // depth of every block by walking up; a chain longer than nb is a cycle
-    for (int32_t b = 0; b < nb; ++b) {
-      int32_t d = 0;
-      for (int32_t x = b; x != -1; x = s.parent[x]) {
-        if (++d > nb) return fail(TREE_ERR_BAD_TREE, "block %d: parent chain has a cycle", b);
-      }
-      if (d > max_depth) return fail(TREE_ERR_DEPTH, "block %d: depth %d > %d", b, d, max_depth);
+  // depth of every block by walking up; a chain longer than nb is a cycle
+  std::vector<int32_t> depth(nb);
+  int32_t dmax = 0;
+  for (int32_t b = 0; b < nb; ++b) {
+    int32_t d = 0;
+    for (int32_t x = b; x != -1; x = s.parent[x]) {
+      if (++d > nb) return fail(TREE_ERR_BAD_TREE, "block %d: parent chain has a cycle", b);
     }
+    if (d > max_depth) return fail(TREE_ERR_DEPTH, "block %d: depth %d > %d", b, d, max_depth);
+    depth[b] = d;
+    dmax = std::max(dmax, d);
   }
-  // ---- children lists of the input forest (input order)
-  std::vector<std::vector<int32_t>> kids(nb);
-  std::vector<int32_t> roots;
-  for (int32_t b = 0; b < nb; ++b) (s.parent[b] < 0 ? roots : kids[s.parent[b]]).push_back(b);
-
   auto key_of = [&](int32_t b) -> uint64_t { return s.key ? s.key[b] : 0; };
   auto res_of = [&](int32_t b) -> int32_t { return s.resident ? (s.resident[b] ? 1 : 0) : 0; };
 
-  // ---- merge identical siblings top-down.  A sibling set is the sorted list
-  // of input children of all members of one merged block.
-  std::vector<int32_t> canon(nb, -1);
-  std::vector<std::vector<int32_t>> ckids(nb);  // canonical -> canonical children, in order
-  std::vector<int32_t> top;
-  struct Work {
-    int32_t owner;  // canonical parent, -1 = the forest
-    std::vector<int32_t> members;
+  // ---- merge identical siblings (trie semantics).  Blocks are visited by depth
+  // and, within a depth, by input index, so a parent's merged identity is known
+  // before its children and the first block of every identical group (the
+  // lowest input index) becomes the group's block.  Two blocks are identical
+  // when their merged parents, lengths and non-zero keys agree.
+  std::vector<int32_t> by_depth(nb), dstart(dmax + 2, 0);
+  for (int32_t b = 0; b < nb; ++b) ++dstart[depth[b] + 1];
+  for (int32_t d = 1; d <= dmax + 1; ++d) dstart[d] += dstart[d - 1];
+  {
+    std::vector<int32_t> fill(dstart.begin(), dstart.end());
+    for (int32_t b = 0; b < nb; ++b) by_depth[fill[depth[b]]++] = b;
+  }
+  std::vector<int32_t> canon(nb, -1), cparent(nb, -1);
+  size_t cap = 16;
+  while (cap < 2 * (size_t)nb) cap <<= 1;
+  struct Slot {
+    int32_t parent, len, block;
+    uint64_t key;
   };
-  std::vector<Work> work;
-  work.push_back({-1, roots});
-  while (!work.empty()) {
-    Work w = std::move(work.back());
-    work.pop_back();
-    std::sort(w.members.begin(), w.members.end());
-    std::map<std::pair<int32_t, uint64_t>, int32_t> seen;
-    std::vector<int32_t> order;
-    std::map<int32_t, std::vector<int32_t>> pooled;
-    for (int32_t b : w.members) {
-      const uint64_t k = key_of(b);
-      int32_t c = b;
-      if (k != 0) {
-        auto it = seen.find({s.length[b], k});
-        if (it != seen.end()) {
-          c = it->second;
-          if (res_of(b) != res_of(c))
-            return fail(TREE_ERR_INVALID_ARG, "blocks %d and %d merge but disagree on residency", c, b);
-        } else {
-          seen.emplace(std::make_pair(s.length[b], k), b);
+  std::vector<Slot> table(cap, Slot{0, 0, -1, 0});
+  auto mix = [](uint64_t x) {
+    x ^= x >> 33;
+    x *= 0xff51afd7ed558ccdull;
+    x ^= x >> 33;
+    x *= 0xc4ceb9fe1a85ec53ull;
+    return x ^ (x >> 33);
+  };
+  for (int32_t idx = 0; idx < nb; ++idx) {
+    const int32_t b = by_depth[idx];
+    const int32_t cp = s.parent[b] >= 0 ? canon[s.parent[b]] : -1;
+    cparent[b] = cp;
+    const uint64_t k = key_of(b);
+    int32_t c = b;
+    if (k != 0) {
+      size_t h = mix(k ^ mix(((uint64_t)(uint32_t)cp << 32) | (uint32_t)s.length[b])) & (cap - 1);
+      for (;; h = (h + 1) & (cap - 1)) {
+        Slot &sl = table[h];
+        if (sl.block < 0) {
+          sl = Slot{cp, s.length[b], b, k};
+          break;
+        }
+        if (sl.parent == cp && sl.len == s.length[b] && sl.key == k) {
+          c = sl.block;
+          break;
         }
       }
-      canon[b] = c;
-      if (c == b) order.push_back(b);
-      auto &pl = pooled[c];
-      pl.insert(pl.end(), kids[b].begin(), kids[b].end());
+      if (c != b && res_of(b) != res_of(c))
+        return fail(TREE_ERR_INVALID_ARG, "blocks %d and %d merge but disagree on residency", c, b);
     }
-    if (w.owner < 0)
-      top = order;
-    else
-      ckids[w.owner] = order;
-    for (auto &kv : pooled)
-      if (!kv.second.empty()) work.push_back({kv.first, std::move(kv.second)});
+    canon[b] = c;
   }
 
-  // ---- depth-first pre-order of canonical blocks
+  // ---- children of merged blocks (CSR, input order) and depth-first pre-order
+  std::vector<int32_t> cstart(nb + 2, 0), clist;
+  clist.reserve(nb);
+  int32_t n_roots = 0;
+  for (int32_t b = 0; b < nb; ++b) {
+    if (canon[b] != b) continue;
+    if (cparent[b] < 0)
+      ++n_roots;
+    else
+      ++cstart[cparent[b] + 2];
+  }
+  for (int32_t i = 2; i <= nb + 1; ++i) cstart[i] += cstart[i - 1];
+  clist.resize(cstart[nb + 1]);
+  std::vector<int32_t> top;
+  top.reserve(n_roots);
+  for (int32_t b = 0; b < nb; ++b) {
+    if (canon[b] != b) continue;
+    if (cparent[b] < 0)
+      top.push_back(b);
+    else
+      clist[cstart[cparent[b] + 1]++] = b;
+  }
+  // after the fill, cstart[c+1] is the end of c's children and cstart[c] their start
   std::vector<int32_t> packed;
+  packed.reserve(nb);
   {
     std::vector<int32_t> st(top.rbegin(), top.rend());
     while (!st.empty()) {
       const int32_t c = st.back();
       st.pop_back();
       packed.push_back(c);
-      const auto &ch = ckids[c];
-      for (auto it = ch.rbegin(); it != ch.rend(); ++it) st.push_back(*it);
+      for (int32_t i = cstart[c + 1] - 1; i >= cstart[c]; --i) st.push_back(clist[i]);
     }
   }
   const int32_t nbc = (int32_t)packed.size();
@@ -191,45 +218,57 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   if (n_res == P.n_tot) return fail(TREE_ERR_INVALID_ARG, "no forward tokens");
   P.n_res = n_res;
 
-  // ---- per-token tables
   const int32_t n_kvt = (P.n_tot + kTile - 1) / kTile;
-  P.pos.assign(P.n_tot, 0);
-  P.send.assign((size_t)n_kvt * kTile, 0);
   int32_t maxpos = 0;
-  for (int32_t i = 0; i < nbc; ++i) {
-    for (int32_t t = 0; t < P.blk_len[i]; ++t) {
-      P.pos[P.blk_start[i] + t] = P.blk_pos0[i] + t;
-      P.send[P.blk_start[i] + t] = P.blk_send[i];
-    }
-    maxpos = std::max(maxpos, P.blk_pos0[i] + P.blk_len[i]);
-  }
+  for (int32_t i = 0; i < nbc; ++i) maxpos = std::max(maxpos, P.blk_pos0[i] + P.blk_len[i]);
   P.max_pos = maxpos;
-  P.pairs = 0;
-  for (int32_t t = P.n_res; t < P.n_tot; ++t) P.pairs += (int64_t)P.pos[t] + 1;
-
-  // per key tile: smallest and largest subtree end (padding keys count as 0)
-  std::vector<int32_t> kt_min(n_kvt), kt_max(n_kvt);
-  for (int32_t kt = 0; kt < n_kvt; ++kt) {
-    int32_t mn = INT32_MAX, mx = INT32_MIN;
-    for (int32_t j = kt * kTile; j < (kt + 1) * kTile; ++j) {
-      mn = std::min(mn, P.send[j]);
-      mx = std::max(mx, P.send[j]);
+  const int32_t *bstart = P.blk_start.data(), *blen = P.blk_len.data(), *bpos0 = P.blk_pos0.data(),
+                *bsend = P.blk_send.data();
+  // packed block holding token t (blocks are sorted by start)
+  auto block_of = [&](int32_t t) {
+    return (int32_t)(std::upper_bound(P.blk_start.begin(), P.blk_start.end(), t) - P.blk_start.begin()) - 1;
+  };
+  // visible pairs of the queries in [a, b): each query sees pos + 1 keys
+  auto pairs_in = [&](int32_t a, int32_t b) {
+    int64_t sum = 0;
+    for (int32_t i = block_of(a); i < nbc && bstart[i] < b; ++i) {
+      const int64_t lo = std::max(a, bstart[i]), hi = std::min(b, bstart[i] + blen[i]);
+      if (hi <= lo) continue;
+      const int64_t first = bpos0[i] + (lo - bstart[i]) + 1;  // pos + 1 of token lo
+      sum += (hi - lo) * first + (hi - lo) * (hi - lo - 1) / 2;
     }
-    kt_min[kt] = mn;
-    kt_max[kt] = mx;
+    return sum;
+  };
+  P.pairs = pairs_in(P.n_res, P.n_tot);
+
+  // per key tile: smallest and largest subtree end of its keys (padding keys count as 0)
+  std::vector<int32_t> kt_min(n_kvt, INT32_MAX), kt_max(n_kvt, INT32_MIN);
+  for (int32_t i = 0; i < nbc; ++i) {
+    const int32_t k0 = bstart[i] / kTile, k1 = (bstart[i] + blen[i] - 1) / kTile;
+    for (int32_t kt = k0; kt <= k1; ++kt) {
+      kt_min[kt] = std::min(kt_min[kt], bsend[i]);
+      kt_max[kt] = std::max(kt_max[kt], bsend[i]);
+    }
   }
+  if (P.n_tot % kTile) kt_min[n_kvt - 1] = 0;
 
   // ---- chunks, query tiles, tile lists
   const int32_t n_fwd = P.n_tot - P.n_res;
   P.n_chunks = (n_fwd + max_fwd - 1) / max_fwd;
+  const int32_t n_qt_est = (n_fwd + kTile - 1) / kTile + P.n_chunks;
+  P.qt_row0.reserve(n_qt_est);
+  P.qt_row1.reserve(n_qt_est);
+  P.qt_ent0.reserve(n_qt_est);
+  P.qt_ent1.reserve(n_qt_est);
+  P.qt_order.reserve(n_qt_est);
+  P.ent.reserve((size_t)n_qt_est * 8);
+  std::vector<int32_t> ord;
   for (int32_t c = 0; c < P.n_chunks; ++c) {
     const int32_t q0 = P.n_res + c * max_fwd, q1 = std::min(q0 + max_fwd, P.n_tot);
     P.chunk_q0.push_back(q0);
     P.chunk_q1.push_back(q1);
     P.chunk_t0.push_back((int32_t)P.qt_row0.size());
-    int64_t cp = 0;
-    for (int32_t t = q0; t < q1; ++t) cp += (int64_t)P.pos[t] + 1;
-    P.chunk_pairs.push_back(cp);
+    P.chunk_pairs.push_back(pairs_in(q0, q1));
     const int32_t e_begin = (int32_t)P.ent.size();
     for (int32_t i0 = q0; i0 < q1; i0 += kTile) {
       const int32_t i1 = std::min(i0 + kTile, q1);
@@ -245,7 +284,7 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
           any = kt_max[kt] > i0;
         } else {
           any = false;
-          for (int32_t j = j0; j < i1 && !any; ++j) any = P.send[j] > i0;
+          for (int32_t i = block_of(j0); i < nbc && bstart[i] < i1 && !any; ++i) any = bsend[i] > i0;
         }
         if (!any) continue;
         // every query sees every key: the tile is whole, lies before the
@@ -258,7 +297,7 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
     P.chunk_t1.push_back((int32_t)P.qt_row0.size());
     P.chunk_nent.push_back((int32_t)P.ent.size() - e_begin);
     // longest-first order of the chunk's tiles; equal work keeps tile order
-    std::vector<int32_t> ord(P.chunk_t1[c] - P.chunk_t0[c]);
+    ord.resize(P.chunk_t1[c] - P.chunk_t0[c]);
     std::iota(ord.begin(), ord.end(), P.chunk_t0[c]);
     std::stable_sort(ord.begin(), ord.end(), [&](int32_t a, int32_t b) {
       return P.qt_ent1[a] - P.qt_ent0[a] > P.qt_ent1[b] - P.qt_ent0[b];
@@ -286,12 +325,13 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
     }
   }
 
-  // ---- device image
+  // ---- device image; the per-token tables are written into it directly
+  const size_t n_send = (size_t)n_kvt * kTile;
   size_t w = 16;  // header words
   P.off_pos = w;
-  w = align4(w + P.pos.size());
+  w = align4(w + P.n_tot);
   P.off_send = w;
-  w = align4(w + P.send.size());
+  w = align4(w + n_send);
   P.off_qtile = w;
   w = align4(w + 4 * P.qt_row0.size());
   P.off_ent = w;
@@ -306,8 +346,9 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   w = align4(w + P.r1.size());
   P.off_r2 = w;
   w = align4(w + P.r2.size());
-  P.image.assign(w, 0);
+  P.image.resize(w);
   int32_t *im = P.image.data();
+  std::fill(im, im + 16, 0);
   im[0] = 0x4C505254;  // "TRPL"
   im[1] = P.n_tot;
   im[2] = P.n_res;
@@ -316,8 +357,15 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   im[5] = (int32_t)P.ent.size();
   im[6] = (int32_t)P.slot_tok.size();
   im[7] = P.n_questions;
-  std::copy(P.pos.begin(), P.pos.end(), im + P.off_pos);
-  std::copy(P.send.begin(), P.send.end(), im + P.off_send);
+  int32_t *pos = im + P.off_pos, *send = im + P.off_send;
+  for (int32_t i = 0; i < nbc; ++i) {
+    const int32_t st = bstart[i], len = blen[i], p0 = bpos0[i], se = bsend[i];
+    for (int32_t t = 0; t < len; ++t) {
+      pos[st + t] = p0 + t;
+      send[st + t] = se;
+    }
+  }
+  std::fill(send + P.n_tot, send + n_send, 0);
   for (size_t t = 0; t < P.qt_row0.size(); ++t) {
     int32_t *r = im + P.off_qtile + 4 * t;
     r[0] = P.qt_row0[t];
@@ -337,6 +385,16 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   std::copy(P.slot_tok.begin(), P.slot_tok.end(), im + P.off_slot_tok);
   std::copy(P.r1.begin(), P.r1.end(), im + P.off_r1);
   std::copy(P.r2.begin(), P.r2.end(), im + P.off_r2);
+  // zero the alignment gaps so the image is fully defined
+  auto zero_gap = [&](size_t from, size_t to) { std::fill(im + from, im + to, 0); };
+  zero_gap(P.off_pos + P.n_tot, P.off_send);
+  zero_gap(P.off_qtile + 4 * P.qt_row0.size(), P.off_ent);
+  zero_gap(P.off_ent + P.ent.size(), P.off_order);
+  zero_gap(P.off_order + P.qt_order.size(), P.off_chunk);
+  zero_gap(P.off_chunk + 4 * (size_t)P.n_chunks, P.off_slot_tok);
+  zero_gap(P.off_slot_tok + P.slot_tok.size(), P.off_r1);
+  zero_gap(P.off_r1 + P.r1.size(), P.off_r2);
+  zero_gap(P.off_r2 + P.r2.size(), w);
   return TREE_OK;
 }
 
@@ -439,8 +497,8 @@ int tree_plan_tables(const tree_plan_t *plan, tree_plan_host_view_t *v) {
   v->blk_send = P.blk_send.data();
   v->blk_resident = P.blk_resident.data();
   v->blk_slot = P.blk_slot.data();
-  v->pos = P.pos.data();
-  v->send = P.send.data();
+  v->pos = P.image.data() + P.off_pos;
+  v->send = P.image.data() + P.off_send;
   v->chunk_q0 = P.chunk_q0.data();
   v->chunk_q1 = P.chunk_q1.data();
   v->chunk_t0 = P.chunk_t0.data();
