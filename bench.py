@@ -40,7 +40,7 @@ N_SETS = 4  # rotating input sets: 4 x ~81 MB > 129 MB L2
 
 # DRAM bytes per attention launch from one ncu capture, valid only for the
 # kernel source it was taken on (sha256 of csrc/attn.cu, first 16 hex digits).
-ATTN_TRAFFIC = {}
+ATTN_TRAFFIC = {(2, "9bb954c98db7dab8"): 52661504}
 
 
 def _peaks():
@@ -137,6 +137,9 @@ class Batch:
             self.p_cal = torch.empty((self.nq, stride), device=dev)
             self.choice = torch.empty(self.nq, dtype=torch.int32, device=dev)
         self.chunks = [self.plan.chunk(c) for c in range(i.n_chunks)]
+        # per input set and chunk: the chunk's query / output rows (views made once)
+        self.views = [[(b["q"][ci.q0 - i.n_res: ci.q1 - i.n_res], b["o"][ci.q0 - i.n_res: ci.q1 - i.n_res])
+                       for ci in self.chunks] for b in self.sets]
 
     def step(self, s, stream, replan=True, ev=None, bufs=None):
         """Enqueue one whole-path step on `stream` using input set s (or `bufs`).
@@ -151,8 +154,10 @@ class Batch:
         self.plan.upload(self.pdev, i.dev_bytes, stream)
         b = bufs if bufs is not None else self.sets[s]
         for c, ci in enumerate(self.chunks):
-            r0, r1 = ci.q0 - i.n_res, ci.q1 - i.n_res
-            qv, ov = b["q"][r0:r1], b["o"][r0:r1]
+            if bufs is None:
+                qv, ov = self.views[s][c]
+            else:
+                qv, ov = b["q"][ci.q0 - i.n_res: ci.q1 - i.n_res], b["o"][ci.q0 - i.n_res: ci.q1 - i.n_res]
             lib.tree_rope(self.plan, self.pdev, c, qv, b["k"], w.hq, w.hkv, w.d, self.tab, i.max_pos, stream)
             if ev is not None:
                 pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -169,6 +174,55 @@ class Batch:
 
     def launches_per_step(self):
         return 2 * len(self.chunks) + (1 if self.nq else 0)
+
+
+def measure_rope(lib, torch, B, stream, reps=40):
+    """tree_rope alone over the rotating input sets: algorithmic GB/s."""
+    w, i = B.w, B.info
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for s in range(N_SETS):
+        for c in range(len(B.chunks)):
+            lib.tree_rope(B.plan, B.pdev, c, B.views[s][c][0], B.sets[s]["k"], w.hq, w.hkv, w.d, B.tab, i.max_pos, stream)
+    ev[0].record(stream)
+    for r in range(reps):
+        s = r % N_SETS
+        for c in range(len(B.chunks)):
+            lib.tree_rope(B.plan, B.pdev, c, B.views[s][c][0], B.sets[s]["k"], w.hq, w.hkv, w.d, B.tab, i.max_pos, stream)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / reps
+    # read + write of every forward row of Q and K, plus its position
+    nbytes = 2 * i.n_fwd * (w.hq + w.hkv) * w.d * 2 + 4 * i.n_fwd
+    return ms, nbytes
+
+
+def measure_readout(lib, torch, dev, stream, reps=64):
+    """readout_decide on 65,536 questions, 16 rotating buffer sets (> L2): algorithmic GB/s."""
+    b = synth.draw_readout_batch()
+    nq, stride = len(b["r1"]), b["stride"]
+    sets = []
+    for _ in range(16):
+        sets.append(dict(logits=torch.from_numpy(b["logits"]).to(dev), r1=torch.from_numpy(b["r1"]).to(dev),
+                         r2=torch.from_numpy(b["r2"]).to(dev), n=torch.from_numpy(b["n_letters"]).to(dev),
+                         T=torch.from_numpy(b["temperature"]).to(dev),
+                         pc=torch.empty((nq, stride), device=dev), ch=torch.empty(nq, dtype=torch.int32, device=dev)))
+
+    def run(x):
+        lib.readout_decide(x["logits"], stride, x["r1"], x["r2"], x["n"], x["T"], nq, x["pc"], None, x["ch"], None,
+                           stream)
+    for x in sets:
+        run(x)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record(stream)
+    for r in range(reps):
+        run(sets[r % 16])
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / reps
+    n = b["n_letters"].astype(np.int64)
+    # logits of both orders, r1/r2/n/T, the zero-padded p_cal row, the choice
+    nbytes = int((2 * n * 4).sum() + 16 * nq + 4 * stride * nq + 4 * nq)
+    return ms, nbytes
 
 
 def run_gpu(args):
@@ -284,6 +338,21 @@ def run_gpu(args):
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4)},
         "gpu_launches": B.launches_per_step() * args.steps,
         "clocks": clk,
+    }
+    rope_ms, rope_bytes = measure_rope(lib, torch, B, stream)
+    ro_ms, ro_bytes = measure_readout(lib, torch, dev, stream)
+    line["kernels"] = {
+        "tree_rope": {"bound": "hbm", "us": round(rope_ms * 1e3, 2), "bytes": rope_bytes,
+                      "achieved": round(rope_bytes / rope_ms / 1e6, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                      "frac": round(rope_bytes / rope_ms / 1e6 / peaks["hbm"], 4),
+                      "note": f"{N_SETS} rotating Q/K sets (> L2)"},
+        "readout_decide_65536q": {"bound": "hbm", "us": round(ro_ms * 1e3, 2), "bytes": ro_bytes,
+                                  "achieved": round(ro_bytes / ro_ms / 1e6, 1), "peak": peaks["hbm"],
+                                  "unit": "GB/s", "frac": round(ro_bytes / ro_ms / 1e6 / peaks["hbm"], 4),
+                                  "note": "65,536 questions, 2-10 letters, 16 rotating buffer sets (> L2)"},
+        "tree_attn_fwd": {"bound": "tensor", "us": round(attn_launch_ms * 1e3, 2), "flops": flops_launch,
+                          "achieved": round(achieved, 2), "peak": peaks["tc"], "unit": "TFLOP/s",
+                          "frac": round(achieved / peaks["tc"], 4)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
