@@ -126,6 +126,7 @@ class Batch:
                                   o=torch.empty((i.n_fwd, w.hq, w.d), dtype=torch.float16, device=dev)))
         self.tab = torch.from_numpy(lib.rope_table(i.max_pos, w.d, w.theta)).to(dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.work = torch.zeros(2, dtype=torch.int32, device=dev)  # persistent-CTA work counter
         self.nq = i.n_questions
         if self.nq:
             stride = w.letter_stride
@@ -163,7 +164,7 @@ class Batch:
                 pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 pair[0].record(stream)
             lib.tree_attn_fwd(self.plan, self.pdev, c, qv, b["k"], b["v"], ov, None, w.hq, w.hkv, w.d,
-                              status=self.status, stream=stream)
+                              status=self.status, stream=stream, work=self.work)
             if ev is not None:
                 pair[1].record(stream)
                 ev.append(pair)
@@ -257,8 +258,10 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
+    h0 = time.perf_counter()
     for s in range(args.steps):
         B.step(s % N_SETS, stream, ev=evs)
+    host_ms = (time.perf_counter() - h0) * 1e3
     t1.record(stream)
     torch.cuda.synchronize()
     total_ms = t0.elapsed_time(t1)
@@ -337,6 +340,7 @@ def run_gpu(args):
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4)},
         "gpu_launches": B.launches_per_step() * args.steps,
+        "host_enqueue_ms_per_step": round(host_ms / args.steps, 4),
         "clocks": clk,
     }
     rope_ms, rope_bytes = measure_rope(lib, torch, B, stream)

@@ -227,6 +227,12 @@ TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev, int32_t ch
 typedef struct {
   int32_t hq, hkv, d;  /* query heads, kv heads (hq % hkv == 0, q head h reads kv head h/(hq/hkv)), d in {64,128} */
   float scale;         /* scores are q.k * scale; 0 = 1/sqrt(d) (AstrAI inference page, "KV Cache") */
+  int32_t *work;       /* device int32[2], or NULL.  Work counter of the persistent CTAs: when given,
+                          CTAs take (query tile, kv head) items in longest-first order as they free
+                          up; it must hold {0, 0} before the first call and each call leaves it at
+                          {0, 0} (the last CTA resets it), so calls on one stream can reuse it;
+                          calls that may overlap on the GPU need separate counters.  NULL: each CTA
+                          takes a fixed round-robin share of the items (no scratch memory). */
 } tree_attn_params_t;
 
 /*

@@ -85,7 +85,8 @@ class _View(C.Structure):
 
 
 class AttnParams(C.Structure):
-    _fields_ = [("hq", C.c_int32), ("hkv", C.c_int32), ("d", C.c_int32), ("scale", C.c_float)]
+    _fields_ = [("hq", C.c_int32), ("hkv", C.c_int32), ("d", C.c_int32), ("scale", C.c_float),
+                ("work", C.c_void_p)]
 
 
 _vp = C.c_void_p
@@ -225,8 +226,8 @@ def tree_rope(plan: Plan, plan_dev, chunk: int, q, k, hq: int, hkv: int, d: int,
 
 
 def tree_attn_fwd(plan: Plan, plan_dev, chunk: int, q, k, v, o, lse, hq: int, hkv: int, d: int,
-                  scale: float = 0.0, status=None, stream=None):
-    p = AttnParams(hq, hkv, d, scale)
+                  scale: float = 0.0, status=None, stream=None, work=None):
+    p = AttnParams(hq, hkv, d, scale, _ptr(work))
     _check(_lib.tree_attn_fwd(plan.handle, _ptr(plan_dev), chunk, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                               _ptr(lse), C.byref(p), _ptr(status), _stream(stream)))
 

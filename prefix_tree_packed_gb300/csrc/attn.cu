@@ -66,6 +66,8 @@ struct AttnArgs {
   float *lse;
   int32_t *status;
   int32_t t0, q0, n_tot, hq, hkv, ratio;
+  int32_t n_items;  // query tiles of the chunk x kv heads x q-head groups
+  int32_t *work;    // {next item, finished CTAs} or nullptr for the round-robin schedule
   float scale_log2;
 };
 
@@ -73,8 +75,10 @@ template <int D, int NH>
 struct Cfg {
   static constexpr int CB = D / 64;               // 64-column boxes per row of a tile
   static constexpr int STAGES = D == 64 ? 3 : 2;  // K/V ring depth
+  static constexpr int QBUF = D == 64 ? 2 : 1;    // Q tiles in flight (next item's Q loads early)
+  static constexpr uint32_t Q_BYTES = NH * CB * BOX_BYTES;
   static constexpr uint32_t Q_OFF = 0;
-  static constexpr uint32_t K_OFF = Q_OFF + NH * CB * BOX_BYTES;
+  static constexpr uint32_t K_OFF = Q_OFF + QBUF * Q_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + STAGES * CB * BOX_BYTES;
   static constexpr uint32_t SEND_OFF = V_OFF + STAGES * CB * BOX_BYTES;
   static constexpr uint32_t SMEM = SEND_OFF + STAGES * 512 + 1024;  // + alignment slack
@@ -92,10 +96,14 @@ struct Cfg {
   static constexpr int SERVICE_REGS = 88;
 };
 
+constexpr int kRing = 4;  // items handed from the producer to the MMA and softmax warps
+
 struct Bars {
-  uint64_t q_full;
+  uint64_t item_full[kRing], item_empty[kRing];
+  int32_t ring[kRing];
+  uint64_t q_full[2], q_empty[2];
   uint64_t k_full[3], v_full[3], kv_empty[3];
-  uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
+  uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
   uint32_t tmem;
   int32_t abort;
 };
@@ -120,12 +128,42 @@ TREE_DEV bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort, i
   }
 }
 
-// Warp-uniform form for the softmax warps, whose next steps are warp-collective.
+// Warp-uniform form: the next steps of the caller are warp-collective.
 TREE_DEV bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *status) {
   const bool ok = wait_bar(bar, parity, abort, status);
   return __all_sync(0xffffffffu, ok);
 }
 
+// One work item: a query tile, the kv head g, and the NH q heads h0.. that read it.
+struct Item {
+  QTile qt;
+  int n;   // key tiles in its list
+  int h0;  // first q head
+  int g;   // kv head
+};
+
+template <int NH>
+TREE_DEV Item item_at(const AttnArgs &a, int w) {
+  const int groups = a.ratio / NH;
+  const int per_tile = a.hkv * groups;
+  const int rank = w / per_tile;
+  const int rem = w - rank * per_tile;
+  Item it;
+  it.g = rem / groups;
+  it.h0 = it.g * a.ratio + (rem - it.g * groups) * NH;
+  it.qt = a.qtiles[__ldg(a.order + a.t0 + rank)];
+  it.n = it.qt.ent1 - it.qt.ent0;
+  return it;
+}
+
+// Persistent CTAs (one per SM).  The producer warp takes items from the
+// longest-first item list -- with a work counter, the next unclaimed item as the
+// CTA frees up; without one, items c, c + G, c + 2G, ... (G = grid size) -- and
+// hands them to the MMA and softmax warps through a small ring in shared memory.
+// Tiles are numbered across the CTA's items in the order it processes them;
+// every barrier phase follows that count (or the item count for per-item
+// barriers), so the producer and MMA warps run ahead into the next item while
+// the softmax warps finish the current one.
 template <int D, int NH>
 __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     tree_attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -136,19 +174,13 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(sm);
   const int32_t *sSend = reinterpret_cast<const int32_t *>(sm + C::SEND_OFF);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pairs = a.ratio / NH;
-  const int per_tile = a.hkv * pairs;
-  const int rank = blockIdx.x / per_tile;
-  const int rem = blockIdx.x - rank * per_tile;
-  const int g = rem / pairs;
-  const int h0 = g * a.ratio + (rem - g * pairs) * NH;
-  const QTile qt = a.qtiles[__ldg(a.order + a.t0 + rank)];
-  const int n = qt.ent1 - qt.ent0;
   volatile int32_t *abort = &bars.abort;
 
-  const uint32_t b_q = smem_u32(&bars.q_full);
+  auto b_if = [&](int r) { return smem_u32(&bars.item_full[r]); };
+  auto b_ie = [&](int r) { return smem_u32(&bars.item_empty[r]); };
+  auto b_qf = [&](int b) { return smem_u32(&bars.q_full[b]); };
+  auto b_qe = [&](int b) { return smem_u32(&bars.q_empty[b]); };
   auto b_k = [&](int s) { return smem_u32(&bars.k_full[s]); };
   auto b_v = [&](int s) { return smem_u32(&bars.v_full[s]); };
   auto b_e = [&](int s) { return smem_u32(&bars.kv_empty[s]); };
@@ -156,9 +188,17 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   auto b_f = [&](int h) { return smem_u32(&bars.s_free[h]); };
   auto b_p = [&](int h) { return smem_u32(&bars.p_full[h]); };
   auto b_o = [&](int h) { return smem_u32(&bars.o_done[h]); };
+  auto b_of = [&](int h) { return smem_u32(&bars.o_free[h]); };
 
   if (threadIdx.x == 0) {
-    mbar_init(b_q, 1);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(b_if(r), 1);
+      mbar_init(b_ie(r), NH * 128 + 1);  // every softmax thread and the MMA warp
+    }
+    for (int b = 0; b < C::QBUF; ++b) {
+      mbar_init(b_qf(b), 1);
+      mbar_init(b_qe(b), 1);
+    }
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(b_k(s), 1);
       mbar_init(b_v(s), 1);
@@ -169,6 +209,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       mbar_init(b_f(h), 128);
       mbar_init(b_p(h), 128);
       mbar_init(b_o(h), 1);
+      mbar_init(b_of(h), 128);
     }
     bars.abort = 0;
     mbar_fence_init();
@@ -178,59 +219,85 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = bars.tmem;
+  volatile int32_t *ring = bars.ring;
 
   if (warp >= 4 * NH) {
     if (NH == 2) regs_dec<C::SERVICE_REGS>();
-    if (warp == C::PROD_WARP && n > 0) {
+    if (warp == C::PROD_WARP) {
       // ---------------------------------------------------------- producer (whole warp, one lane issues)
       if (elect_one()) {
         prefetch_map(&mq);
         prefetch_map(&mk);
         prefetch_map(&mv);
-        mbar_expect_tx(b_q, NH * C::CB * BOX_BYTES);
-#pragma unroll
-        for (int h = 0; h < NH; ++h)
-#pragma unroll
-          for (int c = 0; c < C::CB; ++c)
-            tma_load_2d(s_base + C::Q_OFF + (h * C::CB + c) * BOX_BYTES, &mq, (h0 + h) * D + 64 * c, qt.row0 - a.q0,
-                        b_q);
       }
       __syncwarp();
-      int issued = 0;
-      for (int i = 0; i < n; ++i) {
-        const int st = i % C::STAGES;
-        if (i >= C::STAGES && !wait_bar_warp(b_e(st), ((i / C::STAGES) - 1) & 1, abort, a.status)) break;
-        const int j0 = (__ldg(a.ent + qt.ent0 + i) >> 1) * BN;
+      int t = 0, j = 0, fetched = 0;
+      bool ok = true;
+      while (ok) {
+        // claim the next item and publish it in the ring (a value >= n_items ends the list)
+        const int slot = fetched % kRing;
+        if (fetched >= kRing && !(ok = wait_bar_warp(b_ie(slot), ((fetched / kRing) - 1) & 1, abort, a.status)))
+          break;
+        int w = 0;
+        if (lane == 0) {
+          w = a.work ? atomicAdd(a.work, 1) : (int)blockIdx.x + fetched * (int)gridDim.x;
+          ring[slot] = w;
+          mbar_arrive(b_if(slot));
+        }
+        w = __shfl_sync(0xffffffffu, w, 0);
+        ++fetched;
+        if (w >= a.n_items) break;
+        const Item it = item_at<NH>(a, w);
+        if (it.n <= 0) continue;  // (a plan never makes one: every query tile sees its own rows)
+        const int b = j % C::QBUF;
+        if (j >= C::QBUF && !(ok = wait_bar_warp(b_qe(b), ((j / C::QBUF) - 1) & 1, abort, a.status))) break;
         if (elect_one()) {
-          mbar_expect_tx(b_k(st), C::CB * BOX_BYTES + 512);
+          mbar_expect_tx(b_qf(b), C::Q_BYTES);
 #pragma unroll
-          for (int c = 0; c < C::CB; ++c)
-            tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES, &mk, g * D + 64 * c, j0, b_k(st));
-          bulk_load(s_base + C::SEND_OFF + st * 512, a.send + j0, 512, b_k(st));
-          mbar_expect_tx(b_v(st), C::CB * BOX_BYTES);
+          for (int h = 0; h < NH; ++h)
 #pragma unroll
-          for (int c = 0; c < C::CB; ++c)
-            tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, g * D + 64 * c, j0, b_v(st));
+            for (int c = 0; c < C::CB; ++c)
+              tma_load_2d(s_base + C::Q_OFF + b * C::Q_BYTES + (h * C::CB + c) * BOX_BYTES, &mq,
+                          (it.h0 + h) * D + 64 * c, it.qt.row0 - a.q0, b_qf(b));
         }
         __syncwarp();
-        issued = i + 1;
+        for (int i = 0; i < it.n; ++i, ++t) {
+          const int st = t % C::STAGES;
+          if (t >= C::STAGES && !(ok = wait_bar_warp(b_e(st), ((t / C::STAGES) - 1) & 1, abort, a.status))) break;
+          const int j0 = (__ldg(a.ent + it.qt.ent0 + i) >> 1) * BN;
+          if (elect_one()) {
+            mbar_expect_tx(b_k(st), C::CB * BOX_BYTES + 512);
+#pragma unroll
+            for (int c = 0; c < C::CB; ++c)
+              tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES, &mk, it.g * D + 64 * c, j0, b_k(st));
+            bulk_load(s_base + C::SEND_OFF + st * 512, a.send + j0, 512, b_k(st));
+            mbar_expect_tx(b_v(st), C::CB * BOX_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::CB; ++c)
+              tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, it.g * D + 64 * c, j0, b_v(st));
+          }
+          __syncwarp();
+        }
+        ++j;
       }
       // wind down: every copy issued must have landed before the CTA exits
-      wait_bar(b_q, 0, abort, nullptr, false, kDrainNs);
-      for (int i = (issued > C::STAGES ? issued - C::STAGES : 0); i < issued; ++i) {
-        wait_bar(b_k(i % C::STAGES), (i / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
-        wait_bar(b_v(i % C::STAGES), (i / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
+      for (int u = (t > C::STAGES ? t - C::STAGES : 0); u < t; ++u) {
+        wait_bar(b_k(u % C::STAGES), (u / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
+        wait_bar(b_v(u % C::STAGES), (u / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
       }
-    } else if (warp == C::MMA_WARP && n > 0) {
+      for (int u = (j > C::QBUF ? j - C::QBUF : 0); u < j; ++u)
+        wait_bar(b_qf(u % C::QBUF), (u / C::QBUF) & 1, abort, nullptr, false, kDrainNs);
+    } else if (warp == C::MMA_WARP) {
       // ---------------------------------------------------------- MMA issuer (whole warp, one lane issues)
       constexpr uint32_t idesc_qk = idesc_f16(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, D, true);
-      auto issue_qk = [&](int h, int st) {
+      auto issue_qk = [&](int h, int qb, int st) {
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-            const uint64_t da = sdesc_sw128(s_base + C::Q_OFF + h * C::CB * BOX_BYTES + off, 16, 1024);
+            const uint64_t da =
+                sdesc_sw128(s_base + C::Q_OFF + qb * C::Q_BYTES + h * C::CB * BOX_BYTES + off, 16, 1024);
             const uint64_t db = sdesc_sw128(s_base + C::K_OFF + st * C::CB * BOX_BYTES + off, 16, 1024);
             mma_ss(tmem + 128 * h, da, db, idesc_qk, kk > 0);
           }
@@ -238,193 +305,250 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         }
         __syncwarp();
       };
-      auto issue_pv = [&](int h, int st, int i) {
+      auto issue_pv = [&](int h, int st, bool accumulate) {
         const uint32_t p_col = C::PSEP ? C::P_COL + 64 * h : 128 * h;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint64_t db =
                 sdesc_sw128(s_base + C::V_OFF + st * C::CB * BOX_BYTES + kk * 2048, BOX_BYTES, 1024);
-            mma_ts(tmem + C::O_COL + D * h, tmem + p_col + 8 * kk, db, idesc_pv, (i > 0 || kk > 0));
+            mma_ts(tmem + C::O_COL + D * h, tmem + p_col + 8 * kk, db, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
           }
           mma_commit(b_o(h));
         }
         __syncwarp();
       };
-      bool ok = wait_bar_warp(b_q, 0, abort, a.status) && wait_bar_warp(b_k(0), 0, abort, a.status);
-      int last_o = -1, last_h = 0;  // iteration and head of the last PV commit issued
-      if (ok) {
-        fence_after();
-        for (int h = 0; h < NH; ++h) issue_qk(h, 0);
-        for (int i = 0; i < n && ok; ++i) {
-          const int st = i % C::STAGES;
-          const int st2 = (i + 1) % C::STAGES;
-          if (C::PSEP) {
-            // next S first: S_h is free once the softmax has read it into registers
-            if (i + 1 < n) {
-              if (!(ok = wait_bar_warp(b_k(st2), ((i + 1) / C::STAGES) & 1, abort, a.status))) break;
-              for (int h = 0; h < NH && ok; ++h) {
-                if (!(ok = wait_bar_warp(b_f(h), i & 1, abort, a.status))) break;
-                fence_after();
-                issue_qk(h, st2);
-              }
-              if (!ok) break;
-            }
-            if (!(ok = wait_bar_warp(b_v(st), (i / C::STAGES) & 1, abort, a.status))) break;
-            for (int h = 0; h < NH && ok; ++h) {
-              if (!(ok = wait_bar_warp(b_p(h), i & 1, abort, a.status))) break;
-              fence_after();
-              issue_pv(h, st, i);
-              last_o = i;
-              last_h = h;
-            }
-            if (ok && i + C::STAGES < n) {
-              if (elect_one()) mma_commit(b_e(st));
-              __syncwarp();
-            }
-          } else {
-            // P_h shares S_h's columns: per head, PV(i) then (once it is done) S(i+1)
-            if (!(ok = wait_bar_warp(b_v(st), (i / C::STAGES) & 1, abort, a.status))) break;
-            for (int h = 0; h < NH && ok; ++h) {
-              if (!(ok = wait_bar_warp(b_p(h), i & 1, abort, a.status))) break;
-              fence_after();
-              issue_pv(h, st, i);
-              last_o = i;
-              last_h = h;
-              if (h == NH - 1 && i + C::STAGES < n) {
-                if (elect_one()) mma_commit(b_e(st));
-                __syncwarp();
-              }
-              if (i + 1 < n) {
-                if (h == 0 && !(ok = wait_bar_warp(b_k(st2), ((i + 1) / C::STAGES) & 1, abort, a.status))) break;
-                if (!(ok = wait_bar_warp(b_o(h), i & 1, abort, a.status))) break;
-                fence_after();
-                issue_qk(h, st2);
-              }
-            }
-          }
+      auto commit = [&](uint32_t bar) {
+        if (elect_one()) mma_commit(bar);
+        __syncwarp();
+      };
+      // items from the ring, in order; skips items without key tiles
+      int taken = 0;
+      auto next_item = [&](Item &out) -> int {  // 1: item, 0: list ended, -1: gave up
+        for (;;) {
+          const int slot = taken % kRing;
+          if (!wait_bar_warp(b_if(slot), (taken / kRing) & 1, abort, a.status)) return -1;
+          const int w = ring[slot];
+          __syncwarp();
+          if (elect_one()) mbar_arrive(b_ie(slot));
+          __syncwarp();
+          ++taken;
+          if (w >= a.n_items) return 0;
+          out = item_at<NH>(a, w);
+          if (out.n > 0) return 1;
+        }
+      };
+      Item cur;
+      int got = next_item(cur);
+      bool ok = got >= 0;
+      int jc = 0, ic = 0, T = 0, last_qk = -1;
+      // prologue: S of the first tile
+      if (got == 1) {
+        ok = wait_bar_warp(b_qf(0), 0, abort, a.status) && wait_bar_warp(b_k(0), 0, abort, a.status);
+        if (ok) {
+          fence_after();
+          for (int h = 0; h < NH; ++h) issue_qk(h, 0, 0);
+          last_qk = 0;
+          if (cur.n == 1) commit(b_qe(0));
         }
       }
-      // wind down: all issued MMAs complete before tensor memory is freed
-      if (last_o >= 0) wait_bar(b_o(last_h), last_o & 1, abort, nullptr, false, kDrainNs);
+      while (ok && got == 1) {
+        // the tile after T: the next tile of this item, or the first of the next item
+        int jn = jc, in = ic + 1;
+        Item nxt = cur;
+        bool has_next = in < cur.n;
+        if (!has_next) {
+          const int g2 = next_item(nxt);
+          if (g2 < 0) {
+            ok = false;
+            break;
+          }
+          has_next = g2 == 1;
+          in = 0;
+          jn = jc + 1;
+        }
+        const int qbn = jn % C::QBUF, stn = (T + 1) % C::STAGES;
+        // operands of the next S: its Q tile (first tile of an item) and its K tile
+        auto wait_next_operands = [&]() {
+          if (in == 0 && !wait_bar_warp(b_qf(qbn), (jn / C::QBUF) & 1, abort, a.status)) return false;
+          return wait_bar_warp(b_k(stn), ((T + 1) / C::STAGES) & 1, abort, a.status);
+        };
+        if (C::PSEP && has_next) {
+          if (!(ok = wait_next_operands())) break;
+          // next S first: S_h is free once the softmax has read it into registers
+          for (int h = 0; h < NH && ok; ++h) {
+            if (!(ok = wait_bar_warp(b_f(h), T & 1, abort, a.status))) break;
+            fence_after();
+            issue_qk(h, qbn, stn);
+            last_qk = T + 1;
+          }
+          if (!ok) break;
+          if (in == nxt.n - 1) commit(b_qe(qbn));
+        }
+        const int st = T % C::STAGES;
+        if (!(ok = wait_bar_warp(b_v(st), (T / C::STAGES) & 1, abort, a.status))) break;
+        for (int h = 0; h < NH && ok; ++h) {
+          if (!(ok = wait_bar_warp(b_p(h), T & 1, abort, a.status))) break;
+          // a new item's first PV overwrites O_h: its previous values must have been read
+          if (ic == 0 && jc > 0 && !(ok = wait_bar_warp(b_of(h), (jc - 1) & 1, abort, a.status))) break;
+          fence_after();
+          issue_pv(h, st, ic > 0);
+          if (!C::PSEP && has_next) {
+            // P_h shares S_h's columns: the next S_h waits until this PV has read P_h
+            if (h == 0 && !(ok = wait_next_operands())) break;
+            if (!(ok = wait_bar_warp(b_o(h), T & 1, abort, a.status))) break;
+            fence_after();
+            issue_qk(h, qbn, stn);
+            last_qk = T + 1;
+          }
+        }
+        if (!ok) break;
+        if (!C::PSEP && has_next && in == nxt.n - 1) commit(b_qe(qbn));
+        commit(b_e(st));
+        ++T;
+        if (!has_next) break;
+        jc = jn;
+        ic = in;
+        cur = nxt;
+      }
+      // wind down: every issued MMA (and the commits after it) has completed
+      // before tensor memory is freed
+      if (T > 0) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) wait_bar(b_o(h), (T - 1) & 1, abort, nullptr, false, kDrainNs);
+        for (int u = (T > C::STAGES ? T - C::STAGES : 0); u < T; ++u)
+          wait_bar(b_e(u % C::STAGES), (u / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
+      }
+      if (!ok && last_qk >= 0) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) wait_bar(b_s(h), last_qk & 1, abort, nullptr, false, kDrainNs);
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     if (NH == 2) regs_inc<C::SOFTMAX_REGS>();
     const int h = warp >> 2;
     const int r = 32 * (warp & 3) + lane;
-    const int iq = qt.row0 + r;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t tS = t_lane + 128 * h;
     const uint32_t tP = C::PSEP ? t_lane + C::P_COL + 64 * h : tS;
     const uint32_t tO = t_lane + C::O_COL + D * h;
-    float m = -INFINITY, l = 0.f;
     bool ok = true;
-    int done = 0;
-    for (int i = 0; i < n; ++i) {
-      const int st = i % C::STAGES;
-      const int e = __ldg(a.ent + qt.ent0 + i);
-      if (!(ok = wait_bar_warp(b_s(h), i & 1, abort, a.status))) break;
-      fence_after();
-      uint32_t s[128];
-      tmem_ld32(tS + 0, s);
-      tmem_ld32(tS + 32, s + 32);
-      tmem_ld32(tS + 64, s + 64);
-      tmem_ld32(tS + 96, s + 96);
-      tmem_wait_ld();
-      if (C::PSEP) {
-        fence_before();
-        mbar_arrive(b_f(h));  // S_h may be overwritten by the next QK
-      }
-      if (e & 1) {
-        // partial tile: key j = j0 + c is visible iff j <= iq < send[j]
-        if (!(ok = wait_bar_warp(b_k(st), (i / C::STAGES) & 1, abort, a.status))) break;
-        const int cmax = iq - (e >> 1) * BN;  // keys c <= cmax are not after the query
-        const int4 *sd = reinterpret_cast<const int4 *>(sSend + st * 128);
+    int T = 0;
+    for (int taken = 0; ok; ++taken) {
+      const int slot = taken % kRing;
+      if (!(ok = wait_bar_warp(b_if(slot), (taken / kRing) & 1, abort, a.status))) break;
+      const int w = ring[slot];
+      mbar_arrive(b_ie(slot));
+      if (w >= a.n_items) break;
+      const Item it = item_at<NH>(a, w);
+      if (it.n <= 0) continue;
+      const int iq = it.qt.row0 + r;
+      float m = -INFINITY, l = 0.f;
+      for (int i = 0; i < it.n; ++i, ++T) {
+        const int st = T % C::STAGES;
+        const int e = __ldg(a.ent + it.qt.ent0 + i);
+        if (!(ok = wait_bar_warp(b_s(h), T & 1, abort, a.status))) break;
+        fence_after();
+        uint32_t s[128];
+        tmem_ld32(tS + 0, s);
+        tmem_ld32(tS + 32, s + 32);
+        tmem_ld32(tS + 64, s + 64);
+        tmem_ld32(tS + 96, s + 96);
+        tmem_wait_ld();
+        if (C::PSEP) {
+          fence_before();
+          mbar_arrive(b_f(h));  // S_h may be overwritten by the next QK
+        }
+        if (e & 1) {
+          // partial tile: key j = j0 + c is visible iff j <= iq < send[j]
+          if (!(ok = wait_bar_warp(b_k(st), (T / C::STAGES) & 1, abort, a.status))) break;
+          const int cmax = iq - (e >> 1) * BN;  // keys c <= cmax are not after the query
+          const int4 *sd = reinterpret_cast<const int4 *>(sSend + st * 128);
 #pragma unroll
-        for (int c4 = 0; c4 < 32; ++c4) {
-          const int4 se = sd[c4];
-          const int sv[4] = {se.x, se.y, se.z, se.w};
+          for (int c4 = 0; c4 < 32; ++c4) {
+            const int4 se = sd[c4];
+            const int sv[4] = {se.x, se.y, se.z, se.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = 4 * c4 + u;
-            if (!((c <= cmax) && (iq < sv[u]))) s[c] = __float_as_uint(-INFINITY);
+            for (int u = 0; u < 4; ++u) {
+              const int c = 4 * c4 + u;
+              if (!((c <= cmax) && (iq < sv[u]))) s[c] = __float_as_uint(-INFINITY);
+            }
           }
         }
-      }
-      float mx8[8];
+        float mx8[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+        for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float mt = mx * a.scale_log2;  // -inf stays -inf (scale > 0)
-      const bool grow = mt > m + 8.f;      // also true for the first finite maximum
-      float alpha = 1.f;
-      if (grow) {
-        alpha = ex2(m - mt);  // 0 when m is -inf
-        m = mt;
-      }
-      const float mu = (m == -INFINITY) ? 0.f : m;
-      float sum8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) sum8[u] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float p0 = ex2(fmaf(__uint_as_float(s[c]), a.scale_log2, -mu));
-        const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), a.scale_log2, -mu));
-        sum8[(c >> 1) & 7] += p0 + p1;
-        s[c >> 1] = pack_f16x2(p0, p1);
-      }
-      l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
-      // PV_h(i-1) must be done before P_h is rewritten (separate P) or O_h is rescaled
-      const bool need_o = i > 0 && __any_sync(0xffffffffu, grow);
-      if (i > 0 && (C::PSEP || need_o)) {
-        if (!(ok = wait_bar_warp(b_o(h), (i - 1) & 1, abort, a.status))) break;
-        fence_after();
-      }
-      tmem_st32(tP + 0, s);
-      tmem_st32(tP + 32, s + 32);
-      if (need_o) {
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-          tmem_st32(tO + 32 * c, o);
+        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mt = mx * a.scale_log2;  // -inf stays -inf (scale > 0)
+        const bool grow = mt > m + 8.f;      // also true for the first finite maximum
+        float alpha = 1.f;
+        if (grow) {
+          alpha = ex2(m - mt);  // 0 when m is -inf
+          m = mt;
         }
-      }
-      tmem_wait_st();
-      fence_before();
-      mbar_arrive(b_p(h));
-      done = i + 1;
-    }
-    // ---- epilogue: O / l -> f16 rows of the chunk's output
-    if (ok && done == n && n > 0 && wait_bar_warp(b_o(h), (n - 1) & 1, abort, a.status)) {
-      fence_after();
-      const bool valid = iq < qt.row1;
-      const float inv = 1.f / l;
-      __half *dst = a.o + ((size_t)(iq - a.q0) * a.hq + (h0 + h)) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32 * c, o);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          pk[u] = pack_f16x2(__uint_as_float(o[2 * u]) * inv, __uint_as_float(o[2 * u + 1]) * inv);
-        if (valid) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
-      }
-      if (valid && a.lse) {
         const float mu = (m == -INFINITY) ? 0.f : m;
-        a.lse[(size_t)(iq - a.q0) * a.hq + h0 + h] = (mu + __log2f(l)) * 0.69314718055994531f;
+        float sum8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sum8[u] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[c]), a.scale_log2, -mu));
+          const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), a.scale_log2, -mu));
+          sum8[(c >> 1) & 7] += p0 + p1;
+          s[c >> 1] = pack_f16x2(p0, p1);
+        }
+        l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+        // PV_h of the previous tile of this item must be done before P_h is
+        // rewritten (separate P) or O_h is rescaled; for an item's first tile the
+        // previous item's epilogue has already waited for it
+        const bool need_o = i > 0 && __any_sync(0xffffffffu, grow);
+        if (i > 0 && (C::PSEP || need_o)) {
+          if (!(ok = wait_bar_warp(b_o(h), (T - 1) & 1, abort, a.status))) break;
+          fence_after();
+        }
+        tmem_st32(tP + 0, s);
+        tmem_st32(tP + 32, s + 32);
+        if (need_o) {
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+            tmem_st32(tO + 32 * c, o);
+          }
+        }
+        tmem_wait_st();
+        fence_before();
+        mbar_arrive(b_p(h));
+      }
+      if (!ok) break;
+      // ---- item epilogue: read O_h, hand its columns back, then O / l -> f16 rows
+      if (!(ok = wait_bar_warp(b_o(h), (T - 1) & 1, abort, a.status))) break;
+      fence_after();
+      uint32_t o[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, o + 32 * c);
+      tmem_wait_ld();
+      fence_before();
+      mbar_arrive(b_of(h));
+      if (iq < it.qt.row1) {
+        const float inv = 1.f / l;
+        uint4 *d4 = reinterpret_cast<uint4 *>(a.o + ((size_t)(iq - a.q0) * a.hq + (it.h0 + h)) * D);
+#pragma unroll
+        for (int u = 0; u < D / 8; ++u)
+          d4[u] = make_uint4(pack_f16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv),
+                             pack_f16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv),
+                             pack_f16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv),
+                             pack_f16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv));
+        if (a.lse) {
+          const float mu = (m == -INFINITY) ? 0.f : m;
+          a.lse[(size_t)(iq - a.q0) * a.hq + it.h0 + h] = (mu + __log2f(l)) * 0.69314718055994531f;
+        }
       }
     }
   }
@@ -433,6 +557,14 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   if (warp == C::MMA_WARP) {
     fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (a.work && threadIdx.x == 0) {
+    // the last CTA to finish (all claims are done by then) resets the counter
+    __threadfence();
+    if (atomicAdd(a.work + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(a.work, 0);
+      atomicExch(a.work + 1, 0);
+    }
   }
 }
 
@@ -465,7 +597,7 @@ int make_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows) {
 
 template <int D, int NH>
 int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const void *k, const void *v, void *o,
-              float *lse, int hq, int hkv, float scale, int32_t *status, cudaStream_t s) {
+              float *lse, int hq, int hkv, float scale, int32_t *work, int32_t *status, cudaStream_t s) {
   using C = Cfg<D, NH>;
   static bool attr_set = false;
   auto kern = tree_attn_tc<D, NH>;
@@ -496,7 +628,10 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
   a.ratio = hq / hkv;
   a.scale_log2 = scale * 1.4426950408889634f;
   const int tiles = P.chunk_t1[chunk] - P.chunk_t0[chunk];
-  const dim3 grid((unsigned)(tiles * hkv * (a.ratio / NH)));
+  a.n_items = tiles * hkv * (a.ratio / NH);
+  a.work = work;
+  if (a.n_items == 0) return TREE_OK;
+  const dim3 grid((unsigned)std::min(a.n_items, sm_count()));
   kern<<<grid, C::THREADS, C::SMEM, s>>>(mq, mk, mv, a);
   return launch_status("tree_attn_fwd");
 }
@@ -518,13 +653,15 @@ extern "C" TREE_API int tree_attn_fwd(const tree_plan_t *plan, const void *plan_
   if (d != 64 && d != 128) return fail(TREE_ERR_UNSUPPORTED, "tree_attn_fwd: head dim %d not in {64, 128}", d);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(plan_dev))
     return fail(TREE_ERR_UNSUPPORTED, "tree_attn_fwd: tensors must be 16-byte aligned");
+  if (params->work && (reinterpret_cast<uintptr_t>(params->work) & 7))
+    return fail(TREE_ERR_UNSUPPORTED, "tree_attn_fwd: work counter must be 8-byte aligned");
   const float scale = params->scale > 0.f ? params->scale : 1.f / std::sqrt((float)d);
   const int32_t *img = reinterpret_cast<const int32_t *>(plan_dev);
   const cudaStream_t s = as_stream(stream);
   const bool pair = (hq / hkv) % 2 == 0;
   if (d == 64)
-    return pair ? launch_tc<64, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, status, s)
-                : launch_tc<64, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, status, s);
-  return pair ? launch_tc<128, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, status, s)
-              : launch_tc<128, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, status, s);
+    return pair ? launch_tc<64, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s)
+                : launch_tc<64, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s);
+  return pair ? launch_tc<128, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s)
+              : launch_tc<128, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s);
 }

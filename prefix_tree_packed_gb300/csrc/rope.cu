@@ -14,10 +14,10 @@
 // would put ~2e-3 rad of error on the angle at position 32k.
 //
 // The kernel is a streaming pass over the chunk's Q rows and K rows: one
-// thread rotates 8 pairs of one head (two 16-byte loads and stores), threads of
-// a warp cover consecutive pairs and heads of a row, so every access is a full
-// 32-byte sector; the table stays in L1/L2.  Grid-stride over a grid of
-// (SMs x 8) blocks.
+// thread rotates 8 pairs of one head (two 16-byte loads and stores) in each of
+// 4 consecutive token rows, issuing the loads of all 4 rows before any store;
+// threads of a warp cover consecutive pairs and heads of a row, so every access
+// is a full 32-byte sector; the cos/sin table stays in L1/L2.
 
 #include <cmath>
 
@@ -44,38 +44,48 @@ __device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float4 *cs) 
   }
 }
 
-__global__ void __launch_bounds__(256) rope_kernel(__half *__restrict__ q, __half *__restrict__ k,
-                                                   const int32_t *__restrict__ pos, int32_t q0, int32_t nrows,
-                                                   int hq, int hkv, int d, const float *__restrict__ cos_sin,
-                                                   int32_t max_pos) {
-  const int per_head = d / 16;  // threads per head: 8 pairs each
-  const int64_t q_items = (int64_t)nrows * hq * per_head;
-  const int64_t total = q_items + (int64_t)nrows * hkv * per_head;
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
-       t += (int64_t)gridDim.x * blockDim.x) {
-    __half *base;
-    int64_t r, rem;
-    if (t < q_items) {
-      r = t / (hq * per_head);
-      rem = t - r * (hq * per_head);
-      base = q + (size_t)r * hq * d;
-    } else {
-      const int64_t u = t - q_items;
-      r = u / (hkv * per_head);
-      rem = u - r * (hkv * per_head);
-      base = k + (size_t)(q0 + r) * hkv * d;
+constexpr int kRopeMaxThreads = 512;
+constexpr int kRopeRows = 4;  // token rows per block: loads of 4 rows are in flight per thread
+
+// Block (x, y): token rows [kRopeRows * x, +kRopeRows) of the chunk, items
+// [blockDim.x * y, +blockDim.x) of a row, where a row's items are (q heads, then kv
+// heads) x (d/16 groups of 8 pairs).  A thread keeps the same item for all its
+// rows, so the index arithmetic is done once.
+__global__ void __launch_bounds__(kRopeMaxThreads) rope_kernel(__half *__restrict__ q, __half *__restrict__ k,
+                                                            const int32_t *__restrict__ pos, int32_t q0,
+                                                            int32_t nrows, int hq, int hkv, int d,
+                                                            const float *__restrict__ cos_sin, int32_t max_pos) {
+  const int per_head = d / 16;
+  const int item = blockIdx.y * blockDim.x + threadIdx.x;
+  if (item >= (hq + hkv) * per_head) return;
+  const int head = item / per_head;
+  const int c = item - head * per_head;
+  const bool is_q = head < hq;
+  __half *base = is_q ? q + (size_t)head * d + 8 * c : k + (size_t)(head - hq) * d + 8 * c;
+  const size_t row_stride = (size_t)(is_q ? hq : hkv) * d;
+  const int r0 = blockIdx.x * kRopeRows;
+  uint4 lo[kRopeRows], hi[kRopeRows];
+  int p[kRopeRows];
+  __half *x[kRopeRows];
+#pragma unroll
+  for (int u = 0; u < kRopeRows; ++u) {
+    const int r = r0 + u;
+    p[u] = -1;
+    if (r < nrows) {
+      p[u] = __ldg(pos + q0 + r);
+      x[u] = base + (size_t)(is_q ? r : q0 + r) * row_stride;
+      lo[u] = *reinterpret_cast<const uint4 *>(x[u]);
+      hi[u] = *reinterpret_cast<const uint4 *>(x[u] + d / 2);
     }
-    const int head = (int)(rem / per_head);
-    const int c = (int)(rem - (int64_t)head * per_head);
-    const int p = pos[q0 + r];
-    if (p < 0 || p >= max_pos) continue;  // the host checked the table against the plan
-    __half *x = base + (size_t)head * d + 8 * c;
-    uint4 lo = *reinterpret_cast<const uint4 *>(x);
-    uint4 hi = *reinterpret_cast<const uint4 *>(x + d / 2);
-    const float4 *cs = reinterpret_cast<const float4 *>(cos_sin + ((size_t)p * (d / 2) + 8 * c) * 2);
-    rotate8(lo, hi, cs);
-    *reinterpret_cast<uint4 *>(x) = lo;
-    *reinterpret_cast<uint4 *>(x + d / 2) = hi;
+  }
+#pragma unroll
+  for (int u = 0; u < kRopeRows; ++u) {
+    // a position outside the table cannot come from a plan the host checked
+    if (p[u] < 0 || p[u] >= max_pos) continue;
+    const float4 *cs = reinterpret_cast<const float4 *>(cos_sin + ((size_t)p[u] * (d / 2) + 8 * c) * 2);
+    rotate8(lo[u], hi[u], cs);
+    *reinterpret_cast<uint4 *>(x[u]) = lo[u];
+    *reinterpret_cast<uint4 *>(x[u] + d / 2) = hi[u];
   }
 }
 
@@ -111,12 +121,11 @@ extern "C" TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev,
   if (!aligned16(q) || !aligned16(k) || !aligned16(cos_sin) || !aligned16(plan_dev))
     return fail(TREE_ERR_UNSUPPORTED, "tree_rope: pointers must be 16-byte aligned");
   const int32_t q0 = P.chunk_q0[chunk], n = P.chunk_q1[chunk] - q0;
-  const int64_t total = (int64_t)n * (hq + hkv) * (d / 16);
-  const int threads = 256;
-  const int64_t need = (total + threads - 1) / threads;
-  const int blocks = (int)std::min<int64_t>(need, (int64_t)sm_count() * 8);
+  const int items = (hq + hkv) * (d / 16);
+  const int threads = std::min(kRopeMaxThreads, (items + 31) / 32 * 32);
+  const dim3 grid((unsigned)((n + kRopeRows - 1) / kRopeRows), (unsigned)((items + threads - 1) / threads));
   const int32_t *pos = reinterpret_cast<const int32_t *>(plan_dev) + P.off_pos;
-  rope_kernel<<<blocks, threads, 0, as_stream(stream)>>>(reinterpret_cast<__half *>(q), reinterpret_cast<__half *>(k),
-                                                         pos, q0, n, hq, hkv, d, cos_sin, max_pos);
+  rope_kernel<<<grid, threads, 0, as_stream(stream)>>>(reinterpret_cast<__half *>(q), reinterpret_cast<__half *>(k),
+                                                            pos, q0, n, hq, hkv, d, cos_sin, max_pos);
   return launch_status("tree_rope");
 }

@@ -53,11 +53,11 @@ class Run:
         self.lib.tree_rope(self.plan, self.dev, chunk, q, k, hq, hkv, d, tab, i.max_pos,
                            torch.cuda.current_stream())
 
-    def attn(self, q, k, v, hq, hkv, d, chunk, lse=None, status=None):
+    def attn(self, q, k, v, hq, hkv, d, chunk, lse=None, status=None, work=None):
         ci = self.plan.chunk(chunk)
         o = torch.empty((ci.q1 - ci.q0, hq, d), dtype=torch.float16, device="cuda")
         self.lib.tree_attn_fwd(self.plan, self.dev, chunk, q, k, v, o, lse, hq, hkv, d,
-                               status=status, stream=torch.cuda.current_stream())
+                               status=status, stream=torch.cuda.current_stream(), work=work)
         return o
 
 
@@ -176,8 +176,10 @@ def test_rope_workloads(lib, n):
 
 # ---------------------------------------------------------------- attention
 
-def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per_chunk=48, lse=True):
+def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per_chunk=48, lse=True,
+                dynamic=True):
     r = Run(lib, forest, max_fwd)
+    work = torch.zeros(2, dtype=torch.int32, device="cuda") if dynamic else None
     p = r.oplan
     q, k, v = synth.draw_qkv(p.n_fwd, p.n_tot, hq, hkv, d, seed)
     qr, kr = orope.apply_plan(p, q, k, 500000.0)     # oracle RoPE output is the attention input
@@ -188,8 +190,10 @@ def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per
         ci = r.plan.chunk(c)
         qd = _dev(qr[ci.q0 - p.n_res: ci.q1 - p.n_res])
         ld = torch.full((ci.q1 - ci.q0, hq), np.nan, device="cuda") if lse else None
-        o = r.attn(qd, kd, vd, hq, hkv, d, c, lse=ld, status=st)
+        o = r.attn(qd, kd, vd, hq, hkv, d, c, lse=ld, status=st, work=work)
         torch.cuda.synchronize()
+        if work is not None:
+            assert work.cpu().tolist() == [0, 0]      # the last CTA hands the counter back zeroed
         outs.append(o.float().cpu().numpy())
         if lse:
             lses.append(ld.cpu().numpy())
@@ -239,7 +243,32 @@ def test_attention_random_forests(lib, seed):
     except oplan.PlanError:
         pytest.skip("forest has no forward tokens")
     hq, hkv, d = [(4, 4, 64), (8, 2, 128), (4, 1, 64), (6, 3, 128)][seed % 4]
-    _attn_check(lib, f, hq, hkv, d, seed, max_fwd=int(rng.choice([128, 256, 8192])))
+    _attn_check(lib, f, hq, hkv, d, seed, max_fwd=int(rng.choice([128, 256, 8192])), dynamic=bool(seed % 2))
+
+
+@pytest.mark.parametrize("n", [2, 5])
+def test_attention_round_robin_schedule(lib, n):
+    """Without a work counter every CTA takes a fixed share of the items."""
+    w = synth.workload(n)
+    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=True, dynamic=False)
+
+
+def test_attention_work_counter_reused_across_calls(lib):
+    w = synth.workload(2)
+    r = Run(lib, w.forest)
+    p = r.oplan
+    q, k, v = synth.draw_qkv(p.n_fwd, p.n_tot, w.hq, w.hkv, w.d, w.seed)
+    qr, kr = orope.apply_plan(p, q, k, w.theta)
+    qd, kd, vd = _dev(qr), _dev(kr), _dev(v)
+    work = torch.zeros(2, dtype=torch.int32, device="cuda")
+    outs = [r.attn(qd, kd, vd, w.hq, w.hkv, w.d, 0, work=work) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert work.cpu().tolist() == [0, 0]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    stat = r.attn(qd, kd, vd, w.hq, w.hkv, w.d, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(stat, outs[0])     # same arithmetic whatever the schedule
 
 
 def test_attention_chunked_equals_unchunked(lib):
