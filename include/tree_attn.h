@@ -255,6 +255,29 @@ TREE_API int tree_attn_fwd(const tree_plan_t *plan, const void *plan_dev, int32_
                   const void *k, const void *v, void *o, float *lse, const tree_attn_params_t *params,
                   int32_t *status, tree_stream_t stream);
 
+/*
+ * tree_attn_fwd_noalloc -- the same attention for callers that cannot
+ * allocate device memory: a host program linking only this library with no
+ * allocator of its own, or code whose device memory belongs to another
+ * runtime's pool, where a private cudaMalloc would bypass that runtime's
+ * accounting and synchronise the device.  The pages that define the method
+ * have no counterpart to this entry point: it only changes where scratch lives.
+ *
+ * Arguments and results are those of tree_attn_fwd except that params->work
+ * must be NULL: the persistent CTAs' work counters live in a device array
+ * inside the library, one pair per chunk index, at most 256 chunks per plan
+ * (TREE_ERR_UNSUPPORTED beyond that).  The array (2 KB) stays resident on
+ * every device that has loaded the library until the process exits.  Each
+ * call clears its chunk's counter on `stream` before the launch.  Calls for
+ * the same chunk index that may run at the same time on the GPU (different
+ * streams, several plans) share that counter and race: serialise them.
+ * The first call on each device looks up the array's device address; make that
+ * first call before any stream capture begins.  Nothing is allocated.
+ */
+TREE_API int tree_attn_fwd_noalloc(const tree_plan_t *plan, const void *plan_dev, int32_t chunk, const void *q,
+                                   const void *k, const void *v, void *o, float *lse,
+                                   const tree_attn_params_t *params, int32_t *status, tree_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Letter readout and calibration                                            */
 /* ------------------------------------------------------------------------ */

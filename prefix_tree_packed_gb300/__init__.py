@@ -33,7 +33,7 @@ TREE_ERR_TIMEOUT = 7
 EXPORTS = (
     "tree_last_error", "tree_version", "tree_pack_plan", "tree_plan_free", "tree_plan_query",
     "tree_plan_chunk", "tree_plan_tables", "tree_plan_upload", "tree_rope_table", "tree_rope",
-    "tree_attn_fwd", "readout_decide",
+    "tree_attn_fwd", "tree_attn_fwd_noalloc", "readout_decide",
 )
 
 
@@ -103,9 +103,12 @@ _lib.tree_rope.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, 
                            C.c_int32, _vp]
 _lib.tree_attn_fwd.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp, C.POINTER(AttnParams),
                                _vp, _vp]
+_lib.tree_attn_fwd_noalloc.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp, C.POINTER(AttnParams),
+                                       _vp, _vp]
 _lib.readout_decide.argtypes = [_vp, C.c_int32, _vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp]
 for _f in ("tree_pack_plan", "tree_plan_free", "tree_plan_query", "tree_plan_chunk", "tree_plan_tables",
-           "tree_plan_upload", "tree_rope_table", "tree_rope", "tree_attn_fwd", "readout_decide"):
+           "tree_plan_upload", "tree_rope_table", "tree_rope", "tree_attn_fwd", "tree_attn_fwd_noalloc",
+           "readout_decide"):
     getattr(_lib, _f).restype = C.c_int
 
 
@@ -230,6 +233,14 @@ def tree_attn_fwd(plan: Plan, plan_dev, chunk: int, q, k, v, o, lse, hq: int, hk
     p = AttnParams(hq, hkv, d, scale, _ptr(work))
     _check(_lib.tree_attn_fwd(plan.handle, _ptr(plan_dev), chunk, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                               _ptr(lse), C.byref(p), _ptr(status), _stream(stream)))
+
+
+def tree_attn_fwd_noalloc(plan: Plan, plan_dev, chunk: int, q, k, v, o, lse, hq: int, hkv: int, d: int,
+                          scale: float = 0.0, status=None, stream=None):
+    """tree_attn_fwd with the work counters kept inside the library (nothing allocated)."""
+    p = AttnParams(hq, hkv, d, scale, None)
+    _check(_lib.tree_attn_fwd_noalloc(plan.handle, _ptr(plan_dev), chunk, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                      _ptr(lse), C.byref(p), _ptr(status), _stream(stream)))
 
 
 def readout_decide(logits, stride: int, r1, r2, n_letters, temperature, n_q: int, p_cal, p_avg=None,

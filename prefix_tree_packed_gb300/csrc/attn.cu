@@ -41,6 +41,7 @@
 // awaited (bounded), tensor memory is freed, and the kernel returns.
 
 #include <cmath>
+#include <mutex>
 
 #include <cudaTypedefs.h>
 
@@ -664,4 +665,68 @@ extern "C" TREE_API int tree_attn_fwd(const tree_plan_t *plan, const void *plan_
                 : launch_tc<64, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s);
   return pair ? launch_tc<128, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s)
               : launch_tc<128, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s);
+}
+
+// ---------------------------------------------------------------------------
+// tree_attn_fwd_noalloc: the same attention for callers that cannot allocate
+// device memory themselves.  The persistent CTAs' work counter (two int32 per
+// chunk) then lives in this file's own device array instead of in caller
+// memory.  The array holds kNoAllocChunks counter pairs and stays resident on
+// every device that loads the library until the process exits.
+
+namespace tree {
+namespace {
+
+constexpr int kNoAllocChunks = 256;
+static __device__ __align__(256) int32_t g_noalloc_work[2 * kNoAllocChunks];
+
+constexpr int kMaxDevices = 64;
+int32_t *g_noalloc_ptr[kMaxDevices] = {nullptr};
+std::mutex g_noalloc_mutex;
+
+// Device address of the array on the current device, looked up once per device.
+int noalloc_counters(int32_t **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(TREE_ERR_UNSUPPORTED, "tree_attn_fwd_noalloc: device %d beyond %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    int32_t *ptr = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr), g_noalloc_work);
+    if (e != cudaSuccess || !ptr)
+      return fail(TREE_ERR_CUDA, "tree_attn_fwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TREE_OK;
+}
+
+}  // namespace
+}  // namespace tree
+
+extern "C" TREE_API int tree_attn_fwd_noalloc(const tree_plan_t *plan, const void *plan_dev, int32_t chunk,
+                                              const void *q, const void *k, const void *v, void *o, float *lse,
+                                              const tree_attn_params_t *params, int32_t *status,
+                                              tree_stream_t stream) {
+  using namespace tree;
+  if (!plan || !params) return fail(TREE_ERR_INVALID_ARG, "tree_attn_fwd_noalloc: NULL argument");
+  if (params->work)
+    return fail(TREE_ERR_INVALID_ARG, "tree_attn_fwd_noalloc: params->work must be NULL (the counters are built in)");
+  if (plan->p.n_chunks > kNoAllocChunks)
+    return fail(TREE_ERR_UNSUPPORTED, "tree_attn_fwd_noalloc: plan has %d chunks; the built-in counters cover %d",
+                plan->p.n_chunks, kNoAllocChunks);
+  if (chunk < 0 || chunk >= plan->p.n_chunks)
+    return fail(TREE_ERR_INVALID_ARG, "tree_attn_fwd_noalloc: chunk %d out of range [0, %d)", chunk, plan->p.n_chunks);
+  int32_t *counters = nullptr;
+  int rc = noalloc_counters(&counters);
+  if (rc != TREE_OK) return rc;
+  int32_t *work = counters + 2 * chunk;
+  // start from zero whatever an earlier call left behind
+  const cudaError_t e = cudaMemsetAsync(work, 0, 2 * sizeof(int32_t), as_stream(stream));
+  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd_noalloc: %s", cudaGetErrorString(e));
+  tree_attn_params_t p = *params;
+  p.work = work;
+  return tree_attn_fwd(plan, plan_dev, chunk, q, k, v, o, lse, &p, status, stream);
 }
