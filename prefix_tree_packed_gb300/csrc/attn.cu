@@ -81,7 +81,8 @@ struct Cfg {
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t K_OFF = Q_OFF + QBUF * Q_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + STAGES * CB * BOX_BYTES;
-  static constexpr uint32_t SEND_OFF = V_OFF + STAGES * CB * BOX_BYTES;
+  static constexpr uint32_t O_OFF = V_OFF + STAGES * CB * BOX_BYTES;  // per head: one 128 x 64 staging box
+  static constexpr uint32_t SEND_OFF = O_OFF + NH * BOX_BYTES;
   static constexpr uint32_t SMEM = SEND_OFF + STAGES * 512 + 1024;  // + alignment slack
   static constexpr int WARPS = 4 * NH + 4;        // softmax warpgroups + producer/MMA warpgroup
   static constexpr int THREADS = 32 * WARPS;
@@ -105,6 +106,7 @@ struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[3], v_full[3], kv_empty[3];
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
+  uint64_t ostage_full[2], ostage_free[2];  // output staging box of each head
   uint32_t tmem;
   int32_t abort;
 };
@@ -114,7 +116,7 @@ struct Bars {
 // as another thread of the CTA has given up.
 TREE_DEV bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *status,
                        bool honor_abort = true, uint64_t limit_ns = kWaitNs) {
-  if (mbar_try(bar, parity)) return true;
+  if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try(bar, parity)) return true;
@@ -129,7 +131,8 @@ TREE_DEV bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort, i
   }
 }
 
-// Warp-uniform form: the next steps of the caller are warp-collective.
+// Warp-uniform form: the caller's next steps are warp-collective.  Every lane
+// polls (measured faster than one polling lane plus a broadcast).
 TREE_DEV bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *status) {
   const bool ok = wait_bar(bar, parity, abort, status);
   return __all_sync(0xffffffffu, ok);
@@ -168,7 +171,7 @@ TREE_DEV Item item_at(const AttnArgs &a, int w) {
 template <int D, int NH>
 __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     tree_attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                 const __grid_constant__ CUtensorMap mv, const AttnArgs a) {
+                 const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo, const AttnArgs a) {
   using C = Cfg<D, NH>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
@@ -190,6 +193,8 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   auto b_p = [&](int h) { return smem_u32(&bars.p_full[h]); };
   auto b_o = [&](int h) { return smem_u32(&bars.o_done[h]); };
   auto b_of = [&](int h) { return smem_u32(&bars.o_free[h]); };
+  auto b_osq = [&](int h) { return smem_u32(&bars.ostage_full[h]); };
+  auto b_osf = [&](int h) { return smem_u32(&bars.ostage_free[h]); };
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < kRing; ++r) {
@@ -211,6 +216,8 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       mbar_init(b_p(h), 128);
       mbar_init(b_o(h), 1);
       mbar_init(b_of(h), 128);
+      mbar_init(b_osq(h), 128);
+      mbar_init(b_osf(h), 1);
     }
     bars.abort = 0;
     mbar_fence_init();
@@ -292,29 +299,34 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       // ---------------------------------------------------------- MMA issuer (whole warp, one lane issues)
       constexpr uint32_t idesc_qk = idesc_f16(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, D, true);
+      // Descriptors are built once per operand tile and advanced by constant
+      // offsets (the start-address field holds address / 16 in its low bits).
+      const uint64_t q_desc0 = sdesc_sw128(s_base + C::Q_OFF, 16, 1024);
+      const uint64_t k_desc0 = sdesc_sw128(s_base + C::K_OFF, 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(s_base + C::V_OFF, BOX_BYTES, 1024);
       auto issue_qk = [&](int h, int qb, int st) {
+        const uint64_t da0 = q_desc0 + ((qb * C::Q_BYTES + h * C::CB * BOX_BYTES) >> 4);
+        const uint64_t db0 = k_desc0 + ((st * C::CB * BOX_BYTES) >> 4);
+        const uint32_t d_tmem = tmem + 128 * h;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-            const uint64_t da =
-                sdesc_sw128(s_base + C::Q_OFF + qb * C::Q_BYTES + h * C::CB * BOX_BYTES + off, 16, 1024);
-            const uint64_t db = sdesc_sw128(s_base + C::K_OFF + st * C::CB * BOX_BYTES + off, 16, 1024);
-            mma_ss(tmem + 128 * h, da, db, idesc_qk, kk > 0);
+            const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+            mma_ss(d_tmem, da0 + off, db0 + off, idesc_qk, kk > 0);
           }
           mma_commit(b_s(h));
         }
         __syncwarp();
       };
       auto issue_pv = [&](int h, int st, bool accumulate) {
-        const uint32_t p_col = C::PSEP ? C::P_COL + 64 * h : 128 * h;
+        const uint32_t a_tmem = tmem + (C::PSEP ? C::P_COL + 64 * h : 128 * h);
+        const uint32_t d_tmem = tmem + C::O_COL + D * h;
+        const uint64_t db0 = v_desc0 + ((st * C::CB * BOX_BYTES) >> 4);
+        const uint32_t acc0 = accumulate ? 1u : 0u;
         if (elect_one()) {
+          mma_ts(d_tmem, a_tmem, db0, idesc_pv, acc0);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t db =
-                sdesc_sw128(s_base + C::V_OFF + st * C::CB * BOX_BYTES + kk * 2048, BOX_BYTES, 1024);
-            mma_ts(tmem + C::O_COL + D * h, tmem + p_col + 8 * kk, db, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 1; kk < BN / 16; ++kk) mma_ts(d_tmem, a_tmem + 8 * kk, db0 + kk * (2048 >> 4), idesc_pv, 1u);
           mma_commit(b_o(h));
         }
         __syncwarp();
@@ -435,7 +447,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     const uint32_t tP = C::PSEP ? t_lane + C::P_COL + 64 * h : tS;
     const uint32_t tO = t_lane + C::O_COL + D * h;
     bool ok = true;
-    int T = 0;
+    int T = 0, stage_uses = 0;
     for (int taken = 0; ok; ++taken) {
       const int slot = taken % kRing;
       if (!(ok = wait_bar_warp(b_if(slot), (taken / kRing) & 1, abort, a.status))) break;
@@ -449,6 +461,8 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       for (int i = 0; i < it.n; ++i, ++T) {
         const int st = T % C::STAGES;
         const int e = __ldg(a.ent + it.qt.ent0 + i);
+        // a partial tile also needs the subtree ends of its keys (same stage as K)
+        if ((e & 1) && !(ok = wait_bar_warp(b_k(st), (T / C::STAGES) & 1, abort, a.status))) break;
         if (!(ok = wait_bar_warp(b_s(h), T & 1, abort, a.status))) break;
         fence_after();
         uint32_t s[128];
@@ -463,7 +477,6 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         }
         if (e & 1) {
           // partial tile: key j = j0 + c is visible iff j <= iq < send[j]
-          if (!(ok = wait_bar_warp(b_k(st), (T / C::STAGES) & 1, abort, a.status))) break;
           const int cmax = iq - (e >> 1) * BN;  // keys c <= cmax are not after the query
           const int4 *sd = reinterpret_cast<const int4 *>(sSend + st * 128);
 #pragma unroll
@@ -537,21 +550,46 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       tmem_wait_ld();
       fence_before();
       mbar_arrive(b_of(h));
-      if (iq < it.qt.row1) {
-        const float inv = 1.f / l;
-        uint4 *d4 = reinterpret_cast<uint4 *>(a.o + ((size_t)(iq - a.q0) * a.hq + (it.h0 + h)) * D);
+      // O / l as f16 into this head's 128-byte-swizzled staging box, 64 columns at
+      // a time; lane 0 of the warpgroup issues one TMA store per box once every
+      // row is written, and hands the box back when the store has read it.  Rows
+      // past the chunk are clipped by the store.
+      const float inv = 1.f / l;
+      const uint32_t stage = s_base + C::O_OFF + h * BOX_BYTES;
 #pragma unroll
-        for (int u = 0; u < D / 8; ++u)
-          d4[u] = make_uint4(pack_f16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv),
-                             pack_f16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv),
-                             pack_f16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv),
-                             pack_f16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv));
-        if (a.lse) {
-          const float mu = (m == -INFINITY) ? 0.f : m;
-          a.lse[(size_t)(iq - a.q0) * a.hq + it.h0 + h] = (mu + __log2f(l)) * 0.69314718055994531f;
+      for (int c = 0; c < D / 64; ++c) {
+        const int use = stage_uses++;
+        if (use > 0 && !(ok = wait_bar_warp(b_osf(h), (use - 1) & 1, abort, a.status))) break;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t *x = o + 64 * c + 8 * u;
+          const uint4 v4 = make_uint4(pack_f16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                                      pack_f16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                                      pack_f16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                                      pack_f16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+          const uint32_t addr = stage + r * 128 + ((u ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v4.x), "r"(v4.y), "r"(v4.z),
+                       "r"(v4.w)
+                       : "memory");
+        }
+        fence_async_shared();
+        mbar_arrive(b_osq(h));
+        if (r == 0) {
+          if (wait_bar(b_osq(h), use & 1, abort, a.status)) {
+            tma_store_2d(&mo, (it.h0 + h) * D + 64 * c, it.qt.row0 - a.q0, stage);
+            bulk_commit();
+            bulk_wait_read0();
+          }
+          mbar_arrive(b_osf(h));  // also after a failed wait, so that no thread waits for it
         }
       }
+      if (!ok) break;
+      if (a.lse && iq < it.qt.row1) {
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        a.lse[(size_t)(iq - a.q0) * a.hq + it.h0 + h] = (mu + __log2f(l)) * 0.69314718055994531f;
+      }
     }
+    if (r == 0) bulk_wait0();  // every output store has completed
   }
   fence_before();
   __syncthreads();
@@ -608,10 +646,10 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
     attr_set = true;
   }
   const int32_t q0 = P.chunk_q0[chunk], nq = P.chunk_q1[chunk] - q0;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   int rc;
   if ((rc = make_map(&mq, q, (int64_t)hq * D, nq)) || (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot)) ||
-      (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot)))
+      (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot)) || (rc = make_map(&mo, o, (int64_t)hq * D, nq)))
     return rc;
   AttnArgs a;
   a.send = img + P.off_send;
@@ -633,7 +671,7 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
   a.work = work;
   if (a.n_items == 0) return TREE_OK;
   const dim3 grid((unsigned)std::min(a.n_items, sm_count()));
-  kern<<<grid, C::THREADS, C::SMEM, s>>>(mq, mk, mv, a);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(mq, mk, mv, mo, a);
   return launch_status("tree_attn_fwd");
 }
 
