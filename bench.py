@@ -14,6 +14,11 @@ figure with host<->device copies inside the timed region, SM clocks sampled
 during the timed region, and the CPU oracle timed on the host as a baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl reference]
+  python bench.py --only attn|rope|readout [--workload N] [--steps K] [--warmup W] [--sets S]
+
+--only times one kernel by itself (CUDA events, rotating input sets) and prints
+one JSON line for it; it is also the small, fixed command that profiler captures
+are taken on.
 """
 from __future__ import annotations
 
@@ -40,7 +45,7 @@ N_SETS = 4  # rotating input sets: 4 x ~81 MB > 129 MB L2
 
 # DRAM bytes per attention launch from one ncu capture, valid only for the
 # kernel source it was taken on (sha256 of csrc/attn.cu, first 16 hex digits).
-ATTN_TRAFFIC = {(2, "9bb954c98db7dab8"): 52661504, (2, "5c301e22c09d83cd"): 54190336}
+ATTN_TRAFFIC = {(2, "5c301e22c09d83cd"): 53714688}
 
 
 def _peaks():
@@ -109,7 +114,7 @@ class ClockSampler:
 class Batch:
     """One workload resident on the device (N_SETS rotating copies of Q/K/V/O)."""
 
-    def __init__(self, lib, torch, w: synth.Workload, dev):
+    def __init__(self, lib, torch, w: synth.Workload, dev, n_sets=N_SETS):
         self.lib, self.torch, self.w, self.dev = lib, torch, w, dev
         kw = dict(leaf1=w.leaf1, leaf2=w.leaf2) if w.leaf1 is not None else {}
         self.kw = kw
@@ -120,7 +125,7 @@ class Batch:
         q, k, v = synth.draw_qkv(i.n_fwd, i.n_tot, w.hq, w.hkv, w.d, w.seed)
         self.host = dict(q=q, k=k, v=v)
         self.sets = []
-        for s in range(N_SETS):
+        for s in range(n_sets):
             self.sets.append(dict(q=torch.from_numpy(q).to(dev), k=torch.from_numpy(k).to(dev),
                                   v=torch.from_numpy(v).to(dev),
                                   o=torch.empty((i.n_fwd, w.hq, w.d), dtype=torch.float16, device=dev)))
@@ -177,16 +182,18 @@ class Batch:
         return 2 * len(self.chunks) + (1 if self.nq else 0)
 
 
-def measure_rope(lib, torch, B, stream, reps=40):
+def measure_rope(lib, torch, B, stream, reps=40, warmup=None):
     """tree_rope alone over the rotating input sets: algorithmic GB/s."""
     w, i = B.w, B.info
+    n_sets = len(B.sets)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    for s in range(N_SETS):
+    for s in range(n_sets if warmup is None else warmup):
         for c in range(len(B.chunks)):
-            lib.tree_rope(B.plan, B.pdev, c, B.views[s][c][0], B.sets[s]["k"], w.hq, w.hkv, w.d, B.tab, i.max_pos, stream)
+            lib.tree_rope(B.plan, B.pdev, c, B.views[s % n_sets][c][0], B.sets[s % n_sets]["k"], w.hq, w.hkv, w.d,
+                          B.tab, i.max_pos, stream)
     ev[0].record(stream)
     for r in range(reps):
-        s = r % N_SETS
+        s = r % n_sets
         for c in range(len(B.chunks)):
             lib.tree_rope(B.plan, B.pdev, c, B.views[s][c][0], B.sets[s]["k"], w.hq, w.hkv, w.d, B.tab, i.max_pos, stream)
     ev[1].record(stream)
@@ -197,12 +204,12 @@ def measure_rope(lib, torch, B, stream, reps=40):
     return ms, nbytes
 
 
-def measure_readout(lib, torch, dev, stream, reps=64):
+def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None):
     """readout_decide on 65,536 questions, 16 rotating buffer sets (> L2): algorithmic GB/s."""
     b = synth.draw_readout_batch()
     nq, stride = len(b["r1"]), b["stride"]
     sets = []
-    for _ in range(16):
+    for _ in range(n_sets):
         sets.append(dict(logits=torch.from_numpy(b["logits"]).to(dev), r1=torch.from_numpy(b["r1"]).to(dev),
                          r2=torch.from_numpy(b["r2"]).to(dev), n=torch.from_numpy(b["n_letters"]).to(dev),
                          T=torch.from_numpy(b["temperature"]).to(dev),
@@ -211,12 +218,12 @@ def measure_readout(lib, torch, dev, stream, reps=64):
     def run(x):
         lib.readout_decide(x["logits"], stride, x["r1"], x["r2"], x["n"], x["T"], nq, x["pc"], None, x["ch"], None,
                            stream)
-    for x in sets:
-        run(x)
+    for r in range(n_sets if warmup is None else warmup):
+        run(sets[r % n_sets])
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     ev[0].record(stream)
     for r in range(reps):
-        run(sets[r % 16])
+        run(sets[r % n_sets])
     ev[1].record(stream)
     torch.cuda.synchronize()
     ms = ev[0].elapsed_time(ev[1]) / reps
@@ -224,6 +231,67 @@ def measure_readout(lib, torch, dev, stream, reps=64):
     # logits of both orders, r1/r2/n/T, the zero-padded p_cal row, the choice
     nbytes = int((2 * n * 4).sum() + 16 * nq + 4 * stride * nq + 4 * nq)
     return ms, nbytes
+
+
+def measure_attn(lib, torch, B, stream, reps, warmup):
+    """tree_attn_fwd alone over the rotating input sets, one work counter per chunk.
+
+    Returns the mean time of one whole forward (all chunks) in ms.
+    """
+    w = B.w
+    n_sets = len(B.sets)
+    work = torch.zeros(2 * len(B.chunks), dtype=torch.int32, device=B.dev)
+
+    def fwd(s):
+        for c in range(len(B.chunks)):
+            qv, ov = B.views[s][c]
+            lib.tree_attn_fwd(B.plan, B.pdev, c, qv, B.sets[s]["k"], B.sets[s]["v"], ov, None, w.hq, w.hkv, w.d,
+                              status=B.status, stream=stream, work=work[2 * c: 2 * c + 2])
+    for r in range(warmup):
+        fwd(r % n_sets)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record(stream)
+    for r in range(reps):
+        fwd(r % n_sets)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    assert int(B.status.item()) == 0, "device status word set"
+    return ev[0].elapsed_time(ev[1]) / reps
+
+
+def run_only(args):
+    """One kernel by itself on cuda:0: a JSON line with its time and roofline."""
+    import torch
+    import prefix_tree_packed_gb300 as lib
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peaks = _peaks()
+    line = {"kernel": args.only, "steps": args.steps, "warmup": args.warmup}
+    if args.only == "readout":
+        ms, nbytes = measure_readout(lib, torch, dev, stream, reps=args.steps, n_sets=args.sets or 16,
+                                     warmup=args.warmup)
+        gbs = nbytes / ms / 1e6
+        line.update(workload="65,536 questions, 2-10 letters", us=round(ms * 1e3, 2), bytes=nbytes,
+                    achieved=round(gbs, 1), unit="GB/s", peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4))
+    else:
+        w = synth.workload(args.workload)
+        B = Batch(lib, torch, w, dev, n_sets=args.sets or N_SETS)
+        B.plan.upload(B.pdev, B.info.dev_bytes, stream)
+        line.update(workload=w.name, sets=len(B.sets))
+        if args.only == "rope":
+            ms, nbytes = measure_rope(lib, torch, B, stream, reps=args.steps, warmup=args.warmup)
+            gbs = nbytes / ms / 1e6
+            line.update(us=round(ms * 1e3, 2), bytes=nbytes, achieved=round(gbs, 1), unit="GB/s",
+                        peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4))
+        else:
+            ms = measure_attn(lib, torch, B, stream, reps=args.steps, warmup=args.warmup)
+            tf = 4.0 * w.d * w.hq * B.info.pairs / (ms / 1e3) / 1e12
+            line.update(us_per_forward=round(ms * 1e3, 2), chunks=len(B.chunks), visible_pairs=B.info.pairs,
+                        achieved=round(tf, 2), unit="TFLOP/s", peak=peaks["tc"], frac=round(tf / peaks["tc"], 4))
+    line["peak_source"] = peaks["src"]
+    print(json.dumps(line), flush=True)
 
 
 def run_gpu(args):
@@ -469,10 +537,14 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--only", choices=["attn", "rope", "readout"], default=None)
+    ap.add_argument("--sets", type=int, default=0, help="rotating input sets for --only (0: default)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.only and args.impl == "native":
+        run_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
