@@ -121,7 +121,15 @@ class Batch:
         self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, **kw)
         i = self.plan.info
         self.info = i
-        self.pdev = torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev)
+        # the plan image double-buffered on the device, uploaded from page-locked
+        # staging on a copy stream while the previous step computes
+        self.pdevs = [torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.stage = [torch.empty(i.dev_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        self.ev_up = [torch.cuda.Event() for _ in range(2)]    # upload into pdevs[k] executed
+        self.ev_done = [torch.cuda.Event() for _ in range(2)]  # last launch reading pdevs[k] executed
+        self.k = 0
+        self.pdev = self.pdevs[0]
         q, k, v = synth.draw_qkv(i.n_fwd, i.n_tot, w.hq, w.hkv, w.d, w.seed)
         self.host = dict(q=q, k=k, v=v)
         self.sets = []
@@ -157,7 +165,14 @@ class Batch:
         torch = self.torch
         if replan:
             self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, **self.kw)
-        self.plan.upload(self.pdev, i.dev_bytes, stream)
+        k = self.k
+        self.k ^= 1
+        self.ev_up[k].synchronize()                     # staging k: its copy two steps ago has run
+        self.copy_stream.wait_event(self.ev_done[k])    # pdevs[k]: step s-2 no longer reads it
+        self.plan.upload_staged(self.pdevs[k], i.dev_bytes, self.stage[k], i.dev_bytes, self.copy_stream)
+        self.ev_up[k].record(self.copy_stream)
+        stream.wait_event(self.ev_up[k])
+        self.pdev = self.pdevs[k]
         b = bufs if bufs is not None else self.sets[s]
         for c, ci in enumerate(self.chunks):
             if bufs is None:
@@ -177,6 +192,7 @@ class Batch:
             base = self.pdev.data_ptr()
             lib.readout_decide(self.logits, w.letter_stride, base + i.off_r1, base + i.off_r2, self.nl, self.T,
                                self.nq, self.p_cal, None, self.choice, self.status, stream)
+        self.ev_done[k].record(stream)
 
     def launches_per_step(self):
         return 2 * len(self.chunks) + (1 if self.nq else 0)
@@ -204,9 +220,9 @@ def measure_rope(lib, torch, B, stream, reps=40, warmup=None):
     return ms, nbytes
 
 
-def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None):
-    """readout_decide on 65,536 questions, 16 rotating buffer sets (> L2): algorithmic GB/s."""
-    b = synth.draw_readout_batch()
+def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None, n_questions=65536):
+    """readout_decide on n_questions (2-10 letters each) over rotating buffer sets: algorithmic GB/s."""
+    b = synth.draw_readout_batch(n_questions)
     nq, stride = len(b["r1"]), b["stride"]
     sets = []
     for _ in range(n_sets):
@@ -271,9 +287,9 @@ def run_only(args):
     line = {"kernel": args.only, "steps": args.steps, "warmup": args.warmup}
     if args.only == "readout":
         ms, nbytes = measure_readout(lib, torch, dev, stream, reps=args.steps, n_sets=args.sets or 16,
-                                     warmup=args.warmup)
+                                     warmup=args.warmup, n_questions=args.questions)
         gbs = nbytes / ms / 1e6
-        line.update(workload="65,536 questions, 2-10 letters", us=round(ms * 1e3, 2), bytes=nbytes,
+        line.update(workload=f"{args.questions:,} questions, 2-10 letters", us=round(ms * 1e3, 2), bytes=nbytes,
                     achieved=round(gbs, 1), unit="GB/s", peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4))
     else:
         w = synth.workload(args.workload)
@@ -399,7 +415,7 @@ def run_gpu(args):
                    "rows": 8 if args.workload == 2 else None, "q_heads": w.hq, "kv_heads": w.hkv,
                    "head_dim": w.d, "visible_pairs_per_head": i.pairs, "chunks": len(B.chunks),
                    "questions": B.nq, "l2": f"{N_SETS} rotating input sets (> L2)",
-                   "step": "plan + upload + rope + attention + readout", "parallelism": f"dp{world} (rows)"},
+                   "step": "plan + upload (pinned staging, copy stream, overlaps the previous step) + rope + attention + readout", "parallelism": f"dp{world} (rows)"},
         "tflops_attention": round(achieved, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tc"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["tc"], 4), "traffic": traffic,
@@ -539,6 +555,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--only", choices=["attn", "rope", "readout"], default=None)
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets for --only (0: default)")
+    ap.add_argument("--questions", type=int, default=65536, help="questions for --only readout")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

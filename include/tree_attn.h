@@ -192,6 +192,28 @@ TREE_API int tree_plan_tables(const tree_plan_t *plan, tree_plan_host_view_t *vi
  */
 TREE_API int tree_plan_upload(const tree_plan_t *plan, void *dev_buf, size_t bytes, tree_stream_t stream);
 
+/*
+ * tree_plan_upload through caller-owned page-locked host memory, for callers
+ * that plan the next batch while the GPU still runs the current one.  A copy
+ * from pageable memory goes through the driver's staging buffers and can hold
+ * the calling thread until the GPU has drained earlier work; this call copies
+ * the image into `host_staging` (page-locked, e.g. cudaHostAlloc,
+ * `staging_bytes` >= dev_bytes) on the calling thread and then enqueues an
+ * asynchronous host-to-device copy from it on `stream`, so it never waits for
+ * the GPU.  Upload into a device buffer that no queued kernel still reads
+ * (e.g. two buffers used in turn) on a copy stream, and make the compute
+ * stream wait for that copy (an event) before its launches.
+ *
+ * Ownership: `host_staging` stays the caller's; it must not be rewritten or
+ * freed until the copy has executed on `stream` (record an event after this
+ * call and wait on it first).  The plan may be freed once this returns.
+ * Errors: TREE_ERR_INVALID_ARG (NULL pointer, buffer too small),
+ * TREE_ERR_UNSUPPORTED (dev_buf not 16-byte aligned), TREE_ERR_CUDA.
+ * This is plumbing around the planner; the pages define no such call.
+ */
+TREE_API int tree_plan_upload_staged(const tree_plan_t *plan, void *dev_buf, size_t bytes, void *host_staging,
+                                     size_t staging_bytes, tree_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Rotary embedding at tree positions                                        */
 /* ------------------------------------------------------------------------ */

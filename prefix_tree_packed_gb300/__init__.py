@@ -32,7 +32,8 @@ TREE_ERR_TIMEOUT = 7
 # every symbol the header declares
 EXPORTS = (
     "tree_last_error", "tree_version", "tree_pack_plan", "tree_plan_free", "tree_plan_query",
-    "tree_plan_chunk", "tree_plan_tables", "tree_plan_upload", "tree_rope_table", "tree_rope",
+    "tree_plan_chunk", "tree_plan_tables", "tree_plan_upload", "tree_plan_upload_staged", "tree_rope_table",
+    "tree_rope",
     "tree_attn_fwd", "tree_attn_fwd_noalloc", "readout_decide",
 )
 
@@ -98,6 +99,7 @@ _lib.tree_plan_query.argtypes = [_vp, C.POINTER(PlanInfo)]
 _lib.tree_plan_chunk.argtypes = [_vp, C.c_int32, C.POINTER(ChunkInfo)]
 _lib.tree_plan_tables.argtypes = [_vp, C.POINTER(_View)]
 _lib.tree_plan_upload.argtypes = [_vp, _vp, C.c_size_t, _vp]
+_lib.tree_plan_upload_staged.argtypes = [_vp, _vp, C.c_size_t, _vp, C.c_size_t, _vp]
 _lib.tree_rope_table.argtypes = [_vp, C.c_int32, C.c_int32, C.c_double]
 _lib.tree_rope.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, _vp,
                            C.c_int32, _vp]
@@ -107,7 +109,7 @@ _lib.tree_attn_fwd_noalloc.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, 
                                        _vp, _vp]
 _lib.readout_decide.argtypes = [_vp, C.c_int32, _vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp]
 for _f in ("tree_pack_plan", "tree_plan_free", "tree_plan_query", "tree_plan_chunk", "tree_plan_tables",
-           "tree_plan_upload", "tree_rope_table", "tree_rope", "tree_attn_fwd", "tree_attn_fwd_noalloc",
+           "tree_plan_upload", "tree_plan_upload_staged", "tree_rope_table", "tree_rope", "tree_attn_fwd", "tree_attn_fwd_noalloc",
            "readout_decide"):
     getattr(_lib, _f).restype = C.c_int
 
@@ -214,6 +216,11 @@ class Plan:
 
     def upload(self, dev_buf, nbytes: int, stream=None):
         _check(_lib.tree_plan_upload(self.handle, _ptr(dev_buf), nbytes, _stream(stream)))
+
+    def upload_staged(self, dev_buf, nbytes: int, host_staging, staging_bytes: int, stream=None):
+        """Upload through caller-owned page-locked host memory (never waits for the GPU)."""
+        _check(_lib.tree_plan_upload_staged(self.handle, _ptr(dev_buf), nbytes, _ptr(host_staging),
+                                            staging_bytes, _stream(stream)))
 
 
 def rope_table(max_pos: int, d: int, theta: float) -> np.ndarray:

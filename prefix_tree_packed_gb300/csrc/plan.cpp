@@ -530,4 +530,21 @@ int tree_plan_upload(const tree_plan_t *plan, void *dev_buf, size_t bytes, tree_
   return TREE_OK;
 }
 
+int tree_plan_upload_staged(const tree_plan_t *plan, void *dev_buf, size_t bytes, void *host_staging,
+                            size_t staging_bytes, tree_stream_t stream) {
+  if (!plan || !dev_buf || !host_staging)
+    return tree::fail(TREE_ERR_INVALID_ARG, "tree_plan_upload_staged: NULL argument");
+  const size_t need = plan->p.image.size() * sizeof(int32_t);
+  if (bytes < need || staging_bytes < need)
+    return tree::fail(TREE_ERR_INVALID_ARG, "tree_plan_upload_staged: buffers of %zu / %zu bytes < %zu", bytes,
+                      staging_bytes, need);
+  if (reinterpret_cast<uintptr_t>(dev_buf) % 16)
+    return tree::fail(TREE_ERR_UNSUPPORTED, "tree_plan_upload_staged: device buffer not 16-byte aligned");
+  std::memcpy(host_staging, plan->p.image.data(), need);
+  const cudaError_t e = cudaMemcpyAsync(dev_buf, host_staging, need, cudaMemcpyHostToDevice,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return tree::fail(TREE_ERR_CUDA, "tree_plan_upload_staged: %s", cudaGetErrorString(e));
+  return TREE_OK;
+}
+
 }  // extern "C"

@@ -10,11 +10,16 @@
 // the argmax of p_cal (lowest index on ties); clamp, log, division by T > 0 and
 // softmax are monotone and p sums to 1, so it is taken as the argmax of p.
 //
-// Work layout: a group of G lanes per question, each lane holding letters
-// lane, lane + G, ...  G = 32 (one warp per question, up to 255 letters) in
-// general; G = 1 (one lane per question, no shuffles) when every question has
-// at most 16 letters, i.e. stride <= 16, which makes the kernel bound by HBM
-// rather than by shuffle latency on batches of small questions.
+// Two work layouts.
+//  * stride <= 32 (the usual 2-10 letters): a warp takes 32 consecutive
+//    questions as one tile.  It gathers their logits rows flat (pass j, lane l
+//    reads element l + 32 j of the 32 x stride tile), so one load instruction
+//    touches a few neighbouring rows rather than 32 scattered ones; the rows go
+//    to shared memory at an odd pitch, each lane decides one question from
+//    there without bank conflicts, and the warp writes the tile's p_cal (and
+//    p_avg) rows back as one contiguous, coalesced span.
+//  * stride > 32 (up to 255 letters): one warp per question, lane l holding
+//    letters l, l + 32, ..., reductions by shuffles.
 
 #include <cfloat>
 
@@ -152,6 +157,162 @@ __global__ void __launch_bounds__(256) readout_kernel(const float *__restrict__ 
   if (lane == 0 && choice) choice[q] = arg;
 }
 
+// Decision for one question held in lane registers: x1 = order-1 logits, x2 =
+// order-2 logits already put into original option order, n letters (1..K).
+// Leaves p_avg in x1 and p_cal in x2; returns the argmax of p.
+template <int K>
+__device__ __forceinline__ int decide_lane(float (&x1)[K], float (&x2)[K], int n, float T) {
+  float m1 = -FLT_MAX, m2 = -FLT_MAX;
+#pragma unroll
+  for (int k = 0; k < K; ++k)
+    if (k < n) {
+      m1 = fmaxf(m1, x1[k]);
+      m2 = fmaxf(m2, x2[k]);
+    }
+  float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+  for (int k = 0; k < K; ++k)
+    if (k < n) {
+      x1[k] = expf(x1[k] - m1);
+      x2[k] = expf(x2[k] - m2);
+      s1 += x1[k];
+      s2 += x2[k];
+    }
+  const float inv1 = 1.f / s1, inv2 = 1.f / s2, invT = 1.f / T;
+  float m3 = -FLT_MAX, best = -1.f;
+  int arg = 0;
+#pragma unroll
+  for (int k = 0; k < K; ++k)
+    if (k < n) {
+      const float p = 0.5f * (x1[k] * inv1 + x2[k] * inv2);
+      x1[k] = p;
+      x2[k] = logf(fmaxf(p, kClamp)) * invT;
+      m3 = fmaxf(m3, x2[k]);
+      if (p > best) {  // increasing index: the first maximum wins
+        best = p;
+        arg = k;
+      }
+    }
+  float s3 = 0.f;
+#pragma unroll
+  for (int k = 0; k < K; ++k)
+    if (k < n) {
+      x2[k] = expf(x2[k] - m3);
+      s3 += x2[k];
+    }
+  const float inv3 = 1.f / s3;
+#pragma unroll
+  for (int k = 0; k < K; ++k)
+    if (k < n) x2[k] *= inv3;
+  return arg;
+}
+
+constexpr int kTileWarps = 4;  // warps (32-question tiles) per block
+
+// Tile layout, stride <= K <= 32.  Shared memory per warp: two 32-row tiles
+// (order 1, order 2) at pitch `pitch` = stride rounded up to odd.  `magic` =
+// ceil(2^16 / stride): for e < 32 * 32 and stride <= 32, (e * magic) >> 16 is
+// exactly e / stride (the rounding error e / 2^16 < 1/64 stays below the gap
+// 1/stride between e / stride and the next integer).
+template <int K>
+__global__ void __launch_bounds__(kTileWarps * 32) readout_tile_kernel(
+    const float *__restrict__ logits, int stride, int pitch, uint32_t magic, const int32_t *__restrict__ r1,
+    const int32_t *__restrict__ r2, const int32_t *__restrict__ nl, const float *__restrict__ temp, int nq,
+    float *__restrict__ p_cal, float *__restrict__ p_avg, int32_t *__restrict__ choice,
+    int32_t *__restrict__ status) {
+  extern __shared__ float tile_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t q0 = ((int64_t)blockIdx.x * kTileWarps + warp) * 32;
+  if (q0 >= nq) return;  // whole warps leave together
+  const int nv = (int)min((int64_t)32, (int64_t)nq - q0);
+  float *sa = tile_smem + (size_t)warp * 64 * pitch;
+  float *sb = sa + 32 * pitch;
+
+  int my_r1 = 0, my_r2 = 0, my_n = 0;
+  float T = 1.f;
+  if (lane < nv) {
+    my_r1 = r1[q0 + lane];
+    my_r2 = r2[q0 + lane];
+    my_n = nl[q0 + lane];
+    T = temp[q0 + lane];
+  }
+  const bool bad = lane < nv && (my_n < 1 || my_n > stride || my_n > 255 || !(T > 0.f));
+  const int n_load = (lane < nv && !bad) ? my_n : 0;
+
+  // gather: all loads in flight before the shared-memory stores
+  float va[K], vb[K];
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    const int e = lane + 32 * j;
+    const int qq = (int)(((uint32_t)e * magic) >> 16);
+    const int i = e - qq * stride;
+    // qq < 32 whenever j < stride; shuffles run on every lane with in-range sources
+    const int src = qq & 31;
+    const int ra = __shfl_sync(0xffffffffu, my_r1, src);
+    const int rb = __shfl_sync(0xffffffffu, my_r2, src);
+    const int nn = __shfl_sync(0xffffffffu, n_load, src);
+    va[j] = 0.f;
+    vb[j] = 0.f;
+    if (j < stride && i < nn) {
+      va[j] = logits[(size_t)ra * stride + i];
+      vb[j] = logits[(size_t)rb * stride + i];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    const int e = lane + 32 * j;
+    if (j < stride) {
+      const int qq = (int)(((uint32_t)e * magic) >> 16);
+      const int i = e - qq * stride;
+      sa[qq * pitch + i] = va[j];
+      sb[qq * pitch + i] = vb[j];
+    }
+  }
+  __syncwarp();
+
+  // decide: lane = question; each lane touches only its own two rows
+  if (lane < nv) {
+    float *ra_s = sa + lane * pitch, *rb_s = sb + lane * pitch;
+    if (bad) {
+      for (int i = 0; i < stride; ++i) ra_s[i] = rb_s[i] = 0.f;
+      if (choice) choice[q0 + lane] = -1;
+      if (status) atomicExch(status, TREE_ERR_INVALID_ARG);
+    } else {
+      float x1[K], x2[K];
+#pragma unroll
+      for (int k = 0; k < K; ++k)
+        if (k < my_n) {
+          x1[k] = ra_s[k];
+          x2[k] = rb_s[my_n - 1 - k];  // order-2 letter of original option k
+        }
+      const int arg = decide_lane<K>(x1, x2, my_n, T);
+#pragma unroll
+      for (int k = 0; k < K; ++k)
+        if (k < stride) {
+          ra_s[k] = k < my_n ? x2[k] : 0.f;
+          rb_s[k] = k < my_n ? x1[k] : 0.f;
+        }
+      if (choice) choice[q0 + lane] = arg;
+    }
+  }
+  __syncwarp();
+
+  // write back: the tile's rows are one contiguous span of nv * stride floats
+  float *pc = p_cal + q0 * stride;
+  float *pa = p_avg ? p_avg + q0 * stride : nullptr;
+  const int span = nv * stride;
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    const int e = lane + 32 * j;
+    if (j < stride && e < span) {
+      const int qq = (int)(((uint32_t)e * magic) >> 16);
+      const int i = e - qq * stride;
+      pc[e] = sa[qq * pitch + i];
+      if (pa) pa[e] = sb[qq * pitch + i];
+    }
+  }
+}
+
 }  // namespace
 }  // namespace tree
 
@@ -166,11 +327,18 @@ extern "C" TREE_API int readout_decide(const float *logits, int32_t stride, cons
   if (!logits || !r1 || !r2 || !n_letters || !temperature || !p_cal)
     return fail(TREE_ERR_INVALID_ARG, "readout_decide: NULL argument");
   const cudaStream_t s = as_stream(stream);
-  if (stride <= 16) {
-    const int threads = 256;
-    const int blocks = (int)(((int64_t)n_q + threads - 1) / threads);
-    readout_kernel<1, 16><<<blocks, threads, 0, s>>>(logits, stride, r1, r2, n_letters, temperature, n_q,
-                                                     p_cal, p_avg, choice, status);
+  if (stride <= 32) {
+    const int pitch = stride | 1;
+    const uint32_t magic = (65536u + (uint32_t)stride - 1u) / (uint32_t)stride;
+    const int64_t warps = ((int64_t)n_q + 31) / 32;
+    const int blocks = (int)((warps + kTileWarps - 1) / kTileWarps);
+    const size_t smem = (size_t)kTileWarps * 64 * pitch * sizeof(float);
+    if (stride <= 16)
+      readout_tile_kernel<16><<<blocks, kTileWarps * 32, smem, s>>>(
+          logits, stride, pitch, magic, r1, r2, n_letters, temperature, n_q, p_cal, p_avg, choice, status);
+    else
+      readout_tile_kernel<32><<<blocks, kTileWarps * 32, smem, s>>>(
+          logits, stride, pitch, magic, r1, r2, n_letters, temperature, n_q, p_cal, p_avg, choice, status);
   } else {
     const int threads = 256;
     const int64_t lanes = (int64_t)n_q * 32;

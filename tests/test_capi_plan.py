@@ -121,6 +121,27 @@ def test_question_errors(lib):
         lib.Plan([-1, 0, 0], [4, 2, 2], leaf1=[1], leaf2=[7])
 
 
+def test_upload_argument_checks(lib):
+    # every check runs before any CUDA call, so no device is needed
+    plan = lib.Plan([-1, 0, 0], [130, 7, 9])
+    need = plan.info.dev_bytes
+    with pytest.raises(lib.TreeError) as e:
+        plan.upload_staged(16, need, 32, need - 4)          # staging too small
+    assert e.value.code == lib.TREE_ERR_INVALID_ARG
+    with pytest.raises(lib.TreeError) as e:
+        plan.upload_staged(16, need - 4, 32, need)          # device buffer too small
+    assert e.value.code == lib.TREE_ERR_INVALID_ARG
+    with pytest.raises(lib.TreeError) as e:
+        plan.upload_staged(16, need, 0, need)               # no staging buffer
+    assert e.value.code == lib.TREE_ERR_INVALID_ARG
+    with pytest.raises(lib.TreeError) as e:
+        plan.upload_staged(24, need, 32, need)              # misaligned device buffer
+    assert e.value.code == lib.TREE_ERR_UNSUPPORTED
+    with pytest.raises(lib.TreeError) as e:
+        plan.upload(24, need)
+    assert e.value.code == lib.TREE_ERR_UNSUPPORTED
+
+
 def test_rope_table_matches_double_precision(lib):
     tab = lib.rope_table(40000, 128, 500000.0)
     from oracle import rope

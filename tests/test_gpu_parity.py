@@ -61,6 +61,23 @@ class Run:
         return o
 
 
+def test_staged_upload_matches_plan_image(lib):
+    w = synth.workload(2)
+    plan = lib.Plan.from_forest(w.forest, leaf1=w.leaf1, leaf2=w.leaf2)
+    i = plan.info
+    want = plan.tables()["image"]
+    assert len(want) == i.dev_bytes
+    dev = [torch.full((i.dev_bytes,), 0xAB, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    pin = torch.empty(i.dev_bytes, dtype=torch.uint8).pin_memory()
+    cs = torch.cuda.Stream()
+    plan.upload_staged(dev[0], i.dev_bytes, pin, i.dev_bytes, cs)
+    cs.synchronize()
+    plan.upload(dev[1], i.dev_bytes, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert np.array_equal(dev[0].cpu().numpy(), want)
+    assert np.array_equal(dev[1].cpu().numpy(), want)
+
+
 def _f16_ulp(x):
     x = np.abs(x.astype(np.float32))
     e = np.floor(np.log2(np.maximum(x, 2.0 ** -14)))
@@ -110,7 +127,8 @@ def test_readout_65536_questions(lib):
     _check_readout(lib, b["logits"], b["r1"], b["r2"], b["n_letters"], b["temperature"], b["stride"])
 
 
-@pytest.mark.parametrize("stride,nmax", [(1, 1), (16, 16), (17, 17), (40, 33), (255, 255), (300, 255)])
+@pytest.mark.parametrize("stride,nmax", [(1, 1), (3, 2), (10, 10), (16, 16), (17, 17), (31, 20), (32, 32), (33, 33),
+                                         (40, 33), (255, 255), (300, 255)])
 def test_readout_sizes(lib, stride, nmax):
     rng = np.random.default_rng(stride)
     nq = 333
