@@ -87,7 +87,9 @@ struct Cfg {
   static constexpr int WARPS = 4 * NH + 4;        // softmax warpgroups + producer/MMA warpgroup
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int PROD_WARP = 4 * NH;
-  static constexpr int MMA_WARP = 4 * NH + 1;
+  static constexpr int MMA_WARP = 4 * NH + 1;    // MMA warps MMA_WARP .. MMA_WARP + MW - 1
+  static constexpr int MW = D == 64 ? NH : 1;     // MMA warps: one per head at d = 64, one at d = 128
+  static constexpr bool KV_ONE = STAGES >= 3;     // K and V of a stage complete one barrier
   static constexpr bool PSEP = D == 64;           // P in its own columns
   static constexpr uint32_t P_COL = 128 * NH;     // P_h at P_COL + 64h (PSEP only)
   static constexpr uint32_t O_COL = PSEP ? 128 * NH + 64 * NH : 128 * NH;
@@ -102,7 +104,7 @@ constexpr int kRing = 4;  // items handed from the producer to the MMA and softm
 
 struct Bars {
   uint64_t item_full[kRing], item_empty[kRing];
-  int32_t ring[kRing];
+  int32_t ring[kRing][8];  // claimed item: {w, row0, row1, ent0, ent1, h0, g, first entry}
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[3], v_full[3], kv_empty[3];
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
@@ -199,16 +201,16 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int r = 0; r < kRing; ++r) {
       mbar_init(b_if(r), 1);
-      mbar_init(b_ie(r), NH * 128 + 1);  // every softmax thread and the MMA warp
+      mbar_init(b_ie(r), NH * 128 + C::MW);  // every softmax thread and each MMA warp
     }
     for (int b = 0; b < C::QBUF; ++b) {
       mbar_init(b_qf(b), 1);
-      mbar_init(b_qe(b), 1);
+      mbar_init(b_qe(b), C::MW);
     }
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(b_k(s), 1);
       mbar_init(b_v(s), 1);
-      mbar_init(b_e(s), 1);
+      mbar_init(b_e(s), C::MW);  // one commit per MMA warp
     }
     for (int h = 0; h < NH; ++h) {
       mbar_init(b_s(h), 1);
@@ -227,7 +229,19 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = bars.tmem;
-  volatile int32_t *ring = bars.ring;
+  volatile int32_t(*ring)[8] = bars.ring;
+  // the item the producer decoded into ring slot `slot` (w >= n_items ends the list)
+  auto ring_item = [&](int slot, int &w, Item &it, int &e0) {
+    w = ring[slot][0];
+    it.qt.row0 = ring[slot][1];
+    it.qt.row1 = ring[slot][2];
+    it.qt.ent0 = ring[slot][3];
+    it.qt.ent1 = ring[slot][4];
+    it.h0 = ring[slot][5];
+    it.g = ring[slot][6];
+    e0 = ring[slot][7];
+    it.n = it.qt.ent1 - it.qt.ent0;
+  };
 
   if (warp >= 4 * NH) {
     if (NH == 2) regs_dec<C::SERVICE_REGS>();
@@ -247,15 +261,29 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         if (fetched >= kRing && !(ok = wait_bar_warp(b_ie(slot), ((fetched / kRing) - 1) & 1, abort, a.status)))
           break;
         int w = 0;
-        if (lane == 0) {
-          w = a.work ? atomicAdd(a.work, 1) : (int)blockIdx.x + fetched * (int)gridDim.x;
-          ring[slot] = w;
-          mbar_arrive(b_if(slot));
-        }
+        if (lane == 0) w = a.work ? atomicAdd(a.work, 1) : (int)blockIdx.x + fetched * (int)gridDim.x;
         w = __shfl_sync(0xffffffffu, w, 0);
         ++fetched;
+        // decoded here, so that the consumers read the item from shared memory
+        Item it{};
+        int e0 = 0;
+        if (w < a.n_items) {
+          it = item_at<NH>(a, w);
+          if (it.n > 0) e0 = __ldg(a.ent + it.qt.ent0);
+        }
+        if (lane == 0) {
+          ring[slot][0] = w;
+          ring[slot][1] = it.qt.row0;
+          ring[slot][2] = it.qt.row1;
+          ring[slot][3] = it.qt.ent0;
+          ring[slot][4] = it.qt.ent1;
+          ring[slot][5] = it.h0;
+          ring[slot][6] = it.g;
+          ring[slot][7] = e0;
+          mbar_arrive(b_if(slot));
+        }
+        __syncwarp();
         if (w >= a.n_items) break;
-        const Item it = item_at<NH>(a, w);
         if (it.n <= 0) continue;  // (a plan never makes one: every query tile sees its own rows)
         const int b = j % C::QBUF;
         if (j >= C::QBUF && !(ok = wait_bar_warp(b_qe(b), ((j / C::QBUF) - 1) & 1, abort, a.status))) break;
@@ -274,15 +302,19 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           if (t >= C::STAGES && !(ok = wait_bar_warp(b_e(st), ((t / C::STAGES) - 1) & 1, abort, a.status))) break;
           const int j0 = (__ldg(a.ent + it.qt.ent0 + i) >> 1) * BN;
           if (elect_one()) {
-            mbar_expect_tx(b_k(st), C::CB * BOX_BYTES + 512);
+            // with three stages K, the keys' subtree ends and V complete one
+            // barrier (the loads run far enough ahead that V is in place before
+            // the QK is issued); with two, V has its own
+            const uint32_t v_bar = C::KV_ONE ? b_k(st) : b_v(st);
+            mbar_expect_tx(b_k(st), (C::KV_ONE ? 2 : 1) * C::CB * BOX_BYTES + 512);
 #pragma unroll
             for (int c = 0; c < C::CB; ++c)
               tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES, &mk, it.g * D + 64 * c, j0, b_k(st));
             bulk_load(s_base + C::SEND_OFF + st * 512, a.send + j0, 512, b_k(st));
-            mbar_expect_tx(b_v(st), C::CB * BOX_BYTES);
+            if (!C::KV_ONE) mbar_expect_tx(v_bar, C::CB * BOX_BYTES);
 #pragma unroll
             for (int c = 0; c < C::CB; ++c)
-              tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, it.g * D + 64 * c, j0, b_v(st));
+              tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, it.g * D + 64 * c, j0, v_bar);
           }
           __syncwarp();
         }
@@ -291,12 +323,17 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       // wind down: every copy issued must have landed before the CTA exits
       for (int u = (t > C::STAGES ? t - C::STAGES : 0); u < t; ++u) {
         wait_bar(b_k(u % C::STAGES), (u / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
-        wait_bar(b_v(u % C::STAGES), (u / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
+        if (!C::KV_ONE) wait_bar(b_v(u % C::STAGES), (u / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
       }
       for (int u = (j > C::QBUF ? j - C::QBUF : 0); u < j; ++u)
         wait_bar(b_qf(u % C::QBUF), (u / C::QBUF) & 1, abort, nullptr, false, kDrainNs);
-    } else if (warp == C::MMA_WARP) {
-      // ---------------------------------------------------------- MMA issuer (whole warp, one lane issues)
+    } else if (warp >= C::MMA_WARP && warp < C::MMA_WARP + C::MW) {
+      // ---------------------------------------------------------- MMA issuer of q heads h0 + [hb, he)
+      // One lane issues.  At d = 64 each head has its own MMA warp, so that the
+      // heads' chains of waits run on their own and their MMAs interleave on
+      // the tensor core as operands become ready; at d = 128 (P over S) one
+      // warp orders both heads, PV_h then the next QK_h, head after head.
+      const int hb = (warp - C::MMA_WARP) * (NH / C::MW), he = hb + NH / C::MW;
       constexpr uint32_t idesc_qk = idesc_f16(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, D, true);
       // Descriptors are built once per operand tile and advanced by constant
@@ -307,26 +344,26 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       auto issue_qk = [&](int h, int qb, int st) {
         const uint64_t da0 = q_desc0 + ((qb * C::Q_BYTES + h * C::CB * BOX_BYTES) >> 4);
         const uint64_t db0 = k_desc0 + ((st * C::CB * BOX_BYTES) >> 4);
-        const uint32_t d_tmem = tmem + 128 * h;
+        const uint32_t s_tmem = tmem + 128 * h;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
-            mma_ss(d_tmem, da0 + off, db0 + off, idesc_qk, kk > 0);
+            mma_ss(s_tmem, da0 + off, db0 + off, idesc_qk, kk > 0);
           }
           mma_commit(b_s(h));
         }
         __syncwarp();
       };
       auto issue_pv = [&](int h, int st, bool accumulate) {
-        const uint32_t a_tmem = tmem + (C::PSEP ? C::P_COL + 64 * h : 128 * h);
-        const uint32_t d_tmem = tmem + C::O_COL + D * h;
+        const uint32_t p_tmem = tmem + (C::PSEP ? C::P_COL + 64 * h : 128 * h);
+        const uint32_t o_tmem = tmem + C::O_COL + D * h;
         const uint64_t db0 = v_desc0 + ((st * C::CB * BOX_BYTES) >> 4);
         const uint32_t acc0 = accumulate ? 1u : 0u;
         if (elect_one()) {
-          mma_ts(d_tmem, a_tmem, db0, idesc_pv, acc0);
+          mma_ts(o_tmem, p_tmem, db0, idesc_pv, acc0);
 #pragma unroll
-          for (int kk = 1; kk < BN / 16; ++kk) mma_ts(d_tmem, a_tmem + 8 * kk, db0 + kk * (2048 >> 4), idesc_pv, 1u);
+          for (int kk = 1; kk < BN / 16; ++kk) mma_ts(o_tmem, p_tmem + 8 * kk, db0 + kk * (2048 >> 4), idesc_pv, 1u);
           mma_commit(b_o(h));
         }
         __syncwarp();
@@ -341,13 +378,13 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         for (;;) {
           const int slot = taken % kRing;
           if (!wait_bar_warp(b_if(slot), (taken / kRing) & 1, abort, a.status)) return -1;
-          const int w = ring[slot];
+          int w, e0;
+          ring_item(slot, w, out, e0);
           __syncwarp();
           if (elect_one()) mbar_arrive(b_ie(slot));
           __syncwarp();
           ++taken;
           if (w >= a.n_items) return 0;
-          out = item_at<NH>(a, w);
           if (out.n > 0) return 1;
         }
       };
@@ -360,7 +397,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         ok = wait_bar_warp(b_qf(0), 0, abort, a.status) && wait_bar_warp(b_k(0), 0, abort, a.status);
         if (ok) {
           fence_after();
-          for (int h = 0; h < NH; ++h) issue_qk(h, 0, 0);
+          for (int h = hb; h < he; ++h) issue_qk(h, 0, 0);
           last_qk = 0;
           if (cur.n == 1) commit(b_qe(0));
         }
@@ -387,20 +424,20 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           return wait_bar_warp(b_k(stn), ((T + 1) / C::STAGES) & 1, abort, a.status);
         };
         if (C::PSEP && has_next) {
-          if (!(ok = wait_next_operands())) break;
           // next S first: S_h is free once the softmax has read it into registers
-          for (int h = 0; h < NH && ok; ++h) {
+          if (!(ok = wait_next_operands())) break;
+          for (int h = hb; h < he && ok; ++h) {
             if (!(ok = wait_bar_warp(b_f(h), T & 1, abort, a.status))) break;
             fence_after();
             issue_qk(h, qbn, stn);
             last_qk = T + 1;
           }
           if (!ok) break;
-          if (in == nxt.n - 1) commit(b_qe(qbn));
+          if (in == nxt.n - 1) commit(b_qe(qbn));  // the Q buffer is free once these QKs have read it
         }
         const int st = T % C::STAGES;
-        if (!(ok = wait_bar_warp(b_v(st), (T / C::STAGES) & 1, abort, a.status))) break;
-        for (int h = 0; h < NH && ok; ++h) {
+        if (!C::KV_ONE && !(ok = wait_bar_warp(b_v(st), (T / C::STAGES) & 1, abort, a.status))) break;
+        for (int h = hb; h < he && ok; ++h) {
           if (!(ok = wait_bar_warp(b_p(h), T & 1, abort, a.status))) break;
           // a new item's first PV overwrites O_h: its previous values must have been read
           if (ic == 0 && jc > 0 && !(ok = wait_bar_warp(b_of(h), (jc - 1) & 1, abort, a.status))) break;
@@ -408,7 +445,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           issue_pv(h, st, ic > 0);
           if (!C::PSEP && has_next) {
             // P_h shares S_h's columns: the next S_h waits until this PV has read P_h
-            if (h == 0 && !(ok = wait_next_operands())) break;
+            if (h == hb && !(ok = wait_next_operands())) break;
             if (!(ok = wait_bar_warp(b_o(h), T & 1, abort, a.status))) break;
             fence_after();
             issue_qk(h, qbn, stn);
@@ -424,18 +461,15 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         ic = in;
         cur = nxt;
       }
-      // wind down: every issued MMA (and the commits after it) has completed
-      // before tensor memory is freed
+      // wind down: every MMA this warp issued (and the commits after it) has
+      // completed, and every stage's release has landed, before the CTA exits
       if (T > 0) {
-#pragma unroll
-        for (int h = 0; h < NH; ++h) wait_bar(b_o(h), (T - 1) & 1, abort, nullptr, false, kDrainNs);
+        for (int h = hb; h < he; ++h) wait_bar(b_o(h), (T - 1) & 1, abort, nullptr, false, kDrainNs);
         for (int u = (T > C::STAGES ? T - C::STAGES : 0); u < T; ++u)
           wait_bar(b_e(u % C::STAGES), (u / C::STAGES) & 1, abort, nullptr, false, kDrainNs);
       }
-      if (!ok && last_qk >= 0) {
-#pragma unroll
-        for (int h = 0; h < NH; ++h) wait_bar(b_s(h), last_qk & 1, abort, nullptr, false, kDrainNs);
-      }
+      if (!ok && last_qk >= 0)
+        for (int h = hb; h < he; ++h) wait_bar(b_s(h), last_qk & 1, abort, nullptr, false, kDrainNs);
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -451,16 +485,18 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     for (int taken = 0; ok; ++taken) {
       const int slot = taken % kRing;
       if (!(ok = wait_bar_warp(b_if(slot), (taken / kRing) & 1, abort, a.status))) break;
-      const int w = ring[slot];
+      int w, e_next;
+      Item it;
+      ring_item(slot, w, it, e_next);
       mbar_arrive(b_ie(slot));
       if (w >= a.n_items) break;
-      const Item it = item_at<NH>(a, w);
       if (it.n <= 0) continue;
       const int iq = it.qt.row0 + r;
       float m = -INFINITY, l = 0.f;
       for (int i = 0; i < it.n; ++i, ++T) {
         const int st = T % C::STAGES;
-        const int e = __ldg(a.ent + it.qt.ent0 + i);
+        const int e = e_next;  // the next tile's entry loads while this one is processed
+        if (i + 1 < it.n) e_next = __ldg(a.ent + it.qt.ent0 + i + 1);
         // a partial tile also needs the subtree ends of its keys (same stage as K)
         if ((e & 1) && !(ok = wait_bar_warp(b_k(st), (T / C::STAGES) & 1, abort, a.status))) break;
         if (!(ok = wait_bar_warp(b_s(h), T & 1, abort, a.status))) break;
@@ -490,13 +526,16 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
             }
           }
         }
-        float mx8[8];
+        // row maximum: three-input max over four independent chains
+        float mx4[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+        for (int u = 0; u < 4; ++u) mx4[u] = __uint_as_float(s[u]);
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int c = 4; c < 128; c += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mx4[u] = max3(mx4[u], __uint_as_float(s[c + 2 * u]), __uint_as_float(s[c + 2 * u + 1]));
+        const float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
         const float mt = mx * a.scale_log2;  // -inf stays -inf (scale > 0)
         const bool grow = mt > m + 8.f;      // also true for the first finite maximum
         float alpha = 1.f;
@@ -505,17 +544,21 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           m = mt;
         }
         const float mu = (m == -INFINITY) ? 0.f : m;
-        float sum8[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) sum8[u] = 0.f;
+        // p = 2^(s * scale_log2 - mu) on pairs of lanes (paired fma and add)
+        const uint64_t scale2 = f32x2(a.scale_log2, a.scale_log2), nmu2 = f32x2(-mu, -mu);
+        uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[c]), a.scale_log2, -mu));
-          const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), a.scale_log2, -mu));
-          sum8[(c >> 1) & 7] += p0 + p1;
+          float x0, x1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), scale2, nmu2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum2[(c >> 1) & 3] = add_f32x2(sum2[(c >> 1) & 3], f32x2(p0, p1));
           s[c >> 1] = pack_f16x2(p0, p1);
         }
-        l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+        float sl[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) f32x2_split(sum2[u], sl[2 * u], sl[2 * u + 1]);
+        l = l * alpha + (((sl[0] + sl[1]) + (sl[2] + sl[3])) + ((sl[4] + sl[5]) + (sl[6] + sl[7])));
         // PV_h of the previous tile of this item must be done before P_h is
         // rewritten (separate P) or O_h is rescaled; for an item's first tile the
         // previous item's epilogue has already waited for it
@@ -551,15 +594,23 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       fence_before();
       mbar_arrive(b_of(h));
       // O / l as f16 into this head's 128-byte-swizzled staging box, 64 columns at
-      // a time; lane 0 of the warpgroup issues one TMA store per box once every
-      // row is written, and hands the box back when the store has read it.  Rows
-      // past the chunk are clipped by the store.
+      // a time; row 0's thread issues one TMA store per box once every row is
+      // written.  It waits for a store to have read the box only when the box
+      // is next needed (normally an item later, long done), and then hands it
+      // back, so no warp stalls on the store here.  Rows past the chunk are
+      // clipped by the store.
       const float inv = 1.f / l;
       const uint32_t stage = s_base + C::O_OFF + h * BOX_BYTES;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         const int use = stage_uses++;
-        if (use > 0 && !(ok = wait_bar_warp(b_osf(h), (use - 1) & 1, abort, a.status))) break;
+        if (use > 0) {
+          if (r == 0) {
+            bulk_wait_read0();
+            mbar_arrive(b_osf(h));
+          }
+          if (!(ok = wait_bar_warp(b_osf(h), (use - 1) & 1, abort, a.status))) break;
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const uint32_t *x = o + 64 * c + 8 * u;
@@ -574,13 +625,9 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         }
         fence_async_shared();
         mbar_arrive(b_osq(h));
-        if (r == 0) {
-          if (wait_bar(b_osq(h), use & 1, abort, a.status)) {
-            tma_store_2d(&mo, (it.h0 + h) * D + 64 * c, it.qt.row0 - a.q0, stage);
-            bulk_commit();
-            bulk_wait_read0();
-          }
-          mbar_arrive(b_osf(h));  // also after a failed wait, so that no thread waits for it
+        if (r == 0 && wait_bar(b_osq(h), use & 1, abort, a.status)) {
+          tma_store_2d(&mo, (it.h0 + h) * D + 64 * c, it.qt.row0 - a.q0, stage);
+          bulk_commit();
         }
       }
       if (!ok) break;
