@@ -198,25 +198,27 @@ class Batch:
         return 2 * len(self.chunks) + (1 if self.nq else 0)
 
 
-def measure_rope(lib, torch, B, stream, reps=40, warmup=None):
-    """tree_rope alone over the rotating input sets: algorithmic GB/s."""
+def measure_rope(lib, torch, B, stream, reps=40, warmup=None, keys_only=False):
+    """tree_rope alone over the rotating input sets (Q and K, or K only): algorithmic GB/s."""
     w, i = B.w, B.info
     n_sets = len(B.sets)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    for s in range(n_sets if warmup is None else warmup):
+
+    def run(s):
         for c in range(len(B.chunks)):
-            lib.tree_rope(B.plan, B.pdev, c, B.views[s % n_sets][c][0], B.sets[s % n_sets]["k"], w.hq, w.hkv, w.d,
-                          B.tab, i.max_pos, stream)
+            lib.tree_rope(B.plan, B.pdev, c, None if keys_only else B.views[s][c][0], B.sets[s]["k"], w.hq, w.hkv,
+                          w.d, B.tab, i.max_pos, stream)
+    for s in range(n_sets if warmup is None else warmup):
+        run(s % n_sets)
     ev[0].record(stream)
     for r in range(reps):
-        s = r % n_sets
-        for c in range(len(B.chunks)):
-            lib.tree_rope(B.plan, B.pdev, c, B.views[s][c][0], B.sets[s]["k"], w.hq, w.hkv, w.d, B.tab, i.max_pos, stream)
+        run(r % n_sets)
     ev[1].record(stream)
     torch.cuda.synchronize()
     ms = ev[0].elapsed_time(ev[1]) / reps
-    # read + write of every forward row of Q and K, plus its position
-    nbytes = 2 * i.n_fwd * (w.hq + w.hkv) * w.d * 2 + 4 * i.n_fwd
+    # read + write of every forward row rotated, plus its position
+    heads = w.hkv if keys_only else w.hq + w.hkv
+    nbytes = 2 * i.n_fwd * heads * w.d * 2 + 4 * i.n_fwd
     return ms, nbytes
 
 
@@ -297,7 +299,9 @@ def run_only(args):
         B.plan.upload(B.pdev, B.info.dev_bytes, stream)
         line.update(workload=w.name, sets=len(B.sets))
         if args.only == "rope":
-            ms, nbytes = measure_rope(lib, torch, B, stream, reps=args.steps, warmup=args.warmup)
+            ms, nbytes = measure_rope(lib, torch, B, stream, reps=args.steps, warmup=args.warmup,
+                                      keys_only=args.keys_only)
+            line["keys_only"] = args.keys_only
             gbs = nbytes / ms / 1e6
             line.update(us=round(ms * 1e3, 2), bytes=nbytes, achieved=round(gbs, 1), unit="GB/s",
                         peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4))
@@ -556,6 +560,7 @@ def main():
     ap.add_argument("--only", choices=["attn", "rope", "readout"], default=None)
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets for --only (0: default)")
     ap.add_argument("--questions", type=int, default=65536, help="questions for --only readout")
+    ap.add_argument("--keys-only", action="store_true", help="--only rope: rotate the keys alone")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -234,9 +234,11 @@ TREE_API int tree_rope_table(float *host_out, int32_t max_pos, int32_t d, double
  *   cos_sin  f32 [max_pos][d/2][2] device table from tree_rope_table,
  *            max_pos >= info.max_pos
  *
- * Arithmetic in f32, stored f16 (round to nearest even).  plan_dev is the
- * device image from tree_plan_upload.  d even and <= 256; q and k 16-byte
- * aligned; hq*d and hkv*d multiples of 8.
+ * Arithmetic in f32 (y_i = fma(x_i, cos, -(x_{i+d/2} sin)), y_{i+d/2} =
+ * fma(x_{i+d/2}, cos, x_i sin)), stored f16 (round to nearest even).  plan_dev
+ * is the device image from tree_plan_upload.  d a multiple of 16 and <= 256;
+ * q and k 16-byte aligned.  q may be NULL (hq is then ignored): only the keys
+ * are rotated, for a caller that has rotated its queries elsewhere.
  */
 TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev, int32_t chunk, void *q, void *k,
               int32_t hq, int32_t hkv, int32_t d, const float *cos_sin, int32_t max_pos,

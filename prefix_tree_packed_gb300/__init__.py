@@ -231,6 +231,7 @@ def rope_table(max_pos: int, d: int, theta: float) -> np.ndarray:
 
 def tree_rope(plan: Plan, plan_dev, chunk: int, q, k, hq: int, hkv: int, d: int, cos_sin,
               max_pos: int, stream=None):
+    """Rotate the chunk's queries and keys in place (q=None: keys only)."""
     _check(_lib.tree_rope(plan.handle, _ptr(plan_dev), chunk, _ptr(q), _ptr(k), hq, hkv, d,
                           _ptr(cos_sin), max_pos, _stream(stream)))
 

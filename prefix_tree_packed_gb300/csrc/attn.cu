@@ -90,6 +90,11 @@ struct Cfg {
   static constexpr int MMA_WARP = 4 * NH + 1;    // MMA warps MMA_WARP .. MMA_WARP + MW - 1
   static constexpr int MW = D == 64 ? NH : 1;     // MMA warps: one per head at d = 64, one at d = 128
   static constexpr bool KV_ONE = STAGES >= 3;     // K and V of a stage complete one barrier
+  // At d = 64 the two heads' softmax warps that share an SM sub-partition take
+  // turns at the arithmetic of a tile (head 0, head 1, head 0, ...): the
+  // arithmetic is issue-bound, so while one head computes, the other waits on
+  // tensor memory and barriers instead of competing for the same issue slots.
+  static constexpr bool ALT = NH == 2 && D == 64;
   static constexpr bool PSEP = D == 64;           // P in its own columns
   static constexpr uint32_t P_COL = 128 * NH;     // P_h at P_COL + 64h (PSEP only)
   static constexpr uint32_t O_COL = PSEP ? 128 * NH + 64 * NH : 128 * NH;
@@ -109,6 +114,7 @@ struct Bars {
   uint64_t k_full[3], v_full[3], kv_empty[3];
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
   uint64_t ostage_full[2], ostage_free[2];  // output staging box of each head
+  uint64_t turn[2][4];  // per lane quarter: head h's warp has finished the arithmetic of its tile
   uint32_t tmem;
   int32_t abort;
 };
@@ -121,6 +127,8 @@ TREE_DEV bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort, i
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
+    // try_wait's default suspend window: measured faster than longer sleeps
+    // (a long hint delays the wake-up after the phase completes)
     if (mbar_try(bar, parity)) return true;
     if ((n & 255) == 0) {
       if (honor_abort && *abort) return false;
@@ -220,6 +228,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       mbar_init(b_of(h), 128);
       mbar_init(b_osq(h), 128);
       mbar_init(b_osf(h), 1);
+      for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bars.turn[h][q]), 1);
     }
     bars.abort = 0;
     mbar_fence_init();
@@ -511,6 +520,12 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           fence_before();
           mbar_arrive(b_f(h));  // S_h may be overwritten by the next QK
         }
+        const uint32_t my_turn = smem_u32(&bars.turn[h][warp & 3]), other_turn = smem_u32(&bars.turn[h ^ 1][warp & 3]);
+        if (C::ALT) {
+          // head 1 computes tile T after head 0 has; head 0 computes tile T after head 1 has computed T - 1
+          if (h == 1 && !(ok = wait_bar_warp(other_turn, T & 1, abort, a.status))) break;
+          if (h == 0 && T > 0 && !(ok = wait_bar_warp(other_turn, (T - 1) & 1, abort, a.status))) break;
+        }
         if (e & 1) {
           // partial tile: key j = j0 + c is visible iff j <= iq < send[j]
           const int cmax = iq - (e >> 1) * BN;  // keys c <= cmax are not after the query
@@ -559,6 +574,10 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) f32x2_split(sum2[u], sl[2 * u], sl[2 * u + 1]);
         l = l * alpha + (((sl[0] + sl[1]) + (sl[2] + sl[3])) + ((sl[4] + sl[5]) + (sl[6] + sl[7])));
+        if (C::ALT) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(my_turn);
+        }
         // PV_h of the previous tile of this item must be done before P_h is
         // rewritten (separate P) or O_h is rescaled; for an item's first tile the
         // previous item's epilogue has already waited for it

@@ -26,24 +26,6 @@
 namespace tree {
 namespace {
 
-__device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float4 *cs) {
-  // lo holds x_i .. x_{i+7}, hi holds x_{i+d/2} .. x_{i+d/2+7}; cs: 8 x {cos, sin}
-  __half2 *l = reinterpret_cast<__half2 *>(&lo);
-  __half2 *h = reinterpret_cast<__half2 *>(&hi);
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const float4 c = __ldg(cs + p);  // {cos_a, sin_a, cos_b, sin_b} for pairs 2p, 2p+1
-    const float2 x1 = __half22float2(l[p]);
-    const float2 x2 = __half22float2(h[p]);
-    const float y1a = x1.x * c.x - x2.x * c.y;
-    const float y2a = x2.x * c.x + x1.x * c.y;
-    const float y1b = x1.y * c.z - x2.y * c.w;
-    const float y2b = x2.y * c.z + x1.y * c.w;
-    l[p] = __floats2half2_rn(y1a, y1b);
-    h[p] = __floats2half2_rn(y2a, y2b);
-  }
-}
-
 constexpr int kRopeMaxThreads = 512;
 constexpr int kRopeRows = 4;  // token rows per block: loads of 4 rows are in flight per thread
 
@@ -82,8 +64,9 @@ __global__ void __launch_bounds__(kRopeMaxThreads) rope_kernel(__half *__restric
   for (int u = 0; u < kRopeRows; ++u) {
     // a position outside the table cannot come from a plan the host checked
     if (p[u] < 0 || p[u] >= max_pos) continue;
-    const float4 *cs = reinterpret_cast<const float4 *>(cos_sin + ((size_t)p[u] * (d / 2) + 8 * c) * 2);
-    rotate8(lo[u], hi[u], cs);
+    float4 cs[4];
+    rope_table8(cos_sin, p[u], d, 8 * c, cs);
+    rope_rotate8(lo[u], hi[u], cs);
     *reinterpret_cast<uint4 *>(x[u]) = lo[u];
     *reinterpret_cast<uint4 *>(x[u] + d / 2) = hi[u];
   }
@@ -110,15 +93,16 @@ extern "C" TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev,
                                   void *k, int32_t hq, int32_t hkv, int32_t d, const float *cos_sin,
                                   int32_t max_pos, tree_stream_t stream) {
   using namespace tree;
-  if (!plan || !plan_dev || !q || !k || !cos_sin) return fail(TREE_ERR_INVALID_ARG, "tree_rope: NULL argument");
+  if (!plan || !plan_dev || !k || !cos_sin) return fail(TREE_ERR_INVALID_ARG, "tree_rope: NULL argument");
+  if (!q) hq = 0;  // keys only
   const Plan &P = plan->p;
   if (chunk < 0 || chunk >= P.n_chunks) return fail(TREE_ERR_INVALID_ARG, "tree_rope: chunk %d out of range", chunk);
-  if (hq <= 0 || hkv <= 0 || d <= 0 || d % 16 || d > 256)
+  if (hq < 0 || (q && hq == 0) || hkv <= 0 || d <= 0 || d % 16 || d > 256)
     return fail(TREE_ERR_UNSUPPORTED, "tree_rope: hq %d hkv %d d %d (d must be a multiple of 16, <= 256)", hq,
                 hkv, d);
   if (max_pos < P.max_pos)
     return fail(TREE_ERR_INVALID_ARG, "tree_rope: table has %d positions, plan needs %d", max_pos, P.max_pos);
-  if (!aligned16(q) || !aligned16(k) || !aligned16(cos_sin) || !aligned16(plan_dev))
+  if ((q && !aligned16(q)) || !aligned16(k) || !aligned16(cos_sin) || !aligned16(plan_dev))
     return fail(TREE_ERR_UNSUPPORTED, "tree_rope: pointers must be 16-byte aligned");
   const int32_t q0 = P.chunk_q0[chunk], n = P.chunk_q1[chunk] - q0;
   const int items = (hq + hkv) * (d / 16);

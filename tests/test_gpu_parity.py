@@ -192,6 +192,22 @@ def test_rope_workloads(lib, n):
     assert np.array_equal(kr[: p.n_res], k[: p.n_res])     # resident rows untouched
 
 
+def test_rope_keys_only(lib):
+    """q=None rotates the keys exactly as the call on queries and keys does, and nothing else."""
+    w = synth.workload(3)
+    r = Run(lib, w.forest, w.max_fwd)
+    p, i = r.oplan, r.plan.info
+    q, k, _ = synth.draw_qkv(p.n_fwd, p.n_tot, w.hq, w.hkv, w.d, w.seed)
+    tab = _dev(lib.rope_table(i.max_pos, w.d, w.theta))
+    s = torch.cuda.current_stream()
+    ka, kb, qd = _dev(k), _dev(k), _dev(q)
+    lib.tree_rope(r.plan, r.dev, 0, qd, ka, w.hq, w.hkv, w.d, tab, i.max_pos, s)
+    lib.tree_rope(r.plan, r.dev, 0, None, kb, w.hq, w.hkv, w.d, tab, i.max_pos, s)
+    torch.cuda.synchronize()
+    assert torch.equal(ka, kb)
+    assert not torch.equal(kb, _dev(k))
+
+
 # ---------------------------------------------------------------- attention
 
 def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per_chunk=48, lse=True,
