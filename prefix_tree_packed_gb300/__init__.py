@@ -102,7 +102,7 @@ _lib.tree_plan_upload.argtypes = [_vp, _vp, C.c_size_t, _vp]
 _lib.tree_plan_upload_staged.argtypes = [_vp, _vp, C.c_size_t, _vp, C.c_size_t, _vp]
 _lib.tree_rope_table.argtypes = [_vp, C.c_int32, C.c_int32, C.c_double]
 _lib.tree_rope.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, _vp,
-                           C.c_int32, _vp]
+                           C.c_int32, _vp, _vp]
 _lib.tree_attn_fwd.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp, C.POINTER(AttnParams),
                                _vp, _vp]
 _lib.tree_attn_fwd_noalloc.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp, C.POINTER(AttnParams),
@@ -230,10 +230,10 @@ def rope_table(max_pos: int, d: int, theta: float) -> np.ndarray:
 
 
 def tree_rope(plan: Plan, plan_dev, chunk: int, q, k, hq: int, hkv: int, d: int, cos_sin,
-              max_pos: int, stream=None):
+              max_pos: int, stream=None, status=None):
     """Rotate the chunk's queries and keys in place (q=None: keys only)."""
     _check(_lib.tree_rope(plan.handle, _ptr(plan_dev), chunk, _ptr(q), _ptr(k), hq, hkv, d,
-                          _ptr(cos_sin), max_pos, _stream(stream)))
+                          _ptr(cos_sin), max_pos, _ptr(status), _stream(stream)))
 
 
 def tree_attn_fwd(plan: Plan, plan_dev, chunk: int, q, k, v, o, lse, hq: int, hkv: int, d: int,

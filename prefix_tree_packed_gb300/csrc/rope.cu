@@ -14,10 +14,13 @@
 // would put ~2e-3 rad of error on the angle at position 32k.
 //
 // The kernel is a streaming pass over the chunk's Q rows and K rows: one
-// thread rotates 8 pairs of one head (two 16-byte loads and stores) in each of
-// 4 consecutive token rows, issuing the loads of all 4 rows before any store;
-// threads of a warp cover consecutive pairs and heads of a row, so every access
-// is a full 32-byte sector; the cos/sin table stays in L1/L2.
+// thread rotates 8 pairs of one head (two 16-byte loads and stores) of one
+// token row; threads of a warp cover consecutive pairs and heads of a row, so
+// every access is a full 32-byte sector; the cos/sin table stays in L1/L2.
+// The pass is bound by memory latency, so it is written for occupancy: one row
+// per thread keeps it at 32 registers and many small blocks in flight
+// (measured on GB300 against 2, 3 and 4 rows per thread, a register cap, and a
+// bulk-copy pipeline through shared memory, all slower).
 
 #include <cmath>
 
@@ -27,7 +30,7 @@ namespace tree {
 namespace {
 
 constexpr int kRopeMaxThreads = 512;
-constexpr int kRopeRows = 4;  // token rows per block: loads of 4 rows are in flight per thread
+constexpr int kRopeRows = 1;  // token rows per block
 
 // Block (x, y): token rows [kRopeRows * x, +kRopeRows) of the chunk, items
 // [blockDim.x * y, +blockDim.x) of a row, where a row's items are (q heads, then kv
@@ -91,8 +94,9 @@ extern "C" TREE_API int tree_rope_table(float *host_out, int32_t max_pos, int32_
 
 extern "C" TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev, int32_t chunk, void *q,
                                   void *k, int32_t hq, int32_t hkv, int32_t d, const float *cos_sin,
-                                  int32_t max_pos, tree_stream_t stream) {
+                                  int32_t max_pos, int32_t *status, tree_stream_t stream) {
   using namespace tree;
+  (void)status;  // this kernel has no waits
   if (!plan || !plan_dev || !k || !cos_sin) return fail(TREE_ERR_INVALID_ARG, "tree_rope: NULL argument");
   if (!q) hq = 0;  // keys only
   const Plan &P = plan->p;

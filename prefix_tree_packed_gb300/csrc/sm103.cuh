@@ -82,6 +82,16 @@ TREE_DEV void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t src) {
                "r"(y), "r"(src)
                : "memory");
 }
+// Shared -> global copy of `bytes` (multiple of 16, both addresses 16-byte aligned), in a bulk group.
+TREE_DEV void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+// Wait until at most N bulk groups of this thread still read shared memory.
+template <int N>
+TREE_DEV void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 TREE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 TREE_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 TREE_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
