@@ -239,8 +239,8 @@ TREE_API int tree_rope_table(float *host_out, int32_t max_pos, int32_t d, double
  * is the device image from tree_plan_upload.  d a multiple of 16 and <= 256;
  * q and k 16-byte aligned.  q may be NULL (hq is then ignored): only the keys
  * are rotated, for a caller that has rotated its queries elsewhere.
- * `status` (device int32, may be NULL) receives TREE_ERR_TIMEOUT if a wait
- * for a copy gave up.
+ * `status` (device int32, may be NULL) is the status word of the other
+ * kernels; this kernel never waits and never writes it.
  */
 TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev, int32_t chunk, void *q, void *k,
               int32_t hq, int32_t hkv, int32_t d, const float *cos_sin, int32_t max_pos,

@@ -96,7 +96,7 @@ extern "C" TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev,
                                   void *k, int32_t hq, int32_t hkv, int32_t d, const float *cos_sin,
                                   int32_t max_pos, int32_t *status, tree_stream_t stream) {
   using namespace tree;
-  (void)status;  // this kernel has no waits
+  (void)status;  // the kernel never waits, so it has nothing to report
   if (!plan || !plan_dev || !k || !cos_sin) return fail(TREE_ERR_INVALID_ARG, "tree_rope: NULL argument");
   if (!q) hq = 0;  // keys only
   const Plan &P = plan->p;
