@@ -112,24 +112,25 @@ class ClockSampler:
 # ------------------------------------------------------------------ GPU arm
 
 class Batch:
-    """One workload resident on the device (N_SETS rotating copies of Q/K/V/O)."""
+    """One workload resident on the device (N_SETS rotating copies of Q/K/V/O).
+
+    A step goes through ``tree_runtime_step``: the host planner packs the batch, and the plan
+    transfer, RoPE, attention and readout run as one chain of kernels on the stream, with the
+    plan buffers alternating so that the host plans step s+1 while the GPU runs step s.
+    """
 
     def __init__(self, lib, torch, w: synth.Workload, dev, n_sets=N_SETS):
         self.lib, self.torch, self.w, self.dev = lib, torch, w, dev
         kw = dict(leaf1=w.leaf1, leaf2=w.leaf2) if w.leaf1 is not None else {}
         self.kw = kw
+        self.spec = lib.Spec.from_forest(w.forest, max_fwd=w.max_fwd, **kw)
         self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, **kw)
         i = self.plan.info
         self.info = i
-        # the plan image double-buffered on the device, uploaded from page-locked
-        # staging on a copy stream while the previous step computes
-        self.pdevs = [torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
-        self.stage = [torch.empty(i.dev_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
-        self.copy_stream = torch.cuda.Stream(device=dev)
-        self.ev_up = [torch.cuda.Event() for _ in range(2)]    # upload into pdevs[k] executed
-        self.ev_done = [torch.cuda.Event() for _ in range(2)]  # last launch reading pdevs[k] executed
-        self.k = 0
-        self.pdev = self.pdevs[0]
+        self.rt = lib.Runtime(i.dev_bytes + 4096, max(i.n_chunks, 1))
+        # a plan on the device for the single-kernel measurements
+        self.pdev = torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev)
+        self.plan.upload(self.pdev, i.dev_bytes, torch.cuda.current_stream())
         q, k, v = synth.draw_qkv(i.n_fwd, i.n_tot, w.hq, w.hkv, w.d, w.seed)
         self.host = dict(q=q, k=k, v=v)
         self.sets = []
@@ -139,8 +140,8 @@ class Batch:
                                   o=torch.empty((i.n_fwd, w.hq, w.d), dtype=torch.float16, device=dev)))
         self.tab = torch.from_numpy(lib.rope_table(i.max_pos, w.d, w.theta)).to(dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.work = torch.zeros(2, dtype=torch.int32, device=dev)  # persistent-CTA work counter
         self.nq = i.n_questions
+        self.logits = self.nl = self.T = self.p_cal = self.choice = None
         if self.nq:
             stride = w.letter_stride
             logits = synth.draw_logits(i.n_slots, stride, w.logit_sigma, w.seed)
@@ -155,47 +156,20 @@ class Batch:
         self.views = [[(b["q"][ci.q0 - i.n_res: ci.q1 - i.n_res], b["o"][ci.q0 - i.n_res: ci.q1 - i.n_res])
                        for ci in self.chunks] for b in self.sets]
 
-    def step(self, s, stream, replan=True, ev=None, bufs=None):
+    def step(self, s, stream, ev=None, bufs=None):
         """Enqueue one whole-path step on `stream` using input set s (or `bufs`).
 
-        ev: optional list that receives one (start, end) CUDA event pair per
-        attention launch, recorded on `stream` around the launch.
+        ev: optional pair of CUDA events, recorded around the step's attention launches.
         """
-        lib, w, i = self.lib, self.w, self.info
-        torch = self.torch
-        if replan:
-            self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, **self.kw)
-        k = self.k
-        self.k ^= 1
-        self.ev_up[k].synchronize()                     # staging k: its copy two steps ago has run
-        self.copy_stream.wait_event(self.ev_done[k])    # pdevs[k]: step s-2 no longer reads it
-        self.plan.upload_staged(self.pdevs[k], i.dev_bytes, self.stage[k], i.dev_bytes, self.copy_stream)
-        self.ev_up[k].record(self.copy_stream)
-        stream.wait_event(self.ev_up[k])
-        self.pdev = self.pdevs[k]
+        w, i = self.w, self.info
         b = bufs if bufs is not None else self.sets[s]
-        for c, ci in enumerate(self.chunks):
-            if bufs is None:
-                qv, ov = self.views[s][c]
-            else:
-                qv, ov = b["q"][ci.q0 - i.n_res: ci.q1 - i.n_res], b["o"][ci.q0 - i.n_res: ci.q1 - i.n_res]
-            lib.tree_rope(self.plan, self.pdev, c, qv, b["k"], w.hq, w.hkv, w.d, self.tab, i.max_pos, stream)
-            if ev is not None:
-                pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                pair[0].record(stream)
-            lib.tree_attn_fwd(self.plan, self.pdev, c, qv, b["k"], b["v"], ov, None, w.hq, w.hkv, w.d,
-                              status=self.status, stream=stream, work=self.work)
-            if ev is not None:
-                pair[1].record(stream)
-                ev.append(pair)
-        if self.nq:
-            base = self.pdev.data_ptr()
-            lib.readout_decide(self.logits, w.letter_stride, base + i.off_r1, base + i.off_r2, self.nl, self.T,
-                               self.nq, self.p_cal, None, self.choice, self.status, stream)
-        self.ev_done[k].record(stream)
+        self.rt.step(self.spec, b["q"], b["k"], b["v"], b["o"], self.tab, i.max_pos, w.hq, w.hkv, w.d,
+                     logits=self.logits, stride=w.letter_stride, n_letters=self.nl, temperature=self.T,
+                     p_cal=self.p_cal, choice=self.choice, status=self.status, stream=stream, attn_events=ev)
 
     def launches_per_step(self):
-        return 2 * len(self.chunks) + (1 if self.nq else 0)
+        # plan transfer, RoPE and attention per chunk, readout
+        return 1 + 2 * len(self.chunks) + (1 if self.nq else 0)
 
 
 def measure_rope(lib, torch, B, stream, reps=40, warmup=None, keys_only=False):
@@ -335,10 +309,14 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     for s in range(args.warmup):
         B.step(s % N_SETS, stream)
+    # event pairs around each step's attention launches, created before the timed region
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in evs:
+        a_.record(stream)
+        b_.record(stream)
     torch.cuda.synchronize()
 
-    # ---- device-resident timed region (events around every attention launch)
-    evs = []
+    # ---- device-resident timed region (events around every step's attention launches)
     clocks = ClockSampler(local)
     clocks.start()
     if dist:
@@ -348,7 +326,7 @@ def run_gpu(args):
     t0.record(stream)
     h0 = time.perf_counter()
     for s in range(args.steps):
-        B.step(s % N_SETS, stream, ev=evs)
+        B.step(s % N_SETS, stream, ev=evs[s])
     host_ms = (time.perf_counter() - h0) * 1e3
     t1.record(stream)
     torch.cuda.synchronize()
@@ -404,7 +382,7 @@ def run_gpu(args):
 
     peaks = _peaks()
     flops = 4.0 * w.d * w.hq * i.pairs                      # QK^T + PV on visible pairs only
-    attn_launch_ms = statistics.mean(attn_ms)
+    attn_launch_ms = statistics.mean(attn_ms) / len(B.chunks)  # the pair spans the step's attention launches
     flops_launch = flops / len(B.chunks)
     achieved = flops_launch / (attn_launch_ms / 1e3) / 1e12
     h_attn = _src_hash("attn.cu")
@@ -419,7 +397,7 @@ def run_gpu(args):
                    "rows": 8 if args.workload == 2 else None, "q_heads": w.hq, "kv_heads": w.hkv,
                    "head_dim": w.d, "visible_pairs_per_head": i.pairs, "chunks": len(B.chunks),
                    "questions": B.nq, "l2": f"{N_SETS} rotating input sets (> L2)",
-                   "step": "plan + upload (pinned staging, copy stream, overlaps the previous step) + rope + attention + readout", "parallelism": f"dp{world} (rows)"},
+                   "step": "tree_runtime_step: plan (host) + plan transfer + rope + attention + readout, one kernel chain", "parallelism": f"dp{world} (rows)"},
         "tflops_attention": round(achieved, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tc"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["tc"], 4), "traffic": traffic,

@@ -24,8 +24,9 @@
  *   - The return value is a status code (TREE_OK = 0 on success).  On failure
  *     tree_last_error() returns a message for the calling thread.
  *   - The caller owns all device memory; the library never allocates device
- *     memory.  Plans live in host memory owned by the library
- *     (tree_pack_plan / tree_plan_free).
+ *     memory, except tree_runtime_create, which allocates its buffers once
+ *     and frees them in tree_runtime_destroy.  Plans live in host memory owned
+ *     by the library (tree_pack_plan / tree_plan_free).
  *   - GPU work is enqueued on the caller's stream (NULL = legacy default
  *     stream) and never synchronised inside the library.  Launch errors are
  *     returned; errors found on the device (a bounded wait that gave up) are
@@ -328,6 +329,62 @@ TREE_API int tree_attn_fwd_noalloc(const tree_plan_t *plan, const void *plan_dev
 TREE_API int readout_decide(const float *logits, int32_t stride, const int32_t *r1, const int32_t *r2,
                    const int32_t *n_letters, const float *temperature, int32_t n_q, float *p_cal,
                    float *p_avg, int32_t *choice, int32_t *status, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Runtime: the whole path of one batch per call                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For callers that run batch after batch on one stream: tree_runtime_step
+ * plans the batch and enqueues the plan image's transfer, tree_rope and
+ * tree_attn_fwd for every chunk, and readout_decide, as one chain of kernels
+ * (each overlapping its predecessor's tail and waiting for it before reading
+ * its results).  The runtime owns two device plan buffers and two page-locked
+ * staging buffers used in turn, so the host can plan the next batch while the
+ * GPU runs this one, plus the attention work counters.  This is orchestration
+ * of the calls above; the pages define no such call.
+ *
+ * tree_runtime_create allocates, once: 2 x max_plan_bytes of device memory and
+ * of page-locked host memory, and 8 x max_chunks bytes of device counters (it
+ * synchronises the device).  tree_runtime_destroy waits for the device and
+ * frees them.  A runtime serves one stream at a time (steps on different
+ * streams would share its buffers and race).
+ */
+typedef struct tree_runtime tree_runtime_t;
+
+TREE_API int tree_runtime_create(size_t max_plan_bytes, int32_t max_chunks, tree_runtime_t **out);
+TREE_API int tree_runtime_destroy(tree_runtime_t *rt);
+
+typedef struct {
+  const tree_spec_t *spec;        /* the batch (host memory, read during the call) */
+  const tree_plan_opts_t *opts;   /* may be NULL: defaults */
+  void *q;                        /* f16 [n_fwd, hq, d]: pre-RoPE queries of all chunks, rotated in place */
+  void *k;                        /* f16 [n_tot, hkv, d]: keys, forward rows rotated in place */
+  const void *v;                  /* f16 [n_tot, hkv, d] */
+  void *o;                        /* f16 [n_fwd, hq, d] output */
+  float *lse;                     /* f32 [n_fwd, hq] or NULL */
+  const float *cos_sin;           /* tree_rope_table on the device */
+  int32_t max_pos;                /* rows of cos_sin, >= the plan's max_pos */
+  int32_t hq, hkv, d;
+  float scale;                    /* 0 = 1/sqrt(d) */
+  const float *logits;            /* f32 [n_slots, stride]; the readout arguments may be NULL  */
+  int32_t stride;                 /*   when the batch has no questions                          */
+  const int32_t *n_letters;       /* [n_questions] */
+  const float *temperature;       /* [n_questions] */
+  float *p_cal, *p_avg;           /* [n_questions, stride]; p_avg may be NULL */
+  int32_t *choice;                /* [n_questions] or NULL */
+  int32_t *status;                /* device int32 or NULL (as for the calls above) */
+  void *attn_events[2];           /* cudaEvent_t pair or NULLs: recorded on the stream just before the
+                                     first and just after the last tree_attn_fwd launch of the step */
+} tree_step_args_t;
+
+/*
+ * One batch.  Errors: those of the calls above, TREE_ERR_UNSUPPORTED when the
+ * plan image exceeds max_plan_bytes or the plan has more chunks than
+ * max_chunks.  info_out (may be NULL) receives the batch's plan summary.
+ */
+TREE_API int tree_runtime_step(tree_runtime_t *rt, const tree_step_args_t *args, tree_plan_info_t *info_out,
+                               tree_stream_t stream);
 
 #ifdef __cplusplus
 }

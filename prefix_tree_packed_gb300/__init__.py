@@ -34,7 +34,8 @@ EXPORTS = (
     "tree_last_error", "tree_version", "tree_pack_plan", "tree_plan_free", "tree_plan_query",
     "tree_plan_chunk", "tree_plan_tables", "tree_plan_upload", "tree_plan_upload_staged", "tree_rope_table",
     "tree_rope",
-    "tree_attn_fwd", "tree_attn_fwd_noalloc", "readout_decide",
+    "tree_attn_fwd", "tree_attn_fwd_noalloc", "readout_decide", "tree_runtime_create", "tree_runtime_destroy",
+    "tree_runtime_step",
 )
 
 
@@ -90,6 +91,15 @@ class AttnParams(C.Structure):
                 ("work", C.c_void_p)]
 
 
+class _StepArgs(C.Structure):
+    _fields_ = [("spec", C.c_void_p), ("opts", C.c_void_p), ("q", C.c_void_p), ("k", C.c_void_p),
+                ("v", C.c_void_p), ("o", C.c_void_p), ("lse", C.c_void_p), ("cos_sin", C.c_void_p),
+                ("max_pos", C.c_int32), ("hq", C.c_int32), ("hkv", C.c_int32), ("d", C.c_int32),
+                ("scale", C.c_float), ("logits", C.c_void_p), ("stride", C.c_int32), ("n_letters", C.c_void_p),
+                ("temperature", C.c_void_p), ("p_cal", C.c_void_p), ("p_avg", C.c_void_p), ("choice", C.c_void_p),
+                ("status", C.c_void_p), ("attn_events", C.c_void_p * 2)]
+
+
 _vp = C.c_void_p
 _lib.tree_last_error.restype = C.c_char_p
 _lib.tree_version.restype = C.c_int
@@ -108,6 +118,11 @@ _lib.tree_attn_fwd.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp, C.P
 _lib.tree_attn_fwd_noalloc.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp, C.POINTER(AttnParams),
                                        _vp, _vp]
 _lib.readout_decide.argtypes = [_vp, C.c_int32, _vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp]
+_lib.tree_runtime_create.argtypes = [C.c_size_t, C.c_int32, C.POINTER(_vp)]
+_lib.tree_runtime_destroy.argtypes = [_vp]
+_lib.tree_runtime_step.argtypes = [_vp, C.POINTER(_StepArgs), C.POINTER(PlanInfo), _vp]
+for _f in ("tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step"):
+    getattr(_lib, _f).restype = C.c_int
 for _f in ("tree_pack_plan", "tree_plan_free", "tree_plan_query", "tree_plan_chunk", "tree_plan_tables",
            "tree_plan_upload", "tree_plan_upload_staged", "tree_rope_table", "tree_rope", "tree_attn_fwd", "tree_attn_fwd_noalloc",
            "readout_decide"):
@@ -137,6 +152,74 @@ def _stream(s) -> int | None:
 
 def version() -> int:
     return _lib.tree_version()
+
+
+class Spec:
+    """A batch's forest as the planner reads it (arrays kept alive, struct built once)."""
+
+    def __init__(self, parent, length, key=None, resident=None, leaf1=None, leaf2=None,
+                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0):
+        self._keep = []
+        par = np.ascontiguousarray(parent, np.int32)
+        ln = np.ascontiguousarray(length, np.int32)
+        self.spec = _Spec()
+        self.spec.n_blocks = par.shape[0]
+        self.spec.parent = par.ctypes.data_as(_i32p)
+        self.spec.length = ln.ctypes.data_as(_i32p)
+        self._keep += [par, ln]
+        if key is not None:
+            k = np.ascontiguousarray(key, np.uint64)
+            self.spec.key = k.ctypes.data_as(C.POINTER(C.c_uint64))
+            self._keep.append(k)
+        if resident is not None:
+            r = np.ascontiguousarray(resident, np.uint8)
+            self.spec.resident = r.ctypes.data_as(C.POINTER(C.c_uint8))
+            self._keep.append(r)
+        if leaf1 is not None:
+            l1 = np.ascontiguousarray(leaf1, np.int32)
+            l2 = np.ascontiguousarray(leaf2, np.int32)
+            self.spec.n_questions = l1.shape[0]
+            self.spec.leaf1 = l1.ctypes.data_as(_i32p)
+            self.spec.leaf2 = l2.ctypes.data_as(_i32p)
+            self._keep += [l1, l2]
+        self.opts = _Opts(max_fwd, max_depth, max_row)
+
+    @classmethod
+    def from_forest(cls, forest, **kw):
+        return cls(forest.parent, forest.length, forest.key, forest.resident, **kw)
+
+
+class Runtime:
+    """``tree_runtime``: the whole path of one batch per ``step`` call, on one stream."""
+
+    def __init__(self, max_plan_bytes: int, max_chunks: int):
+        h = _vp()
+        _check(_lib.tree_runtime_create(max_plan_bytes, max_chunks, C.byref(h)))
+        self.handle = h
+        self.info = PlanInfo()
+
+    def close(self):
+        h = getattr(self, "handle", None)
+        if h:
+            _lib.tree_runtime_destroy(h)
+            self.handle = None
+
+    __del__ = close
+
+    def step(self, spec: Spec, q, k, v, o, cos_sin, max_pos: int, hq: int, hkv: int, d: int, logits=None,
+             stride: int = 0, n_letters=None, temperature=None, p_cal=None, p_avg=None, choice=None,
+             lse=None, status=None, stream=None, scale: float = 0.0, attn_events=None) -> PlanInfo:
+        """attn_events: optional pair of torch.cuda.Event recorded around the step's attention launches."""
+        a = _StepArgs(C.addressof(spec.spec), C.addressof(spec.opts), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                      _ptr(cos_sin), max_pos, hq, hkv, d, scale, _ptr(logits), stride, _ptr(n_letters),
+                      _ptr(temperature), _ptr(p_cal), _ptr(p_avg), _ptr(choice), _ptr(status))
+        if attn_events is not None:
+            h0, h1 = attn_events[0].cuda_event, attn_events[1].cuda_event
+            if not h0 or not h1:
+                raise ValueError("attn_events: record each event once first (torch creates them lazily)")
+            a.attn_events[0], a.attn_events[1] = h0, h1
+        _check(_lib.tree_runtime_step(self.handle, C.byref(a), C.byref(self.info), _stream(stream)))
+        return self.info
 
 
 class Plan:

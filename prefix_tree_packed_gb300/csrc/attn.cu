@@ -262,6 +262,9 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         prefetch_map(&mv);
       }
       __syncwarp();
+      // Q, K, V may come from the kernel before this one in the stream (RoPE):
+      // everything above overlapped its tail; every read of them starts here
+      griddep_wait();
       int t = 0, j = 0, fetched = 0;
       bool ok = true;
       while (ok) {
@@ -292,7 +295,11 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           mbar_arrive(b_if(slot));
         }
         __syncwarp();
-        if (w >= a.n_items) break;
+        if (w >= a.n_items) {
+          // no more items for this CTA: the next kernel in the stream may start launching
+          griddep_launch();
+          break;
+        }
         if (it.n <= 0) continue;  // (a plan never makes one: every query tile sees its own rows)
         const int b = j % C::QBUF;
         if (j >= C::QBUF && !(ok = wait_bar_warp(b_qe(b), ((j / C::QBUF) - 1) & 1, abort, a.status))) break;
@@ -737,7 +744,8 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
   a.work = work;
   if (a.n_items == 0) return TREE_OK;
   const dim3 grid((unsigned)std::min(a.n_items, sm_count()));
-  kern<<<grid, C::THREADS, C::SMEM, s>>>(mq, mk, mv, mo, a);
+  const cudaError_t e = launch_dependent(kern, grid, dim3(C::THREADS), C::SMEM, s, mq, mk, mv, mo, a);
+  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd: launch failed: %s", cudaGetErrorString(e));
   return launch_status("tree_attn_fwd");
 }
 

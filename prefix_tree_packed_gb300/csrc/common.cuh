@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 #include "internal.h"
 
@@ -24,6 +25,25 @@ inline cudaStream_t as_stream(tree_stream_t s) { return reinterpret_cast<cudaStr
 
 // Number of SMs of the current device (cached per process; GB300 has 152).
 int sm_count();
+
+// Launch `kernel` on `s` allowed to start while the stream's previous kernel is
+// still running (programmatic dependent launch): the kernel must execute
+// griddepcontrol.wait before it reads anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Rotary embedding of 8 pairs (x_i, x_{i+d/2}): lo holds x_i .. x_{i+7}, hi the
 // partners, cs their 8 {cos, sin} entries of the table.  The

@@ -24,6 +24,7 @@
 #include <cfloat>
 
 #include "common.cuh"
+#include "sm103.cuh"
 
 namespace tree {
 namespace {
@@ -55,6 +56,7 @@ __global__ void __launch_bounds__(256) readout_kernel(const float *__restrict__ 
                                                       float *__restrict__ p_avg,
                                                       int32_t *__restrict__ choice,
                                                       int32_t *__restrict__ status) {
+  sm103::griddep_wait();  // the logits may come from the kernel before this one in the stream
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const int q = gtid / G;
   const int lane = gtid % G;
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(kTileWarps * 32) readout_tile_kernel(
     float *__restrict__ p_cal, float *__restrict__ p_avg, int32_t *__restrict__ choice,
     int32_t *__restrict__ status) {
   extern __shared__ float tile_smem[];
+  sm103::griddep_wait();  // the logits may come from the kernel before this one in the stream
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t q0 = ((int64_t)blockIdx.x * kTileWarps + warp) * 32;
   if (q0 >= nq) return;  // whole warps leave together
@@ -333,18 +336,22 @@ extern "C" TREE_API int readout_decide(const float *logits, int32_t stride, cons
     const int64_t warps = ((int64_t)n_q + 31) / 32;
     const int blocks = (int)((warps + kTileWarps - 1) / kTileWarps);
     const size_t smem = (size_t)kTileWarps * 64 * pitch * sizeof(float);
-    if (stride <= 16)
-      readout_tile_kernel<16><<<blocks, kTileWarps * 32, smem, s>>>(
-          logits, stride, pitch, magic, r1, r2, n_letters, temperature, n_q, p_cal, p_avg, choice, status);
-    else
-      readout_tile_kernel<32><<<blocks, kTileWarps * 32, smem, s>>>(
-          logits, stride, pitch, magic, r1, r2, n_letters, temperature, n_q, p_cal, p_avg, choice, status);
+    // launched to overlap the previous kernel's tail; the kernels wait for it before reading
+    const cudaError_t e =
+        stride <= 16 ? launch_dependent(readout_tile_kernel<16>, dim3(blocks), dim3(kTileWarps * 32), smem, s, logits,
+                                        stride, pitch, magic, r1, r2, n_letters, temperature, n_q, p_cal, p_avg,
+                                        choice, status)
+                     : launch_dependent(readout_tile_kernel<32>, dim3(blocks), dim3(kTileWarps * 32), smem, s, logits,
+                                        stride, pitch, magic, r1, r2, n_letters, temperature, n_q, p_cal, p_avg,
+                                        choice, status);
+    if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "readout_decide: launch failed: %s", cudaGetErrorString(e));
   } else {
     const int threads = 256;
     const int64_t lanes = (int64_t)n_q * 32;
     const int blocks = (int)((lanes + threads - 1) / threads);
-    readout_kernel<32, 8><<<blocks, threads, 0, s>>>(logits, stride, r1, r2, n_letters, temperature, n_q,
-                                                     p_cal, p_avg, choice, status);
+    const cudaError_t e = launch_dependent(readout_kernel<32, 8>, dim3(blocks), dim3(threads), 0, s, logits, stride,
+                                           r1, r2, n_letters, temperature, n_q, p_cal, p_avg, choice, status);
+    if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "readout_decide: launch failed: %s", cudaGetErrorString(e));
   }
   return launch_status("readout_decide");
 }

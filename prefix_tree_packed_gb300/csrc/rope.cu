@@ -25,9 +25,12 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "sm103.cuh"
 
 namespace tree {
 namespace {
+
+using namespace sm103;
 
 constexpr int kRopeMaxThreads = 512;
 constexpr int kRopeRows = 1;  // token rows per block
@@ -40,6 +43,8 @@ __global__ void __launch_bounds__(kRopeMaxThreads) rope_kernel(__half *__restric
                                                             const int32_t *__restrict__ pos, int32_t q0,
                                                             int32_t nrows, int hq, int hkv, int d,
                                                             const float *__restrict__ cos_sin, int32_t max_pos) {
+  // the attention that follows in the stream may start launching (it waits for this grid before reading)
+  griddep_launch();
   const int per_head = d / 16;
   const int item = blockIdx.y * blockDim.x + threadIdx.x;
   if (item >= (hq + hkv) * per_head) return;

@@ -1,0 +1,157 @@
+// tree_runtime: the whole hot path of one batch in one call, for callers that
+// run batch after batch on one stream.
+//
+//   plan (host) -> plan image to the device -> per chunk: RoPE, attention ->
+//   readout/calibration
+//
+// Each step packs the batch with the host planner, copies the plan image into
+// one of two page-locked staging buffers, and enqueues on the caller's stream:
+// a small kernel that copies the image from the staging buffer (read over the
+// host link) into one of two device image buffers, then tree_rope and
+// tree_attn_fwd for every chunk, then readout_decide.  Everything is one chain
+// of kernels on one stream, each launched to overlap its predecessor's tail and
+// waiting for it (griddepcontrol) before reading its results; there is no copy
+// engine and no second stream in the step.  The two buffers alternate between
+// steps: a staging buffer is rewritten only after the copy kernel that read it
+// two steps earlier has run (an event, normally long passed), and a device
+// image is rewritten only by a kernel that waits for the previous step's last
+// kernel, so the host can plan the next batch while the GPU runs this one.
+
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "sm103.cuh"
+
+struct tree_runtime {
+  size_t cap = 0;  // bytes per plan image
+  int32_t max_chunks = 0;
+  void *dev_image[2] = {nullptr, nullptr};
+  void *staging[2] = {nullptr, nullptr};     // page-locked host memory
+  void *staging_dev[2] = {nullptr, nullptr}; // the same memory as the device sees it
+  cudaEvent_t fetched[2] = {nullptr, nullptr};
+  int32_t *work = nullptr;                   // device int32[2 * max_chunks]: attention work counters
+  uint64_t steps = 0;
+};
+
+namespace tree {
+namespace {
+
+__global__ void __launch_bounds__(256) fetch_image(const int4 *__restrict__ src, int4 *__restrict__ dst, int n16) {
+  // the destination was last read by the kernels of the step before the previous one
+  sm103::griddep_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x) dst[i] = src[i];
+  sm103::griddep_launch();
+}
+
+void release(tree_runtime *rt) {
+  for (int k = 0; k < 2; ++k) {
+    if (rt->dev_image[k]) cudaFree(rt->dev_image[k]);
+    if (rt->staging[k]) cudaFreeHost(rt->staging[k]);
+    if (rt->fetched[k]) cudaEventDestroy(rt->fetched[k]);
+  }
+  if (rt->work) cudaFree(rt->work);
+  delete rt;
+}
+
+}  // namespace
+}  // namespace tree
+
+extern "C" TREE_API int tree_runtime_create(size_t max_plan_bytes, int32_t max_chunks, tree_runtime_t **out) {
+  using namespace tree;
+  if (!out || max_plan_bytes == 0 || max_chunks <= 0)
+    return fail(TREE_ERR_INVALID_ARG, "tree_runtime_create: max_plan_bytes %zu, max_chunks %d", max_plan_bytes,
+                max_chunks);
+  *out = nullptr;
+  auto *rt = new tree_runtime;
+  rt->cap = (max_plan_bytes + 15) / 16 * 16;
+  rt->max_chunks = max_chunks;
+  cudaError_t e = cudaSuccess;
+  for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+    e = cudaMalloc(&rt->dev_image[k], rt->cap);
+    if (e == cudaSuccess) e = cudaHostAlloc(&rt->staging[k], rt->cap, cudaHostAllocMapped);
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(&rt->staging_dev[k], rt->staging[k], 0);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&rt->fetched[k], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) e = cudaMalloc(&rt->work, sizeof(int32_t) * 2 * (size_t)max_chunks);
+  if (e == cudaSuccess) e = cudaMemset(rt->work, 0, sizeof(int32_t) * 2 * (size_t)max_chunks);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();  // the counters are zero before any step
+  if (e != cudaSuccess) {
+    release(rt);
+    return fail(TREE_ERR_CUDA, "tree_runtime_create: %s", cudaGetErrorString(e));
+  }
+  *out = rt;
+  return TREE_OK;
+}
+
+extern "C" TREE_API int tree_runtime_destroy(tree_runtime_t *rt) {
+  if (!rt) return TREE_OK;
+  // buffers may still be in use by queued work
+  for (int k = 0; k < 2; ++k)
+    if (rt->fetched[k]) cudaEventSynchronize(rt->fetched[k]);
+  cudaDeviceSynchronize();
+  tree::release(rt);
+  return TREE_OK;
+}
+
+extern "C" TREE_API int tree_runtime_step(tree_runtime_t *rt, const tree_step_args_t *a, tree_plan_info_t *info_out,
+                                          tree_stream_t stream) {
+  using namespace tree;
+  if (!rt || !a || !a->spec || !a->q || !a->k || !a->v || !a->o || !a->cos_sin)
+    return fail(TREE_ERR_INVALID_ARG, "tree_runtime_step: NULL argument");
+  tree_plan_t *plan = nullptr;
+  int rc = tree_pack_plan(a->spec, a->opts, &plan);
+  if (rc != TREE_OK) return rc;
+  struct Guard {
+    tree_plan_t *p;
+    ~Guard() { tree_plan_free(p); }
+  } guard{plan};
+  const Plan &P = plan->p;
+  const size_t bytes = P.image.size() * sizeof(int32_t);
+  if (bytes > rt->cap)
+    return fail(TREE_ERR_UNSUPPORTED, "tree_runtime_step: plan image of %zu bytes > capacity %zu", bytes, rt->cap);
+  if (P.n_chunks > rt->max_chunks)
+    return fail(TREE_ERR_UNSUPPORTED, "tree_runtime_step: %d chunks > capacity %d", P.n_chunks, rt->max_chunks);
+  if (P.n_questions > 0 && (!a->logits || !a->n_letters || !a->temperature || !a->p_cal))
+    return fail(TREE_ERR_INVALID_ARG, "tree_runtime_step: the batch has questions but no readout buffers");
+  const cudaStream_t s = as_stream(stream);
+  const int k = (int)(rt->steps & 1);
+  // the copy kernel that read staging[k] two steps ago has run
+  cudaError_t e = cudaEventSynchronize(rt->fetched[k]);
+  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_runtime_step: %s", cudaGetErrorString(e));
+  std::memcpy(rt->staging[k], P.image.data(), bytes);
+  const int n16 = (int)(bytes / 16);
+  e = launch_dependent(fetch_image, dim3((unsigned)std::min(152, (n16 + 255) / 256)), dim3(256), 0, s,
+                       reinterpret_cast<const int4 *>(rt->staging_dev[k]), reinterpret_cast<int4 *>(rt->dev_image[k]),
+                       n16);
+  if (e == cudaSuccess) e = cudaEventRecord(rt->fetched[k], s);
+  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_runtime_step: %s", cudaGetErrorString(e));
+  ++rt->steps;
+  const void *img = rt->dev_image[k];
+  const size_t qrow = (size_t)a->hq * a->d * 2;  // bytes per query row
+  for (int c = 0; c < P.n_chunks; ++c) {
+    const int32_t q0 = P.chunk_q0[c];
+    void *qc = static_cast<uint8_t *>(a->q) + (size_t)(q0 - P.n_res) * qrow;
+    void *oc = static_cast<uint8_t *>(a->o) + (size_t)(q0 - P.n_res) * qrow;
+    float *lc = a->lse ? a->lse + (size_t)(q0 - P.n_res) * a->hq : nullptr;
+    rc = tree_rope(plan, img, c, qc, a->k, a->hq, a->hkv, a->d, a->cos_sin, a->max_pos, a->status, stream);
+    if (rc != TREE_OK) return rc;
+    tree_attn_params_t ap = {a->hq, a->hkv, a->d, a->scale, rt->work + 2 * c};
+    if (c == 0 && a->attn_events[0] &&
+        (e = cudaEventRecord(static_cast<cudaEvent_t>(a->attn_events[0]), s)) != cudaSuccess)
+      return fail(TREE_ERR_CUDA, "tree_runtime_step: %s", cudaGetErrorString(e));
+    rc = tree_attn_fwd(plan, img, c, qc, a->k, a->v, oc, lc, &ap, a->status, stream);
+    if (rc != TREE_OK) return rc;
+    if (c == P.n_chunks - 1 && a->attn_events[1] &&
+        (e = cudaEventRecord(static_cast<cudaEvent_t>(a->attn_events[1]), s)) != cudaSuccess)
+      return fail(TREE_ERR_CUDA, "tree_runtime_step: %s", cudaGetErrorString(e));
+  }
+  if (P.n_questions > 0) {
+    const int32_t *base = static_cast<const int32_t *>(img);
+    rc = readout_decide(a->logits, a->stride, base + P.off_r1, base + P.off_r2, a->n_letters, a->temperature,
+                        P.n_questions, a->p_cal, a->p_avg, a->choice, a->status, stream);
+    if (rc != TREE_OK) return rc;
+  }
+  if (info_out) return tree_plan_query(plan, info_out);
+  return TREE_OK;
+}

@@ -93,6 +93,13 @@ TREE_DEV void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 TREE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Programmatic dependent launch.  griddep_wait: block until the grids this one
+// depends on have completed and their writes are visible (returns at once when
+// the grid was launched without a programmatic dependency).  griddep_launch:
+// this CTA no longer holds back the launch of the grid that depends on it.
+TREE_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+TREE_DEV void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 TREE_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 TREE_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Generic-proxy shared-memory writes become visible to the async proxy (TMA).
