@@ -9,6 +9,9 @@
 // "reverse" maps order-2 letter k to original option n-1-k.  The decision is
 // the argmax of p_cal (lowest index on ties); clamp, log, division by T > 0 and
 // softmax are monotone and p sums to 1, so it is taken as the argmax of p.
+// exp, log and the reciprocals use the hardware approximations (__expf,
+// __logf, __fdividef): their error on these probabilities is ~1e-6, and the
+// kernel is bound by its instruction count at large batches.
 //
 // Two work layouts.
 //  * stride <= 32 (the usual 2-10 letters): a warp takes 32 consecutive
@@ -98,15 +101,15 @@ __global__ void __launch_bounds__(256) readout_kernel(const float *__restrict__ 
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     if (lane + G * k < n) {
-      x1[k] = expf(x1[k] - m1);
-      x2[k] = expf(x2[k] - m2);
+      x1[k] = __expf(x1[k] - m1);
+      x2[k] = __expf(x2[k] - m2);
       s1 += x1[k];
       s2 += x2[k];
     }
   }
   s1 = group_sum<G>(s1);
   s2 = group_sum<G>(s2);
-  const float inv1 = 1.f / s1, inv2 = 1.f / s2, invT = 1.f / T;
+  const float inv1 = __fdividef(1.f, s1), inv2 = __fdividef(1.f, s2), invT = __fdividef(1.f, T);
   // p (kept in x1), its calibrated logit (kept in x2), argmax of p
   float m3 = -FLT_MAX, best = -1.f;
   int arg = 0x7fffffff;
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(256) readout_kernel(const float *__restrict__ 
     if (i < n) {
       const float p = 0.5f * (x1[k] * inv1 + x2[k] * inv2);
       x1[k] = p;
-      x2[k] = logf(fmaxf(p, kClamp)) * invT;
+      x2[k] = __logf(fmaxf(p, kClamp)) * invT;
       m3 = fmaxf(m3, x2[k]);
       if (p > best) {  // letters visited in increasing index: first maximum wins
         best = p;
@@ -138,12 +141,12 @@ __global__ void __launch_bounds__(256) readout_kernel(const float *__restrict__ 
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     if (lane + G * k < n) {
-      x2[k] = expf(x2[k] - m3);
+      x2[k] = __expf(x2[k] - m3);
       s3 += x2[k];
     }
   }
   s3 = group_sum<G>(s3);
-  const float inv3 = 1.f / s3;
+  const float inv3 = __fdividef(1.f, s3);
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     const int i = lane + G * k;
@@ -175,12 +178,12 @@ __device__ __forceinline__ int decide_lane(float (&x1)[K], float (&x2)[K], int n
 #pragma unroll
   for (int k = 0; k < K; ++k)
     if (k < n) {
-      x1[k] = expf(x1[k] - m1);
-      x2[k] = expf(x2[k] - m2);
+      x1[k] = __expf(x1[k] - m1);
+      x2[k] = __expf(x2[k] - m2);
       s1 += x1[k];
       s2 += x2[k];
     }
-  const float inv1 = 1.f / s1, inv2 = 1.f / s2, invT = 1.f / T;
+  const float inv1 = __fdividef(1.f, s1), inv2 = __fdividef(1.f, s2), invT = __fdividef(1.f, T);
   float m3 = -FLT_MAX, best = -1.f;
   int arg = 0;
 #pragma unroll
@@ -188,7 +191,7 @@ __device__ __forceinline__ int decide_lane(float (&x1)[K], float (&x2)[K], int n
     if (k < n) {
       const float p = 0.5f * (x1[k] * inv1 + x2[k] * inv2);
       x1[k] = p;
-      x2[k] = logf(fmaxf(p, kClamp)) * invT;
+      x2[k] = __logf(fmaxf(p, kClamp)) * invT;
       m3 = fmaxf(m3, x2[k]);
       if (p > best) {  // increasing index: the first maximum wins
         best = p;
@@ -199,10 +202,10 @@ __device__ __forceinline__ int decide_lane(float (&x1)[K], float (&x2)[K], int n
 #pragma unroll
   for (int k = 0; k < K; ++k)
     if (k < n) {
-      x2[k] = expf(x2[k] - m3);
+      x2[k] = __expf(x2[k] - m3);
       s3 += x2[k];
     }
-  const float inv3 = 1.f / s3;
+  const float inv3 = __fdividef(1.f, s3);
 #pragma unroll
   for (int k = 0; k < K; ++k)
     if (k < n) x2[k] *= inv3;
@@ -210,13 +213,14 @@ __device__ __forceinline__ int decide_lane(float (&x1)[K], float (&x2)[K], int n
 }
 
 constexpr int kTileWarps = 4;  // warps (32-question tiles) per block
+constexpr int kLoopQuestions = 262144;  // from this batch size on, decide with loops (measured crossover)
 
 // Tile layout, stride <= K <= 32.  Shared memory per warp: two 32-row tiles
 // (order 1, order 2) at pitch `pitch` = stride rounded up to odd.  `magic` =
 // ceil(2^16 / stride): for e < 32 * 32 and stride <= 32, (e * magic) >> 16 is
 // exactly e / stride (the rounding error e / 2^16 < 1/64 stays below the gap
 // 1/stride between e / stride and the next integer).
-template <int K>
+template <int K, bool LOOPS>
 __global__ void __launch_bounds__(kTileWarps * 32) readout_tile_kernel(
     const float *__restrict__ logits, int stride, int pitch, uint32_t magic, const int32_t *__restrict__ r1,
     const int32_t *__restrict__ r2, const int32_t *__restrict__ nl, const float *__restrict__ temp, int nq,
@@ -273,7 +277,12 @@ __global__ void __launch_bounds__(kTileWarps * 32) readout_tile_kernel(
   }
   __syncwarp();
 
-  // decide: lane = question; each lane touches only its own two rows
+  // decide: lane = question; each lane touches only its own two rows.  Small
+  // batches keep the letters in registers (fully unrolled: shortest latency);
+  // large ones decide from the rows in shared memory with loops over the n
+  // letters (fewer registers and instructions: more warps in flight).  Both
+  // forms do the same operations in the same order.
+  if (!LOOPS) {
   if (lane < nv) {
     float *ra_s = sa + lane * pitch, *rb_s = sb + lane * pitch;
     if (bad) {
@@ -297,6 +306,61 @@ __global__ void __launch_bounds__(kTileWarps * 32) readout_tile_kernel(
         }
       if (choice) choice[q0 + lane] = arg;
     }
+  }
+  } else {
+  if (lane < nv) {
+    float *ra_s = sa + lane * pitch, *rb_s = sb + lane * pitch;
+    if (bad) {
+      for (int i = 0; i < stride; ++i) ra_s[i] = rb_s[i] = 0.f;
+      if (choice) choice[q0 + lane] = -1;
+      if (status) atomicExch(status, TREE_ERR_INVALID_ARG);
+    } else {
+      const int n = my_n;
+      float m1 = -FLT_MAX, m2 = -FLT_MAX;
+      for (int i = 0; i < n; ++i) {
+        m1 = fmaxf(m1, ra_s[i]);
+        m2 = fmaxf(m2, rb_s[i]);
+      }
+      float s1 = 0.f, s2 = 0.f;
+      // option i of order 2 is letter n-1-i of its row; each slot is read, then overwritten
+      for (int i = 0; i < n; ++i) {
+        const float e1 = __expf(ra_s[i] - m1), e2 = __expf(rb_s[n - 1 - i] - m2);
+        s1 += e1;
+        s2 += e2;
+        ra_s[i] = e1;
+        rb_s[n - 1 - i] = e2;
+      }
+      const float inv1 = __fdividef(1.f, s1), inv2 = __fdividef(1.f, s2), invT = __fdividef(1.f, T);
+      float m3 = -FLT_MAX, best = -1.f;
+      int arg = 0;
+      for (int i = 0; i < n; ++i) {
+        const float p = 0.5f * (ra_s[i] * inv1 + rb_s[n - 1 - i] * inv2);
+        const float lg = __logf(fmaxf(p, kClamp)) * invT;
+        ra_s[i] = lg;
+        rb_s[n - 1 - i] = p;  // in reversed order for now
+        m3 = fmaxf(m3, lg);
+        if (p > best) {  // increasing index: the first maximum wins
+          best = p;
+          arg = i;
+        }
+      }
+      for (int i = 0; i < n / 2; ++i) {  // p_avg into original option order
+        const float t = rb_s[i];
+        rb_s[i] = rb_s[n - 1 - i];
+        rb_s[n - 1 - i] = t;
+      }
+      for (int i = n; i < stride; ++i) rb_s[i] = 0.f;
+      float s3 = 0.f;
+      for (int i = 0; i < n; ++i) {
+        const float e3 = __expf(ra_s[i] - m3);
+        s3 += e3;
+        ra_s[i] = e3;
+      }
+      const float inv3 = __fdividef(1.f, s3);
+      for (int i = 0; i < stride; ++i) ra_s[i] = i < n ? ra_s[i] * inv3 : 0.f;
+      if (choice) choice[q0 + lane] = arg;
+    }
+  }
   }
   __syncwarp();
 
@@ -337,13 +401,11 @@ extern "C" TREE_API int readout_decide(const float *logits, int32_t stride, cons
     const int blocks = (int)((warps + kTileWarps - 1) / kTileWarps);
     const size_t smem = (size_t)kTileWarps * 64 * pitch * sizeof(float);
     // launched to overlap the previous kernel's tail; the kernels wait for it before reading
-    const cudaError_t e =
-        stride <= 16 ? launch_dependent(readout_tile_kernel<16>, dim3(blocks), dim3(kTileWarps * 32), smem, s, logits,
-                                        stride, pitch, magic, r1, r2, n_letters, temperature, n_q, p_cal, p_avg,
-                                        choice, status)
-                     : launch_dependent(readout_tile_kernel<32>, dim3(blocks), dim3(kTileWarps * 32), smem, s, logits,
-                                        stride, pitch, magic, r1, r2, n_letters, temperature, n_q, p_cal, p_avg,
-                                        choice, status);
+    const bool loops = n_q >= kLoopQuestions;
+    auto kern = stride <= 16 ? (loops ? readout_tile_kernel<16, true> : readout_tile_kernel<16, false>)
+                             : (loops ? readout_tile_kernel<32, true> : readout_tile_kernel<32, false>);
+    const cudaError_t e = launch_dependent(kern, dim3(blocks), dim3(kTileWarps * 32), smem, s, logits, stride, pitch,
+                                           magic, r1, r2, n_letters, temperature, n_q, p_cal, p_avg, choice, status);
     if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "readout_decide: launch failed: %s", cudaGetErrorString(e));
   } else {
     const int threads = 256;
