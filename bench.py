@@ -288,6 +288,27 @@ def run_only(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ ranks (one GPU each)
+
+def rank_workload(n: int, rank: int) -> synth.Workload:
+    """Each rank packs and runs its own batch (rows are independent: no data exchange)."""
+    return synth.workload(n, seed=n + 101 * rank)
+
+
+def max_over_ranks(dist, values, device):
+    """Elementwise max of per-rank timings (the only collective, outside the timed region)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_value(tokens_per_step: int, world: int, steps: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_step * world * steps / (ms / 1e3)
+
+
 def run_gpu(args):
     import torch
 
@@ -303,7 +324,7 @@ def run_gpu(args):
     import prefix_tree_packed_gb300 as lib
 
     # every rank packs and runs its own batch: rows are independent, no data exchange
-    w = synth.workload(args.workload, seed=args.workload + 101 * rank)
+    w = rank_workload(args.workload, rank)
     B = Batch(lib, torch, w, dev)
     i = B.info
     stream = torch.cuda.current_stream()
@@ -372,13 +393,10 @@ def run_gpu(args):
     e2e_ms = a.elapsed_time(b)
 
     # ---- max over ranks
-    ms = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(ms[0]), float(ms[1])
+    total_ms, e2e_ms = max_over_ranks(dist, [total_ms, e2e_ms], dev)
     toks_step = i.n_fwd
-    value = toks_step * world * args.steps / (total_ms / 1e3)
-    e2e_value = toks_step * world * args.steps / (e2e_ms / 1e3)
+    value = job_value(toks_step, world, args.steps, total_ms)
+    e2e_value = job_value(toks_step, world, args.steps, e2e_ms)
 
     peaks = _peaks()
     flops = 4.0 * w.d * w.hq * i.pairs                      # QK^T + PV on visible pairs only
