@@ -96,6 +96,9 @@ struct Cfg {
   // tensor memory and barriers instead of competing for the same issue slots.
   static constexpr bool ALT = NH == 2 && D == 64;
   static constexpr bool PSEP = D == 64;           // P in its own columns
+  // d = 128: an item's epilogue waits until the next item's first P is stored
+  // (measured faster there; at d = 64 it delays the next item's first PV)
+  static constexpr bool DEFER = !PSEP;
   static constexpr uint32_t P_COL = 128 * NH;     // P_h at P_COL + 64h (PSEP only)
   static constexpr uint32_t O_COL = PSEP ? 128 * NH + 64 * NH : 128 * NH;
   static constexpr uint32_t TMEM_USED = O_COL + D * NH;
@@ -498,6 +501,67 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     const uint32_t tO = t_lane + C::O_COL + D * h;
     bool ok = true;
     int T = 0, stage_uses = 0;
+    // With DEFER the epilogue of an item waits until the P of the next item's
+    // first tile is stored: the wait for the item's last PV then overlaps that
+    // tile's arithmetic.  The finished item's state waits here meanwhile.
+    bool pend = false;
+    Item pit{};
+    int piq = 0;
+    float pm = 0.f, pl = 0.f;
+    auto epilogue = [&]() -> bool {
+      // ---- read O_h, hand its columns back, then O / l -> f16 rows
+      if (!wait_bar_warp(b_o(h), (T - 1) & 1, abort, a.status)) return false;
+      fence_after();
+      uint32_t o[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, o + 32 * c);
+      tmem_wait_ld();
+      fence_before();
+      mbar_arrive(b_of(h));
+      // O / l as f16 into this head's 128-byte-swizzled staging box, 64 columns at
+      // a time; row 0's thread issues one TMA store per box once every row is
+      // written.  It waits for a store to have read the box only when the box
+      // is next needed (normally an item later, long done), and then hands it
+      // back, so no warp stalls on the store here.  Rows past the chunk are
+      // clipped by the store.
+      const float inv = 1.f / pl;
+      const uint32_t stage = s_base + C::O_OFF + h * BOX_BYTES;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int use = stage_uses++;
+        if (use > 0) {
+          if (r == 0) {
+            bulk_wait_read0();
+            mbar_arrive(b_osf(h));
+          }
+          if (!wait_bar_warp(b_osf(h), (use - 1) & 1, abort, a.status)) return false;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t *x = o + 64 * c + 8 * u;
+          const uint4 v4 = make_uint4(pack_f16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                                      pack_f16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                                      pack_f16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                                      pack_f16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+          const uint32_t addr = stage + r * 128 + ((u ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v4.x), "r"(v4.y), "r"(v4.z),
+                       "r"(v4.w)
+                       : "memory");
+        }
+        fence_async_shared();
+        mbar_arrive(b_osq(h));
+        if (r == 0 && wait_bar(b_osq(h), use & 1, abort, a.status)) {
+          tma_store_2d(&mo, (pit.h0 + h) * D + 64 * c, pit.qt.row0 - a.q0, stage);
+          bulk_commit();
+        }
+      }
+      if (a.lse && piq < pit.qt.row1) {
+        const float mu = (pm == -INFINITY) ? 0.f : pm;
+        a.lse[(size_t)(piq - a.q0) * a.hq + pit.h0 + h] = (mu + __log2f(pl)) * 0.69314718055994531f;
+      }
+      pend = false;
+      return true;
+    };
     for (int taken = 0; ok; ++taken) {
       const int slot = taken % kRing;
       if (!(ok = wait_bar_warp(b_if(slot), (taken / kRing) & 1, abort, a.status))) break;
@@ -585,11 +649,10 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(my_turn);
         }
-        // PV_h of the previous tile of this item must be done before P_h is
-        // rewritten (separate P) or O_h is rescaled; for an item's first tile the
-        // previous item's epilogue has already waited for it
+        // PV_h of the previous tile must be done before P_h is rewritten
+        // (separate P) or O_h is rescaled
         const bool need_o = i > 0 && __any_sync(0xffffffffu, grow);
-        if (i > 0 && (C::PSEP || need_o)) {
+        if ((i > 0 || pend) && (C::PSEP || need_o)) {
           if (!(ok = wait_bar_warp(b_o(h), (T - 1) & 1, abort, a.status))) break;
           fence_after();
         }
@@ -608,60 +671,19 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         tmem_wait_st();
         fence_before();
         mbar_arrive(b_p(h));
+        // the previous item's epilogue, now that this item's first P is stored
+        // (its first PV waits for the previous O to be read)
+        if (pend && !(ok = epilogue())) break;
       }
       if (!ok) break;
-      // ---- item epilogue: read O_h, hand its columns back, then O / l -> f16 rows
-      if (!(ok = wait_bar_warp(b_o(h), (T - 1) & 1, abort, a.status))) break;
-      fence_after();
-      uint32_t o[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, o + 32 * c);
-      tmem_wait_ld();
-      fence_before();
-      mbar_arrive(b_of(h));
-      // O / l as f16 into this head's 128-byte-swizzled staging box, 64 columns at
-      // a time; row 0's thread issues one TMA store per box once every row is
-      // written.  It waits for a store to have read the box only when the box
-      // is next needed (normally an item later, long done), and then hands it
-      // back, so no warp stalls on the store here.  Rows past the chunk are
-      // clipped by the store.
-      const float inv = 1.f / l;
-      const uint32_t stage = s_base + C::O_OFF + h * BOX_BYTES;
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int use = stage_uses++;
-        if (use > 0) {
-          if (r == 0) {
-            bulk_wait_read0();
-            mbar_arrive(b_osf(h));
-          }
-          if (!(ok = wait_bar_warp(b_osf(h), (use - 1) & 1, abort, a.status))) break;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t *x = o + 64 * c + 8 * u;
-          const uint4 v4 = make_uint4(pack_f16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
-                                      pack_f16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
-                                      pack_f16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
-                                      pack_f16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
-          const uint32_t addr = stage + r * 128 + ((u ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v4.x), "r"(v4.y), "r"(v4.z),
-                       "r"(v4.w)
-                       : "memory");
-        }
-        fence_async_shared();
-        mbar_arrive(b_osq(h));
-        if (r == 0 && wait_bar(b_osq(h), use & 1, abort, a.status)) {
-          tma_store_2d(&mo, (it.h0 + h) * D + 64 * c, it.qt.row0 - a.q0, stage);
-          bulk_commit();
-        }
-      }
-      if (!ok) break;
-      if (a.lse && iq < it.qt.row1) {
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        a.lse[(size_t)(iq - a.q0) * a.hq + it.h0 + h] = (mu + __log2f(l)) * 0.69314718055994531f;
-      }
+      pend = true;
+      pit = it;
+      piq = iq;
+      pm = m;
+      pl = l;
+      if (!C::DEFER && !(ok = epilogue())) break;
     }
+    if (ok && pend) ok = epilogue();
     if (r == 0) bulk_wait0();  // every output store has completed
   }
   fence_before();
