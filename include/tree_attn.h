@@ -151,6 +151,7 @@ typedef struct {
   size_t dev_bytes;      /* size of the device image (tree_plan_upload) */
   /* byte offsets of the device image's arrays (int32 each) */
   size_t off_pos, off_send, off_qtile, off_ent, off_order, off_chunk, off_slot_tok, off_r1, off_r2;
+  size_t off_runs;       /* run tables of the key tiles (see tree_plan_host_view_t.runs) */
 } tree_plan_info_t;
 
 TREE_API int tree_plan_query(const tree_plan_t *plan, tree_plan_info_t *info);
@@ -182,6 +183,11 @@ typedef struct {
   const int32_t *r1, *r2;                         /* [n_questions] readout slots of each question */
   const void *image;                              /* the device image, host copy */
   size_t image_bytes;
+  const int32_t *runs;  /* [ceil(n_tot/128)][84] per 128-key tile, its keys split into maximal runs of
+                           equal send: word 0 the number of runs n; if n <= 16, words 4 + r the run's
+                           send, words 20 + 4r .. 23 + 4r its keys as a 128-bit mask (key c of the
+                           tile is bit c % 32 of word c / 32); all else 0.  A query i sees the keys
+                           of run r, apart from keys after i, iff i < send of r. */
 } tree_plan_host_view_t;
 
 TREE_API int tree_plan_tables(const tree_plan_t *plan, tree_plan_host_view_t *view);

@@ -68,7 +68,7 @@ class PlanInfo(C.Structure):
         "n_entries", "n_slots", "n_questions", "max_fwd", "bm", "bn", "max_pos")] + [
         ("pairs", C.c_int64), ("dev_bytes", C.c_size_t)] + [(n, C.c_size_t) for n in (
         "off_pos", "off_send", "off_qtile", "off_ent", "off_order", "off_chunk", "off_slot_tok",
-        "off_r1", "off_r2")]
+        "off_r1", "off_r2", "off_runs")]
 
 
 class ChunkInfo(C.Structure):
@@ -83,7 +83,8 @@ _VIEW_FIELDS = ("block_map", "blk_start", "blk_len", "blk_parent", "blk_depth", 
 
 
 class _View(C.Structure):
-    _fields_ = [(n, _i32p) for n in _VIEW_FIELDS] + [("image", C.c_void_p), ("image_bytes", C.c_size_t)]
+    _fields_ = [(n, _i32p) for n in _VIEW_FIELDS] + [("image", C.c_void_p), ("image_bytes", C.c_size_t),
+                                                     ("runs", _i32p)]
 
 
 class AttnParams(C.Structure):
@@ -295,6 +296,7 @@ class Plan:
             out[n] = np.ctypeslib.as_array(p, shape=(cnt,)).copy() if cnt > 0 else np.zeros(0, np.int32)
         out["image"] = np.ctypeslib.as_array(C.cast(v.image, C.POINTER(C.c_uint8)),
                                              shape=(v.image_bytes,)).copy()
+        out["runs"] = np.ctypeslib.as_array(v.runs, shape=(n_kvt, 84)).copy()
         return out
 
     def upload(self, dev_buf, nbytes: int, stream=None):

@@ -60,6 +60,7 @@ constexpr uint64_t kDrainNs = 500000000ull;
 
 struct AttnArgs {
   const int32_t *send;
+  const int32_t *runs;  // run tables of the key tiles
   const QTile *qtiles;
   const int32_t *ent;
   const int32_t *order;
@@ -82,18 +83,13 @@ struct Cfg {
   static constexpr uint32_t K_OFF = Q_OFF + QBUF * Q_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + STAGES * CB * BOX_BYTES;
   static constexpr uint32_t O_OFF = V_OFF + STAGES * CB * BOX_BYTES;  // per head: one 128 x 64 staging box
-  static constexpr uint32_t SEND_OFF = O_OFF + NH * BOX_BYTES;
-  static constexpr uint32_t SMEM = SEND_OFF + STAGES * 512 + 1024;  // + alignment slack
+  static constexpr uint32_t RUNS_OFF = O_OFF + NH * BOX_BYTES;       // per stage: the key tile's run table
+  static constexpr uint32_t SMEM = RUNS_OFF + STAGES * 512 + 1024;  // + alignment slack
   static constexpr int WARPS = 4 * NH + 4;        // softmax warpgroups + producer/MMA warpgroup
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int PROD_WARP = 4 * NH;
   static constexpr int MMA_WARP = 4 * NH + 1;    // MMA warps MMA_WARP .. MMA_WARP + MW - 1
   static constexpr int MW = D == 64 ? NH : 1;     // MMA warps: one per head at d = 64, one at d = 128
-  static constexpr int RUNS_WARP = 4 * NH + 3;    // builds the run tables of partial key tiles
-  // Run tables (d = 128 only): measured faster there; at d = 64 the partial
-  // tiles are mostly diagonal tiles whose keys land just before their scores,
-  // and waiting for the table costs more than testing the keys one by one.
-  static constexpr bool RUNS = D == 128;
   static constexpr bool KV_ONE = STAGES >= 3;     // K and V of a stage complete one barrier
   // At d = 64 the two heads' softmax warps that share an SM sub-partition take
   // turns at the arithmetic of a tile (head 0, head 1, head 0, ...): the
@@ -120,8 +116,6 @@ struct Bars {
   int32_t ring[kRing][8];  // claimed item: {w, row0, row1, ent0, ent1, h0, g, first entry}
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[3], v_full[3], kv_empty[3];
-  uint64_t runs_ready[3];  // the stage's run table is written (one phase per tile, in order)
-  int32_t runs_n[3];       // runs in the stage's key tile
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
   uint64_t ostage_full[2], ostage_free[2];  // output staging box of each head
   uint64_t turn[2][4];  // per lane quarter: head h's warp has finished the arithmetic of its tile
@@ -156,36 +150,6 @@ TREE_DEV bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort, i
 TREE_DEV bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *status) {
   const bool ok = wait_bar(bar, parity, abort, status);
   return __all_sync(0xffffffffu, ok);
-}
-
-// Run table of a partial key tile: its keys split into runs of equal subtree
-// end.  A query i sees the keys of run r (j <= i aside) iff i < end[r], so its
-// 128-bit visibility mask is the OR of the masks of those runs.  Written over
-// the stage's subtree ends when the tile has at most kMaxRuns runs (else the
-// ends stay, and the mask is built from them key by key).
-constexpr int kMaxRuns = 16;
-struct RunTable {
-  int32_t end[kMaxRuns];
-  uint4 bits[kMaxRuns];
-};
-static_assert(sizeof(RunTable) <= 512, "run table");
-
-// Bounded wait that naps between tests, for a warp that is not on the
-// critical path (it leaves the issue slots to the warps it shares them with).
-TREE_DEV bool wait_bar_nap(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *status) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
-    __nanosleep(128);
-    if ((n & 63) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitNs) {
-        *abort = 1;
-        if (status) atomicExch(status, TREE_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
 }
 
 // One work item: a query tile, the kv head g, and the NH q heads h0.. that read it.
@@ -227,7 +191,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   __shared__ Bars bars;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(sm);
-  const int32_t *sSend = reinterpret_cast<const int32_t *>(sm + C::SEND_OFF);
+  const int32_t *sRuns = reinterpret_cast<const int32_t *>(sm + C::RUNS_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int32_t *abort = &bars.abort;
 
@@ -249,7 +213,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int r = 0; r < kRing; ++r) {
       mbar_init(b_if(r), 1);
-      mbar_init(b_ie(r), NH * 128 + C::MW + (C::RUNS ? 1 : 0));  // softmax threads, MMA warps, runs warp
+      mbar_init(b_ie(r), NH * 128 + C::MW);  // every softmax thread and each MMA warp
     }
     for (int b = 0; b < C::QBUF; ++b) {
       mbar_init(b_qf(b), 1);
@@ -259,7 +223,6 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       mbar_init(b_k(s), 1);
       mbar_init(b_v(s), 1);
       mbar_init(b_e(s), C::MW);  // one commit per MMA warp
-      mbar_init(smem_u32(&bars.runs_ready[s]), 32);
     }
     for (int h = 0; h < NH; ++h) {
       mbar_init(b_s(h), 1);
@@ -363,11 +326,11 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
             // barrier (the loads run far enough ahead that V is in place before
             // the QK is issued); with two, V has its own
             const uint32_t v_bar = C::KV_ONE ? b_k(st) : b_v(st);
-            mbar_expect_tx(b_k(st), (C::KV_ONE ? 2 : 1) * C::CB * BOX_BYTES + 512);
+            mbar_expect_tx(b_k(st), (C::KV_ONE ? 2 : 1) * C::CB * BOX_BYTES + kRunWords * 4);
 #pragma unroll
             for (int c = 0; c < C::CB; ++c)
               tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES, &mk, it.g * D + 64 * c, j0, b_k(st));
-            bulk_load(s_base + C::SEND_OFF + st * 512, a.send + j0, 512, b_k(st));
+            bulk_load(s_base + C::RUNS_OFF + st * 512, a.runs + (size_t)(j0 / BN) * kRunWords, kRunWords * 4, b_k(st));
             if (!C::KV_ONE) mbar_expect_tx(v_bar, C::CB * BOX_BYTES);
 #pragma unroll
             for (int c = 0; c < C::CB; ++c)
@@ -527,68 +490,6 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       }
       if (!ok && last_qk >= 0)
         for (int h = hb; h < he; ++h) wait_bar(b_s(h), last_qk & 1, abort, nullptr, false, kDrainNs);
-    } else if (C::RUNS && warp == C::RUNS_WARP) {
-      // ---------------------------------------------------------- run tables of partial key tiles
-      // Follows the CTA's tiles in order; for every tile it waits for the
-      // stage's keys (so it never runs a stage ahead of its readers), builds the
-      // run table when the tile is partial, and completes the stage's phase.
-      // Lane l holds keys 4l .. 4l+3.
-      int taken = 0, T = 0;
-      bool okr = true;
-      while (okr) {
-        const int slot = taken % kRing;
-        if (!wait_bar_nap(b_if(slot), (taken / kRing) & 1, abort, a.status)) break;
-        int w, e_next;
-        Item it;
-        ring_item(slot, w, it, e_next);
-        __syncwarp();
-        if (elect_one()) mbar_arrive(b_ie(slot));
-        __syncwarp();
-        ++taken;
-        if (w >= a.n_items) break;
-        for (int i = 0; i < it.n; ++i, ++T) {
-          const int st = T % C::STAGES;
-          const int e = e_next;
-          if (i + 1 < it.n) e_next = __ldg(a.ent + it.qt.ent0 + i + 1);
-          if (!(okr = wait_bar_warp(b_k(st), (T / C::STAGES) & 1, abort, a.status))) break;
-          if (e & 1) {
-            int32_t *sd = const_cast<int32_t *>(sSend) + st * 128;
-            const int4 sv4 = reinterpret_cast<const int4 *>(sd)[lane];
-            const int v[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
-            int prev = __shfl_up_sync(0xffffffffu, v[3], 1);
-            if (lane == 0) prev = -1;  // subtree ends are >= 0
-            const int f0 = v[0] != prev, f1 = v[1] != v[0], f2 = v[2] != v[1], f3 = v[3] != v[2];
-            const int cnt = f0 + f1 + f2 + f3;
-            int incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const int y = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += y;
-            }
-            const int R = __shfl_sync(0xffffffffu, incl, 31);
-            const int r0 = incl - cnt + f0 - 1, r1 = r0 + f1, r2 = r1 + f2, r3 = r2 + f3;
-            __syncwarp();  // every lane has read the ends before the table overwrites them
-            if (lane == 0) bars.runs_n[st] = R;
-            if (R <= kMaxRuns) {
-              RunTable *tb = reinterpret_cast<RunTable *>(sd);
-              if (f0) tb->end[r0] = v[0];
-              if (f1) tb->end[r1] = v[1];
-              if (f2) tb->end[r2] = v[2];
-              if (f3) tb->end[r3] = v[3];
-              for (int r = 0; r < R; ++r) {
-                uint32_t word = (uint32_t)((r0 == r) | ((r1 == r) << 1) | ((r2 == r) << 2) | ((r3 == r) << 3))
-                                << (4 * (lane & 7));
-                word |= __shfl_xor_sync(0xffffffffu, word, 1);
-                word |= __shfl_xor_sync(0xffffffffu, word, 2);
-                word |= __shfl_xor_sync(0xffffffffu, word, 4);
-                if ((lane & 7) == 0) reinterpret_cast<uint32_t *>(&tb->bits[r])[lane >> 3] = word;
-              }
-            }
-          }
-          __syncwarp();
-          mbar_arrive(smem_u32(&bars.runs_ready[st]));
-        }
-      }
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -677,11 +578,8 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         const int st = T % C::STAGES;
         const int e = e_next;  // the next tile's entry loads while this one is processed
         if (i + 1 < it.n) e_next = __ldg(a.ent + it.qt.ent0 + i + 1);
-        // a partial tile also needs its run table (built once its keys have
-        // landed), or without run tables the subtree ends (same stage as K)
-        if ((e & 1) && !(ok = wait_bar_warp(C::RUNS ? smem_u32(&bars.runs_ready[st]) : b_k(st),
-                                            (T / C::STAGES) & 1, abort, a.status)))
-          break;
+        // a partial tile also needs the run table of its keys (same stage as K)
+        if ((e & 1) && !(ok = wait_bar_warp(b_k(st), (T / C::STAGES) & 1, abort, a.status))) break;
         if (!(ok = wait_bar_warp(b_s(h), T & 1, abort, a.status))) break;
         fence_after();
         uint32_t s[128];
@@ -700,33 +598,19 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           if (h == 1 && !(ok = wait_bar_warp(other_turn, T & 1, abort, a.status))) break;
           if (h == 0 && T > 0 && !(ok = wait_bar_warp(other_turn, (T - 1) & 1, abort, a.status))) break;
         }
-        if ((e & 1) && !C::RUNS) {
-          // partial tile: key j = j0 + c is visible iff j <= iq < send[j]
-          const int cmax = iq - (e >> 1) * BN;  // keys c <= cmax are not after the query
-          const int4 *sd = reinterpret_cast<const int4 *>(sSend + st * 128);
-#pragma unroll
-          for (int c4 = 0; c4 < 32; ++c4) {
-            const int4 se = sd[c4];
-            const int sv[4] = {se.x, se.y, se.z, se.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int c = 4 * c4 + u;
-              if (!((c <= cmax) && (iq < sv[u]))) s[c] = __float_as_uint(-INFINITY);
-            }
-          }
-        }
-        if ((e & 1) && C::RUNS) {
+        if (e & 1) {
           // partial tile: key j = j0 + c is visible iff j <= iq < send[j].  The
-          // row's 128-bit mask, then one bit test per score.
-          const int cmax = iq - (e >> 1) * BN;  // keys c <= cmax are not after the query
-          const int R = bars.runs_n[st];
+          // row's 128-bit mask (the runs of the tile that end after the query,
+          // cut at the query's own column), then one bit test per score.
+          const int j0 = (e >> 1) * BN;
+          const int cmax = iq - j0;  // keys c <= cmax are not after the query
+          const int32_t *tb = sRuns + st * 128;
+          const int R = tb[0];
           uint32_t mw0 = 0u, mw1 = 0u, mw2 = 0u, mw3 = 0u;
           if (R <= kMaxRuns) {
-            // the runs whose subtree ends after the query
-            const RunTable *tb = reinterpret_cast<const RunTable *>(sSend + st * 128);
             for (int rr = 0; rr < R; ++rr) {
-              const bool vis = iq < tb->end[rr];
-              const uint4 b = tb->bits[rr];
+              const bool vis = iq < tb[4 + rr];
+              const uint4 b = reinterpret_cast<const uint4 *>(tb + 20)[rr];
               mw0 |= vis ? b.x : 0u;
               mw1 |= vis ? b.y : 0u;
               mw2 |= vis ? b.z : 0u;
@@ -734,10 +618,10 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
             }
           } else {
             // many short blocks: test the keys' subtree ends one by one
-            const int4 *sd = reinterpret_cast<const int4 *>(sSend + st * 128);
+            const int4 *sd = reinterpret_cast<const int4 *>(a.send + j0);
 #pragma unroll 1
             for (int c4 = 0; c4 < 32; ++c4) {
-              const int4 se = sd[c4];
+              const int4 se = __ldg(sd + c4);
               const uint32_t nib = (uint32_t)(iq < se.x) | ((uint32_t)(iq < se.y) << 1) |
                                    ((uint32_t)(iq < se.z) << 2) | ((uint32_t)(iq < se.w) << 3);
               const uint32_t bit = nib << (4 * (c4 & 7));
@@ -750,7 +634,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           }
           uint32_t mw[4] = {mw0, mw1, mw2, mw3};
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {  // cut at the query's own column
+          for (int q4 = 0; q4 < 4; ++q4) {
             const int k = cmax - 32 * q4;
             mw[q4] &= k >= 31 ? 0xffffffffu : (k < 0 ? 0u : (0xffffffffu >> (31 - k)));
           }
@@ -894,6 +778,7 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
     return rc;
   AttnArgs a;
   a.send = img + P.off_send;
+  a.runs = img + P.off_runs;
   a.qtiles = reinterpret_cast<const QTile *>(img + P.off_qtile);
   a.ent = img + P.off_ent;
   a.order = img + P.off_order;

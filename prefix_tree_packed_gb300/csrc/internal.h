@@ -30,8 +30,19 @@ struct Plan {
   // device image: int32 words, arrays 16-byte aligned
   std::vector<int32_t> image;
   size_t off_pos = 0, off_send = 0, off_qtile = 0, off_ent = 0, off_order = 0, off_chunk = 0,
-         off_slot_tok = 0, off_r1 = 0, off_r2 = 0;  // in int32 words
+         off_slot_tok = 0, off_r1 = 0, off_r2 = 0, off_runs = 0;  // in int32 words
 };
+
+// Run table of a 128-key tile, in the device image (kRunWords int32 words per
+// key tile): the tile's keys split into maximal runs of equal subtree end.
+// A query i sees the keys of run r (apart from keys after i) iff i < end[r],
+// so its 128-bit visibility mask is the OR of those runs' masks.
+//   word 0        n, the number of runs (> kMaxRuns: the rest is not filled)
+//   words 1-3     0
+//   words 4-19    end[kMaxRuns]
+//   words 20-83   bits[kMaxRuns][4]: key c of the tile is bit c%32 of word c/32
+constexpr int kMaxRuns = 16;
+constexpr int kRunWords = 84;  // 336 bytes, a multiple of 16
 
 // Device image record for one query tile (off_qtile points at an array of these).
 struct QTile {

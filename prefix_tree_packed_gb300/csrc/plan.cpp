@@ -346,6 +346,8 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   w = align4(w + P.r1.size());
   P.off_r2 = w;
   w = align4(w + P.r2.size());
+  P.off_runs = w;
+  w = align4(w + (size_t)n_kvt * kRunWords);
   P.image.resize(w);
   int32_t *im = P.image.data();
   std::fill(im, im + 16, 0);
@@ -385,6 +387,22 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   std::copy(P.slot_tok.begin(), P.slot_tok.end(), im + P.off_slot_tok);
   std::copy(P.r1.begin(), P.r1.end(), im + P.off_r1);
   std::copy(P.r2.begin(), P.r2.end(), im + P.off_r2);
+  // run tables of the key tiles
+  std::fill(im + P.off_runs, im + P.off_runs + (size_t)n_kvt * kRunWords, 0);
+  for (int32_t t = 0; t < n_kvt; ++t) {
+    int32_t *tb = im + P.off_runs + (size_t)t * kRunWords;
+    const int32_t *sd = send + (size_t)t * kTile;
+    int32_t n = 0;
+    for (int32_t c = 0; c < kTile; ++c) {
+      if (c == 0 || sd[c] != sd[c - 1]) {
+        if (n < kMaxRuns) tb[4 + n] = sd[c];
+        ++n;
+      }
+      if (n <= kMaxRuns) tb[20 + 4 * (n - 1) + c / 32] |= (int32_t)(1u << (c % 32));
+    }
+    tb[0] = n;
+    if (n > kMaxRuns) std::fill(tb + 4, tb + kRunWords, 0);  // only the count is meaningful
+  }
   // zero the alignment gaps so the image is fully defined
   auto zero_gap = [&](size_t from, size_t to) { std::fill(im + from, im + to, 0); };
   zero_gap(P.off_pos + P.n_tot, P.off_send);
@@ -394,7 +412,8 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   zero_gap(P.off_chunk + 4 * (size_t)P.n_chunks, P.off_slot_tok);
   zero_gap(P.off_slot_tok + P.slot_tok.size(), P.off_r1);
   zero_gap(P.off_r1 + P.r1.size(), P.off_r2);
-  zero_gap(P.off_r2 + P.r2.size(), w);
+  zero_gap(P.off_r2 + P.r2.size(), P.off_runs);
+  zero_gap(P.off_runs + (size_t)n_kvt * kRunWords, w);
   return TREE_OK;
 }
 
@@ -468,6 +487,7 @@ int tree_plan_query(const tree_plan_t *plan, tree_plan_info_t *info) {
   info->off_slot_tok = P.off_slot_tok * 4;
   info->off_r1 = P.off_r1 * 4;
   info->off_r2 = P.off_r2 * 4;
+  info->off_runs = P.off_runs * 4;
   return TREE_OK;
 }
 
@@ -499,6 +519,7 @@ int tree_plan_tables(const tree_plan_t *plan, tree_plan_host_view_t *v) {
   v->blk_slot = P.blk_slot.data();
   v->pos = P.image.data() + P.off_pos;
   v->send = P.image.data() + P.off_send;
+  v->runs = P.image.data() + P.off_runs;
   v->chunk_q0 = P.chunk_q0.data();
   v->chunk_q1 = P.chunk_q1.data();
   v->chunk_t0 = P.chunk_t0.data();

@@ -121,6 +121,66 @@ def test_question_errors(lib):
         lib.Plan([-1, 0, 0], [4, 2, 2], leaf1=[1], leaf2=[7])
 
 
+def _check_runs(runs, send, rng):
+    """Run tables against maximal runs of equal send recomputed from the oracle's send."""
+    n_kvt = runs.shape[0]
+    for t in range(n_kvt):
+        sd = send[128 * t: 128 * t + 128]
+        starts = [0] + [c for c in range(1, 128) if sd[c] != sd[c - 1]]
+        n = int(runs[t, 0])
+        assert n == len(starts)
+        if n > 16:
+            assert not runs[t, 1:].any()
+            continue
+        assert not runs[t, 1:4].any()
+        masks = []
+        for r, a in enumerate(starts):
+            b = starts[r + 1] if r + 1 < n else 128
+            assert runs[t, 4 + r] == sd[a]
+            bits = runs[t, 20 + 4 * r: 24 + 4 * r].astype(np.uint32)
+            m = np.array([(int(bits[c // 32]) >> (c % 32)) & 1 for c in range(128)], bool)
+            assert np.array_equal(m, (np.arange(128) >= a) & (np.arange(128) < b))
+            masks.append(m)
+        assert not runs[t, 4 + n: 20].any() and not runs[t, 20 + 4 * n:].any()
+        # what the kernel relies on: OR of the runs that end after a query = the key-by-key test
+        for i in rng.integers(0, int(sd.max()) + 2, 8):
+            vis = np.zeros(128, bool)
+            for r in range(n):
+                if i < runs[t, 4 + r]:
+                    vis |= masks[r]
+            assert np.array_equal(vis, i < sd)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_run_tables_workloads(lib, n):
+    w = synth.workload(n)
+    kw = dict(leaf1=w.leaf1, leaf2=w.leaf2) if w.leaf1 is not None else {}
+    plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, **kw)
+    ref, _ = oplan.plan_forest(w.forest, max_fwd=w.max_fwd, **kw)
+    send = np.zeros(plan.tables()["runs"].shape[0] * 128, np.int64)
+    rs = np.asarray(ref.send)[: len(send)]  # the oracle's send (0 past n_tot)
+    send[: len(rs)] = rs
+    _check_runs(plan.tables()["runs"], send, np.random.default_rng(n))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_run_tables_random_forests(lib, seed):
+    rng = np.random.default_rng(700 + seed)
+    # tiny blocks give tiles of more than 16 runs, larger ones fewer
+    f = synth.random_forest(rng, n_roots=int(rng.integers(1, 4)), max_blocks=int(rng.integers(10, 90)),
+                            max_len=[3, 6, 40][seed % 3], resident_root=bool(seed % 2))
+    try:
+        ref, _ = oplan.plan_forest(f, max_fwd=8192)
+    except oplan.PlanError:
+        pytest.skip("forest has no forward tokens")
+    plan = lib.Plan.from_forest(f, max_fwd=8192)
+    runs = plan.tables()["runs"]
+    send = np.zeros(runs.shape[0] * 128, np.int64)
+    rs = np.asarray(ref.send)[: len(send)]
+    send[: len(rs)] = rs
+    _check_runs(runs, send, rng)
+
+
 def test_upload_argument_checks(lib):
     # every check runs before any CUDA call, so no device is needed
     plan = lib.Plan([-1, 0, 0], [130, 7, 9])
