@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(256) readout_kernel(const float *__restrict__ 
                                                       float *__restrict__ p_avg,
                                                       int32_t *__restrict__ choice,
                                                       int32_t *__restrict__ status) {
-  sm103::griddep_wait();  // the logits may come from the kernel before this one in the stream
+  sm103::griddep_wait();    // the logits may come from the kernel before this one in the stream
+  sm103::griddep_launch();  // the next kernel may launch (it waits for this one if it reads its results)
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const int q = gtid / G;
   const int lane = gtid % G;
@@ -227,7 +228,8 @@ __global__ void __launch_bounds__(kTileWarps * 32) readout_tile_kernel(
     float *__restrict__ p_cal, float *__restrict__ p_avg, int32_t *__restrict__ choice,
     int32_t *__restrict__ status) {
   extern __shared__ float tile_smem[];
-  sm103::griddep_wait();  // the logits may come from the kernel before this one in the stream
+  sm103::griddep_wait();    // the logits may come from the kernel before this one in the stream
+  sm103::griddep_launch();  // the next kernel may launch (it waits for this one if it reads its results)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t q0 = ((int64_t)blockIdx.x * kTileWarps + warp) * 32;
   if (q0 >= nq) return;  // whole warps leave together
