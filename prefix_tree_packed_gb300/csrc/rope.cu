@@ -43,7 +43,10 @@ __global__ void __launch_bounds__(kRopeMaxThreads) rope_kernel(__half *__restric
                                                             const int32_t *__restrict__ pos, int32_t q0,
                                                             int32_t nrows, int hq, int hkv, int d,
                                                             const float *__restrict__ cos_sin, int32_t max_pos) {
-  // the attention that follows in the stream may start launching (it waits for this grid before reading)
+  // launched to overlap the kernel before it in the stream: wait for it before
+  // reading the positions or the rows (it may write them), then let the next
+  // kernel launch (it waits for this grid before reading)
+  griddep_wait();
   griddep_launch();
   const int per_head = d / 16;
   const int item = blockIdx.y * blockDim.x + threadIdx.x;
@@ -118,7 +121,9 @@ extern "C" TREE_API int tree_rope(const tree_plan_t *plan, const void *plan_dev,
   const int threads = std::min(kRopeMaxThreads, (items + 31) / 32 * 32);
   const dim3 grid((unsigned)((n + kRopeRows - 1) / kRopeRows), (unsigned)((items + threads - 1) / threads));
   const int32_t *pos = reinterpret_cast<const int32_t *>(plan_dev) + P.off_pos;
-  rope_kernel<<<grid, threads, 0, as_stream(stream)>>>(reinterpret_cast<__half *>(q), reinterpret_cast<__half *>(k),
-                                                            pos, q0, n, hq, hkv, d, cos_sin, max_pos);
+  const cudaError_t e = launch_dependent(rope_kernel, grid, dim3(threads), 0, as_stream(stream),
+                                         reinterpret_cast<__half *>(q), reinterpret_cast<__half *>(k), pos, q0, n, hq,
+                                         hkv, d, cos_sin, max_pos);
+  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_rope: launch failed: %s", cudaGetErrorString(e));
   return launch_status("tree_rope");
 }

@@ -10,8 +10,7 @@
 // host link) into one of two device image buffers, then tree_rope and
 // tree_attn_fwd for every chunk, then readout_decide.  Everything is one chain
 // of kernels on one stream, each launched to overlap its predecessor's tail and
-// waiting for it (griddepcontrol) before reading its results (tree_rope, which
-// rewrites Q and K in place, is launched in plain stream order); there is no copy
+// waiting for it (griddepcontrol) before reading its results; there is no copy
 // engine and no second stream in the step.  The two buffers alternate between
 // steps: a staging buffer is rewritten only after the copy kernel that read it
 // two steps earlier has run (an event, normally long passed), and a device
@@ -39,10 +38,11 @@ namespace tree {
 namespace {
 
 // Copies the plan image from page-locked staging into a device buffer.  It does
-// not wait for the kernel before it (the previous step's readout): the buffer it
-// writes was last read by the step before that, which has completed, because
-// every step's RoPE is launched in plain stream order (it starts only after all
-// earlier work on the stream); so the copy overlaps the previous readout.
+// not wait for the kernel before it (the previous step's readout): it starts
+// only once that readout has passed its own wait for the previous step's
+// attention, and the buffer it writes was last read by the step before, which
+// had completed before the previous step's RoPE passed its wait.  So the copy,
+// and then this step's RoPE (which waits for the copy), overlap the readout.
 __global__ void __launch_bounds__(256) fetch_image(const int4 *__restrict__ src, int4 *__restrict__ dst, int n16) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x) dst[i] = src[i];
 }
