@@ -266,6 +266,10 @@ typedef struct {
                           {0, 0} (the last CTA resets it), so calls on one stream can reuse it;
                           calls that may overlap on the GPU need separate counters.  NULL: each CTA
                           takes a fixed round-robin share of the items (no scratch memory). */
+  int32_t self_test;   /* 0 normally.  Nonzero: a self-test of the device-side failure detection;
+                          before issuing any copy or MMA each CTA waits on a barrier that nothing
+                          arrives on, gives up after 2 ms, writes TREE_ERR_TIMEOUT to `status`, and
+                          winds down; no output is written.  The context stays usable. */
 } tree_attn_params_t;
 
 /*

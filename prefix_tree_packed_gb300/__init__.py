@@ -89,7 +89,7 @@ class _View(C.Structure):
 
 class AttnParams(C.Structure):
     _fields_ = [("hq", C.c_int32), ("hkv", C.c_int32), ("d", C.c_int32), ("scale", C.c_float),
-                ("work", C.c_void_p)]
+                ("work", C.c_void_p), ("self_test", C.c_int32)]
 
 
 class _StepArgs(C.Structure):
@@ -322,8 +322,9 @@ def tree_rope(plan: Plan, plan_dev, chunk: int, q, k, hq: int, hkv: int, d: int,
 
 
 def tree_attn_fwd(plan: Plan, plan_dev, chunk: int, q, k, v, o, lse, hq: int, hkv: int, d: int,
-                  scale: float = 0.0, status=None, stream=None, work=None):
-    p = AttnParams(hq, hkv, d, scale, _ptr(work))
+                  scale: float = 0.0, status=None, stream=None, work=None, self_test: bool = False):
+    """self_test=True: exercise the device-side timeout (status gets TREE_ERR_TIMEOUT, no output)."""
+    p = AttnParams(hq, hkv, d, scale, _ptr(work), 1 if self_test else 0)
     _check(_lib.tree_attn_fwd(plan.handle, _ptr(plan_dev), chunk, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                               _ptr(lse), C.byref(p), _ptr(status), _stream(stream)))
 

@@ -57,6 +57,7 @@ constexpr int BN = 128;                    // keys per tile (queries per tile: 1
 constexpr uint32_t BOX_BYTES = 128 * 128;  // one 128-row x 64-column f16 box (128-byte rows)
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 500000000ull;
+constexpr uint64_t kSelfTestNs = 2000000ull;
 
 struct AttnArgs {
   const int32_t *send;
@@ -71,6 +72,7 @@ struct AttnArgs {
   int32_t n_items;  // query tiles of the chunk x kv heads x q-head groups
   int32_t *work;    // {next item, finished CTAs} or nullptr for the round-robin schedule
   float scale_log2;
+  int32_t self_test;  // the timeout self-test (see tree_attn_params_t)
 };
 
 template <int D, int NH>
@@ -119,6 +121,7 @@ struct Bars {
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
   uint64_t ostage_full[2], ostage_free[2];  // output staging box of each head
   uint64_t turn[2][4];  // per lane quarter: head h's warp has finished the arithmetic of its tile
+  uint64_t never;  // a barrier nothing arrives on (timeout self-test)
   uint32_t tmem;
   int32_t abort;
 };
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       mbar_init(b_osf(h), 1);
       for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bars.turn[h][q]), 1);
     }
+    mbar_init(smem_u32(&bars.never), 1);
     bars.abort = 0;
     mbar_fence_init();
   }
@@ -271,6 +275,13 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       griddep_wait();
       int t = 0, j = 0, fetched = 0;
       bool ok = true;
+      if (a.self_test) {
+        // timeout self-test: before any copy or MMA is issued, wait 2 ms on a
+        // barrier nothing arrives on; the wait gives up, writes TREE_ERR_TIMEOUT
+        // and raises the CTA's abort flag, and every role winds down
+        ok = wait_bar(smem_u32(&bars.never), 0, abort, a.status, true, kSelfTestNs);
+        ok = __all_sync(0xffffffffu, ok);
+      }
       while (ok) {
         // claim the next item and publish it in the ring (a value >= n_items ends the list)
         const int slot = fetched % kRing;
@@ -761,7 +772,8 @@ int make_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows) {
 
 template <int D, int NH>
 int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const void *k, const void *v, void *o,
-              float *lse, int hq, int hkv, float scale, int32_t *work, int32_t *status, cudaStream_t s) {
+              float *lse, int hq, int hkv, float scale, int32_t *work, int32_t self_test, int32_t *status,
+              cudaStream_t s) {
   using C = Cfg<D, NH>;
   static bool attr_set = false;
   auto kern = tree_attn_tc<D, NH>;
@@ -792,6 +804,7 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
   a.hkv = hkv;
   a.ratio = hq / hkv;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.self_test = self_test;
   const int tiles = P.chunk_t1[chunk] - P.chunk_t0[chunk];
   a.n_items = tiles * hkv * (a.ratio / NH);
   a.work = work;
@@ -826,10 +839,10 @@ extern "C" TREE_API int tree_attn_fwd(const tree_plan_t *plan, const void *plan_
   const cudaStream_t s = as_stream(stream);
   const bool pair = (hq / hkv) % 2 == 0;
   if (d == 64)
-    return pair ? launch_tc<64, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s)
-                : launch_tc<64, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s);
-  return pair ? launch_tc<128, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s)
-              : launch_tc<128, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, status, s);
+    return pair ? launch_tc<64, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, params->self_test, status, s)
+                : launch_tc<64, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, params->self_test, status, s);
+  return pair ? launch_tc<128, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, params->self_test, status, s)
+              : launch_tc<128, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, params->self_test, status, s);
 }
 
 // ---------------------------------------------------------------------------

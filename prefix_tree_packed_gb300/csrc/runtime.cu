@@ -139,7 +139,7 @@ extern "C" TREE_API int tree_runtime_step(tree_runtime_t *rt, const tree_step_ar
     float *lc = a->lse ? a->lse + (size_t)(q0 - P.n_res) * a->hq : nullptr;
     rc = tree_rope(plan, img, c, qc, a->k, a->hq, a->hkv, a->d, a->cos_sin, a->max_pos, a->status, stream);
     if (rc != TREE_OK) return rc;
-    tree_attn_params_t ap = {a->hq, a->hkv, a->d, a->scale, rt->work + 2 * c};
+    tree_attn_params_t ap = {a->hq, a->hkv, a->d, a->scale, rt->work + 2 * c, 0};
     if (c == 0 && a->attn_events[0] &&
         (e = cudaEventRecord(static_cast<cudaEvent_t>(a->attn_events[0]), s)) != cudaSuccess)
       return fail(TREE_ERR_CUDA, "tree_runtime_step: %s", cudaGetErrorString(e));

@@ -313,6 +313,35 @@ def test_attention_chunked_equals_unchunked(lib):
     assert np.abs(a - b).max() <= 2 * ATOL_O
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 64), (8, 2, 128), (3, 3, 64)])
+def test_attention_timeout_self_test_reports_and_recovers(lib, hq, hkv, d):
+    """A wait that runs out (on a barrier nothing arrives on) is reported in the
+    status word, writes no output, and leaves the context usable."""
+    w = synth.workload(2)
+    r = Run(lib, w.forest)
+    p = r.oplan
+    q, k, v = synth.draw_qkv(p.n_fwd, p.n_tot, hq, hkv, d, 31)
+    qr, kr = orope.apply_plan(p, q, k, w.theta)
+    qd, kd, vd = _dev(qr), _dev(kr), _dev(v)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    work = torch.zeros(2, dtype=torch.int32, device="cuda")
+    o = torch.full((p.n_fwd, hq, d), 7.0, dtype=torch.float16, device="cuda")
+    lib.tree_attn_fwd(r.plan, r.dev, 0, qd, kd, vd, o, None, hq, hkv, d, status=st,
+                      stream=torch.cuda.current_stream(), work=work, self_test=True)
+    torch.cuda.synchronize()
+    assert int(st.item()) == lib.TREE_ERR_TIMEOUT
+    assert bool((o == 7.0).all())                     # nothing written
+    assert work.cpu().tolist() == [0, 0]              # the counter is handed back all the same
+    st.zero_()
+    got = r.attn(qd, kd, vd, hq, hkv, d, 0, status=st, work=work)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rng = np.random.default_rng(5)
+    rows = rng.choice(p.n_fwd, 48, replace=False)
+    ref = oatt.attend_rows(p, qr, kr, v, rows)
+    assert np.abs(got.float().cpu().numpy()[rows] - ref).max() <= ATOL_O
+
+
 def test_attention_rejects_bad_shapes(lib):
     w = synth.workload(1)
     r = Run(lib, w.forest)
