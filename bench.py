@@ -515,12 +515,12 @@ def _threads():
     return os.cpu_count()
 
 
-def cpu_baseline(w, budget_s=20.0):
+def cpu_baseline(w, budget_s=15.0):
     t = time.perf_counter()
     n = _oracle_step(w)
     dt = time.perf_counter() - t
     reps = 1
-    while time.perf_counter() - t + dt < budget_s and reps < 3:
+    while time.perf_counter() - t + dt < budget_s and reps < 20:
         n += _oracle_step(w)
         reps += 1
     dt = time.perf_counter() - t
@@ -562,12 +562,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--only", choices=["attn", "rope", "readout"], default=None)
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets for --only (0: default)")
     ap.add_argument("--questions", type=int, default=65536, help="questions for --only readout")
