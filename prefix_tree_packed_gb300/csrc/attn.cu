@@ -619,7 +619,9 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           const int R = tb[0];
           uint32_t mw0 = 0u, mw1 = 0u, mw2 = 0u, mw3 = 0u;
           if (R <= kMaxRuns) {
-            for (int rr = 0; rr < R; ++rr) {
+#pragma unroll
+            for (int rr = 0; rr < kMaxRuns; ++rr) {
+              if (rr >= R) break;
               const bool vis = iq < tb[4 + rr];
               const uint4 b = reinterpret_cast<const uint4 *>(tb + 20)[rr];
               mw0 |= vis ? b.x : 0u;
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           }
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (!((mw[c >> 5] >> (c & 31)) & 1u)) s[c] = __float_as_uint(-INFINITY);
+            s[c] = (mw[c >> 5] & (1u << (c & 31))) ? s[c] : __float_as_uint(-INFINITY);
         }
         // row maximum: three-input max over four independent chains
         float mx4[4];
