@@ -36,6 +36,9 @@ EXPORTS = (
     "tree_rope",
     "tree_attn_fwd", "tree_attn_fwd_noalloc", "readout_decide", "tree_runtime_create", "tree_runtime_destroy",
     "tree_runtime_step",
+    # include/tree_queue.h
+    "tree_queue_default_opts", "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel",
+    "tree_queue_info", "tree_queue_pop", "tree_batch_view", "tree_batch_free",
 )
 
 
@@ -56,6 +59,31 @@ class _Spec(C.Structure):
     _fields_ = [("n_blocks", C.c_int32), ("parent", _i32p), ("length", _i32p),
                 ("key", C.POINTER(C.c_uint64)), ("resident", C.POINTER(C.c_uint8)),
                 ("n_questions", C.c_int32), ("leaf1", _i32p), ("leaf2", _i32p)]
+
+
+class _Block(C.Structure):
+    _fields_ = [("key", C.c_uint64), ("length", C.c_int32)]
+
+
+class _Request(C.Structure):
+    _fields_ = [("id", C.c_int64), ("arrival_ms", C.c_double), ("n_prompts", C.c_int32),
+                ("prompt_blocks", _i32p), ("blocks", C.POINTER(_Block)), ("n_questions", C.c_int32),
+                ("q_prompt1", _i32p), ("q_prompt2", _i32p)]
+
+
+class QueueOpts(C.Structure):
+    _fields_ = [("max_batch_tokens", C.c_int32), ("long_tokens", C.c_int32), ("fifo", C.c_int32),
+                ("ms_per_token", C.c_double), ("max_depth", C.c_int32), ("max_row", C.c_int32),
+                ("n_resident", C.c_int32), ("resident_keys", C.POINTER(C.c_uint64))]
+
+
+class _QueueInfo(C.Structure):
+    _fields_ = [("n_short", C.c_int32), ("n_long", C.c_int32)]
+
+
+class _BatchView(C.Structure):
+    _fields_ = [("lane", C.c_int32), ("n_requests", C.c_int32), ("request_ids", C.POINTER(C.c_int64)),
+                ("request_q0", _i32p), ("cost", C.c_int64), ("spec", _Spec)]
 
 
 class _Opts(C.Structure):
@@ -122,7 +150,18 @@ _lib.readout_decide.argtypes = [_vp, C.c_int32, _vp, _vp, _vp, _vp, C.c_int32, _
 _lib.tree_runtime_create.argtypes = [C.c_size_t, C.c_int32, C.POINTER(_vp)]
 _lib.tree_runtime_destroy.argtypes = [_vp]
 _lib.tree_runtime_step.argtypes = [_vp, C.POINTER(_StepArgs), C.POINTER(PlanInfo), _vp]
-for _f in ("tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step"):
+_lib.tree_queue_default_opts.argtypes = [C.POINTER(QueueOpts)]
+_lib.tree_queue_create.argtypes = [C.POINTER(QueueOpts), C.POINTER(_vp)]
+_lib.tree_queue_destroy.argtypes = [_vp]
+_lib.tree_queue_push.argtypes = [_vp, C.POINTER(_Request), C.POINTER(C.c_int64)]
+_lib.tree_queue_cancel.argtypes = [_vp, C.c_int64]
+_lib.tree_queue_info.argtypes = [_vp, C.POINTER(_QueueInfo)]
+_lib.tree_queue_pop.argtypes = [_vp, C.c_double, C.POINTER(_vp)]
+_lib.tree_batch_view.argtypes = [_vp, C.POINTER(_BatchView)]
+_lib.tree_batch_free.argtypes = [_vp]
+for _f in ("tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
+           "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel", "tree_queue_info",
+           "tree_queue_pop", "tree_batch_view", "tree_batch_free"):
     getattr(_lib, _f).restype = C.c_int
 for _f in ("tree_pack_plan", "tree_plan_free", "tree_plan_query", "tree_plan_chunk", "tree_plan_tables",
            "tree_plan_upload", "tree_plan_upload_staged", "tree_rope_table", "tree_rope", "tree_attn_fwd", "tree_attn_fwd_noalloc",
@@ -188,6 +227,92 @@ class Spec:
     @classmethod
     def from_forest(cls, forest, **kw):
         return cls(forest.parent, forest.length, forest.key, forest.resident, **kw)
+
+
+def queue_default_opts() -> QueueOpts:
+    o = QueueOpts()
+    _check(_lib.tree_queue_default_opts(C.byref(o)))
+    return o
+
+
+class Batch:
+    """One batch taken from a ``Queue``: its requests and its forest (``spec``), copied out."""
+
+    def __init__(self, view: _BatchView):
+        n = view.n_requests
+        nb = view.spec.n_blocks
+        nq = view.spec.n_questions
+        self.lane = int(view.lane)
+        self.cost = int(view.cost)
+        self.request_ids = [int(view.request_ids[i]) for i in range(n)]
+        self.request_q0 = np.array([view.request_q0[i] for i in range(n + 1)], np.int32)
+        self.parent = np.array([view.spec.parent[i] for i in range(nb)], np.int32)
+        self.length = np.array([view.spec.length[i] for i in range(nb)], np.int32)
+        self.key = np.array([view.spec.key[i] for i in range(nb)], np.uint64)
+        self.resident = np.array([view.spec.resident[i] for i in range(nb)], np.uint8)
+        self.leaf1 = np.array([view.spec.leaf1[i] for i in range(nq)], np.int32)
+        self.leaf2 = np.array([view.spec.leaf2[i] for i in range(nq)], np.int32)
+
+    def spec(self, **kw) -> "Spec":
+        return Spec(self.parent, self.length, self.key, self.resident, self.leaf1, self.leaf2, **kw)
+
+
+class Queue:
+    """``tree_queue``: HRRN / FIFO request queue with a long-request lane, batches as prefix-tree forests."""
+
+    def __init__(self, opts: QueueOpts | None = None, resident_keys=()):
+        o = queue_default_opts() if opts is None else opts
+        keys = np.ascontiguousarray(list(resident_keys), np.uint64)
+        o.n_resident = keys.shape[0]
+        o.resident_keys = keys.ctypes.data_as(C.POINTER(C.c_uint64)) if keys.shape[0] else None
+        self._q = _vp()
+        _check(_lib.tree_queue_create(C.byref(o), C.byref(self._q)))
+
+    def close(self):
+        if self._q:
+            _lib.tree_queue_destroy(self._q)
+            self._q = _vp()
+
+    def __del__(self):
+        self.close()
+
+    def push(self, rid: int, arrival_ms: float, prompts, questions=()) -> int:
+        """prompts: list of [(key, length), ...] root first; questions: [(prompt1, prompt2), ...]. Returns the cost."""
+        counts = np.array([len(p) for p in prompts], np.int32)
+        blocks = (_Block * max(int(counts.sum()), 1))()
+        i = 0
+        for p in prompts:
+            for key, length in p:
+                blocks[i].key = int(key)
+                blocks[i].length = int(length)
+                i += 1
+        q1 = np.array([a for a, _ in questions], np.int32)
+        q2 = np.array([b for _, b in questions], np.int32)
+        r = _Request(int(rid), float(arrival_ms), counts.shape[0], counts.ctypes.data_as(_i32p), blocks,
+                     q1.shape[0], q1.ctypes.data_as(_i32p), q2.ctypes.data_as(_i32p))
+        cost = C.c_int64()
+        _check(_lib.tree_queue_push(self._q, C.byref(r), C.byref(cost)))
+        return int(cost.value)
+
+    def cancel(self, rid: int):
+        _check(_lib.tree_queue_cancel(self._q, int(rid)))
+
+    def info(self) -> tuple[int, int]:
+        i = _QueueInfo()
+        _check(_lib.tree_queue_info(self._q, C.byref(i)))
+        return int(i.n_short), int(i.n_long)
+
+    def pop(self, now_ms: float) -> Batch | None:
+        b = _vp()
+        _check(_lib.tree_queue_pop(self._q, float(now_ms), C.byref(b)))
+        if not b:
+            return None
+        try:
+            v = _BatchView()
+            _check(_lib.tree_batch_view(b, C.byref(v)))
+            return Batch(v)
+        finally:
+            _lib.tree_batch_free(b)
 
 
 class Runtime:

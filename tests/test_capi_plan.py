@@ -19,9 +19,11 @@ def lib():
 
 
 def test_exports_every_declared_symbol(lib):
-    with open(os.path.join(ROOT, "include", "tree_attn.h")) as f:
-        hdr = f.read()
-    declared = set(re.findall(r"^TREE_API\s+[\w\s\*]*?\*?\s*(\w+)\s*\(", hdr, flags=re.M))
+    declared = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            with open(os.path.join(ROOT, "include", h)) as f:
+                declared |= set(re.findall(r"^TREE_API\s+[\w\s\*]*?\*?\s*(\w+)\s*\(", f.read(), flags=re.M))
     assert declared == set(lib.EXPORTS)
     for name in declared:
         getattr(lib._lib, name)          # raises if the shared object lacks it
