@@ -1,0 +1,64 @@
+/*
+ * tree_layer.h -- the Llama layer around the tree attention (GB300, sm_103a):
+ * the projections as tensor-core GEMMs with fused epilogues, and RMSNorm.
+ *
+ * The basal-rs Architecture page ("01 / Request path: GPU forward pass") runs
+ * the Llama model in f16 over the batch as one compact token list, without
+ * padding.  A layer over the packed tokens of a batch is
+ *
+ *     xn = rmsnorm(x, w_in)                      tree_rmsnorm
+ *     q, k, v = xn Wq^T, xn Wk^T, xn Wv^T        tree_gemm STORE (k, v into the cache rows)
+ *     q, k rotated at tree positions             tree_rope           (tree_attn.h)
+ *     o = attention over tree blocks             tree_attn_fwd       (tree_attn.h)
+ *     h = x + o Wo^T                             tree_gemm RESIDUAL
+ *     hn = rmsnorm(h, w_post)                    tree_rmsnorm
+ *     g = silu(hn Wg^T) * (hn Wu^T)              tree_gemm SWIGLU
+ *     y = h + g Wd^T                             tree_gemm RESIDUAL
+ *
+ * Conventions as in tree_attn.h: status codes, caller-owned device memory,
+ * work enqueued on the caller's stream (launched so that it may overlap the
+ * tail of the kernel before it; it waits for that kernel before reading).
+ * f16 tensors are row-major, densely packed, 16-byte aligned.
+ */
+#ifndef TREE_LAYER_H
+#define TREE_LAYER_H
+
+#include "tree_attn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum tree_gemm_epilogue {
+  TREE_GEMM_STORE = 0,    /* C = A B^T */
+  TREE_GEMM_RESIDUAL = 1, /* C = A B^T + R   (R [m, n], may be C itself) */
+  TREE_GEMM_SWIGLU = 2    /* C = silu(A G^T) * (A U^T), B = [G; U] with 2n rows, silu(g) = g / (1 + e^-g) */
+};
+
+/*
+ * C[m, n] = epilogue(A B^T): A f16 [m, k] (an activation), B f16 [n, k] (a
+ * Linear weight, [2n, k] for SWIGLU), f32 accumulation over the whole of k in
+ * one fixed order (no split over k), the epilogue in f32, C f16 [m, n].
+ * n and k multiples of 8; m >= 0 (0: nothing to do).  `status` (device int32,
+ * may be NULL) receives TREE_ERR_TIMEOUT if a bounded device wait gives up.
+ * Errors: TREE_ERR_INVALID_ARG (NULL, sizes, unknown epilogue, RESIDUAL without
+ * R), TREE_ERR_UNSUPPORTED (n or k not a multiple of 8, misaligned pointer),
+ * TREE_ERR_CUDA.
+ */
+TREE_API int tree_gemm(const void *a, const void *b, void *c, const void *r, int32_t m, int32_t n, int32_t k,
+                       int32_t epi, int32_t *status, tree_stream_t stream);
+
+/*
+ * y[i, :] = f16( f16(x[i, :] / sqrt(mean_j x[i, j]^2 + eps)) * w ), the Llama
+ * RMSNorm with its f32 statistics: the normalised row is rounded to f16 before
+ * the f16 weight multiplies it.  x, y f16 [rows, cols] (y may be x), w f16
+ * [cols]; cols a multiple of 8 and at most 16384.
+ */
+TREE_API int tree_rmsnorm(const void *x, const void *w, void *y, int32_t rows, int32_t cols, float eps,
+                          tree_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREE_LAYER_H */

@@ -39,7 +39,13 @@ EXPORTS = (
     # include/tree_queue.h
     "tree_queue_default_opts", "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel",
     "tree_queue_info", "tree_queue_pop", "tree_batch_view", "tree_batch_free",
+    # include/tree_layer.h
+    "tree_gemm", "tree_rmsnorm",
 )
+
+GEMM_STORE = 0
+GEMM_RESIDUAL = 1
+GEMM_SWIGLU = 2
 
 
 class TreeError(RuntimeError):
@@ -150,6 +156,8 @@ _lib.readout_decide.argtypes = [_vp, C.c_int32, _vp, _vp, _vp, _vp, C.c_int32, _
 _lib.tree_runtime_create.argtypes = [C.c_size_t, C.c_int32, C.POINTER(_vp)]
 _lib.tree_runtime_destroy.argtypes = [_vp]
 _lib.tree_runtime_step.argtypes = [_vp, C.POINTER(_StepArgs), C.POINTER(PlanInfo), _vp]
+_lib.tree_gemm.argtypes = [_vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
+_lib.tree_rmsnorm.argtypes = [_vp, _vp, _vp, C.c_int32, C.c_int32, C.c_float, _vp]
 _lib.tree_queue_default_opts.argtypes = [C.POINTER(QueueOpts)]
 _lib.tree_queue_create.argtypes = [C.POINTER(QueueOpts), C.POINTER(_vp)]
 _lib.tree_queue_destroy.argtypes = [_vp]
@@ -159,7 +167,7 @@ _lib.tree_queue_info.argtypes = [_vp, C.POINTER(_QueueInfo)]
 _lib.tree_queue_pop.argtypes = [_vp, C.c_double, C.POINTER(_vp)]
 _lib.tree_batch_view.argtypes = [_vp, C.POINTER(_BatchView)]
 _lib.tree_batch_free.argtypes = [_vp]
-for _f in ("tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
+for _f in ("tree_gemm", "tree_rmsnorm", "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
            "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel", "tree_queue_info",
            "tree_queue_pop", "tree_batch_view", "tree_batch_free"):
     getattr(_lib, _f).restype = C.c_int
@@ -227,6 +235,16 @@ class Spec:
     @classmethod
     def from_forest(cls, forest, **kw):
         return cls(forest.parent, forest.length, forest.key, forest.resident, **kw)
+
+
+def gemm(a, b, c, m: int, n: int, k: int, epi: int = GEMM_STORE, r=None, status=None, stream=None):
+    """tree_gemm: C[m, n] = epilogue(A[m, k] B^T), f16 in and out, f32 accumulation."""
+    _check(_lib.tree_gemm(_ptr(a), _ptr(b), _ptr(c), _ptr(r), m, n, k, epi, _ptr(status), _stream(stream)))
+
+
+def rmsnorm(x, w, y, rows: int, cols: int, eps: float = 1e-5, stream=None):
+    """tree_rmsnorm: y = f16(f16(x / sqrt(mean(x^2) + eps)) * w) per row."""
+    _check(_lib.tree_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, cols, eps, _stream(stream)))
 
 
 def queue_default_opts() -> QueueOpts:

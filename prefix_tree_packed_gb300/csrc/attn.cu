@@ -43,8 +43,6 @@
 #include <cmath>
 #include <mutex>
 
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "sm103.cuh"
 
@@ -745,33 +743,6 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2-D map over a [rows, cols] f16 matrix with 128-row x 64-column boxes, 128-byte swizzle.
-int make_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows) {
-  auto enc = encode_fn();
-  if (!enc) return fail(TREE_ERR_CUDA, "tree_attn_fwd: cuTensorMapEncodeTiled unavailable");
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, 128};
-  const cuuint32_t es[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(TREE_ERR_CUDA, "tree_attn_fwd: tensor map encode failed (%d)", (int)r);
-  return TREE_OK;
-}
-
 template <int D, int NH>
 int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const void *k, const void *v, void *o,
               float *lse, int hq, int hkv, float scale, int32_t *work, int32_t self_test, int32_t *status,
@@ -787,8 +758,10 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
   const int32_t q0 = P.chunk_q0[chunk], nq = P.chunk_q1[chunk] - q0;
   CUtensorMap mq, mk, mv, mo;
   int rc;
-  if ((rc = make_map(&mq, q, (int64_t)hq * D, nq)) || (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot)) ||
-      (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot)) || (rc = make_map(&mo, o, (int64_t)hq * D, nq)))
+  if ((rc = make_map(&mq, q, (int64_t)hq * D, nq, "tree_attn_fwd")) ||
+      (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
+      (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
+      (rc = make_map(&mo, o, (int64_t)hq * D, nq, "tree_attn_fwd")))
     return rc;
   AttnArgs a;
   a.send = img + P.off_send;

@@ -1,6 +1,7 @@
 // Helpers shared by the CUDA translation units of the library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -25,6 +26,11 @@ inline cudaStream_t as_stream(tree_stream_t s) { return reinterpret_cast<cudaStr
 
 // Number of SMs of the current device (cached per process; GB300 has 152).
 int sm_count();
+
+// 2-D TMA map over a row-major [rows, cols] f16 matrix: 128-row x 64-column
+// boxes (128-byte rows), 128-byte swizzle, zero fill outside the matrix.
+// `who` names the caller in error messages.
+int make_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, const char *who);
 
 // Launch `kernel` on `s` allowed to start while the stream's previous kernel is
 // still running (programmatic dependent launch): the kernel must execute

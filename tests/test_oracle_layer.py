@@ -1,0 +1,53 @@
+"""Oracle layer pieces pinned to closed forms and to library routines on special cases."""
+import numpy as np
+
+from oracle import layer as ol
+
+
+def test_rmsnorm_closed_forms():
+    # [3, 4]: mean square 12.5, so n = [3, 4] / sqrt(12.5 + eps)
+    x = np.array([[3.0, 4.0]], np.float16)
+    w = np.array([1.0, 2.0], np.float16)
+    y = ol.rmsnorm(x, w, 0.0)
+    n = np.array([3.0, 4.0]) / np.sqrt(12.5)
+    assert y.dtype == np.float16
+    np.testing.assert_array_equal(y[0], (n.astype(np.float16).astype(np.float64) * [1.0, 2.0]).astype(np.float16))
+    # a constant row normalises to its sign; eps shrinks it by sqrt(c^2 / (c^2 + eps))
+    x = np.full((2, 8), [[-0.5], [2.0]], np.float16)
+    w = np.ones(8, np.float16)
+    np.testing.assert_array_equal(ol.rmsnorm(x, w, 0.0), np.sign(x.astype(np.float64)).astype(np.float16))
+    y = ol.rmsnorm(x[1:], w, 1.0).astype(np.float64)
+    np.testing.assert_allclose(y, 2.0 / np.sqrt(4.0 + 1.0), rtol=2 ** -10)
+    # scale invariance (eps = 0): rmsnorm(a x) = rmsnorm(x) for a power of two
+    x = np.random.default_rng(0).standard_normal((4, 64)).astype(np.float16)
+    w = np.random.default_rng(1).standard_normal(64).astype(np.float16)
+    np.testing.assert_array_equal(ol.rmsnorm(x, w, 0.0), ol.rmsnorm((x.astype(np.float64) * 4).astype(np.float16), w, 0.0))
+
+
+def test_gemm_against_integer_matmul():
+    # small integers: every product and sum is exact in f64 and the result exact in f16
+    rng = np.random.default_rng(2)
+    a = rng.integers(-4, 5, (37, 24)).astype(np.float16)
+    b = rng.integers(-4, 5, (19, 24)).astype(np.float16)
+    exact = a.astype(np.int64) @ b.astype(np.int64).T
+    np.testing.assert_array_equal(ol.gemm(a, b).astype(np.int64), exact)
+    r = rng.integers(-8, 9, (37, 19)).astype(np.float16)
+    np.testing.assert_array_equal(ol.gemm(a, b, "residual", r).astype(np.int64), exact + r.astype(np.int64))
+
+
+def test_swiglu_closed_forms():
+    assert ol.silu(0.0) == 0.0
+    np.testing.assert_allclose(ol.silu(40.0), 40.0, rtol=1e-15)
+    x = np.linspace(-6, 6, 13)
+    np.testing.assert_allclose(ol.silu(-x), ol.silu(x) - x, atol=1e-14)   # silu(-x) = silu(x) - x
+    np.testing.assert_allclose(ol.silu(x), x * 0.5 * (1 + np.tanh(x / 2)), atol=1e-14)
+    # swiglu with the up half equal to ones is silu of the gate
+    rng = np.random.default_rng(3)
+    a = rng.integers(-3, 4, (5, 16)).astype(np.float16)
+    g = rng.integers(-2, 3, (4, 16)).astype(np.float16)
+    u_one = np.zeros((4, 16), np.float16)
+    u_one[:, 0] = 1
+    a1 = a.copy()
+    a1[:, 0] = 1
+    got = ol.gemm(a1, np.concatenate([g, u_one]), "swiglu")
+    np.testing.assert_array_equal(got, ol.silu(a1.astype(np.float64) @ g.astype(np.float64).T).astype(np.float16))
