@@ -57,6 +57,44 @@ TREE_API int tree_gemm(const void *a, const void *b, void *c, const void *r, int
 TREE_API int tree_rmsnorm(const void *x, const void *w, void *y, int32_t rows, int32_t cols, float eps,
                           tree_stream_t stream);
 
+/* The weights of one Llama layer (device f16, row-major, 16-byte aligned). */
+typedef struct {
+  int32_t hidden, hq, hkv, d, ffn; /* model width, query / kv heads, head dim (64 or 128), MLP width */
+  float eps;                       /* RMSNorm epsilon (Llama: 1e-5) */
+  const void *w_in;                /* [hidden]            RMSNorm before attention */
+  const void *wq;                  /* [hq * d, hidden] */
+  const void *wk, *wv;             /* [hkv * d, hidden] */
+  const void *wo;                  /* [hidden, hq * d] */
+  const void *w_post;              /* [hidden]            RMSNorm before the MLP */
+  const void *wgu;                 /* [2 * ffn, hidden]   gate rows, then up rows */
+  const void *wd;                  /* [hidden, ffn] */
+} tree_layer_weights_t;
+
+/* Bytes of the workspace tree_layer_fwd needs for this plan and these sizes. */
+TREE_API int tree_layer_workspace_bytes(const tree_plan_t *plan, const tree_layer_weights_t *w, size_t *bytes);
+
+/*
+ * One Llama layer over the forward tokens of a planned batch (the sequence at
+ * the top of this header), every chunk of the plan:
+ *
+ *   x        f16 [n_fwd, hidden]   the forward tokens' hidden states, packed order
+ *   k_cache, v_cache f16 [n_tot, hkv * d]  rows [0, n_res) hold the resident
+ *            tokens' post-RoPE keys and their values (read); rows [n_res, n_tot)
+ *            receive this layer's post-RoPE keys and values
+ *   y        f16 [n_fwd, hidden]   the layer's output (may not alias x)
+ *   cos_sin  f32 rotary table (tree_rope_table), max_pos >= info.max_pos
+ *   workspace  device memory of tree_layer_workspace_bytes, 256-byte aligned
+ *   work     device int32 [2 * n_chunks] attention work counters, {0} before the
+ *            first call (each call leaves them 0), or NULL
+ *
+ * All launches go to `stream` in order; nothing is synchronised.  Errors as the
+ * calls it makes, plus TREE_ERR_INVALID_ARG for a short workspace.
+ */
+TREE_API int tree_layer_fwd(const tree_plan_t *plan, const void *plan_dev, const tree_layer_weights_t *w,
+                            const void *x, void *k_cache, void *v_cache, void *y, const float *cos_sin,
+                            int32_t max_pos, void *workspace, size_t workspace_bytes, int32_t *work,
+                            int32_t *status, tree_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

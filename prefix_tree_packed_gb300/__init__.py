@@ -40,7 +40,7 @@ EXPORTS = (
     "tree_queue_default_opts", "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel",
     "tree_queue_info", "tree_queue_pop", "tree_batch_view", "tree_batch_free",
     # include/tree_layer.h
-    "tree_gemm", "tree_rmsnorm",
+    "tree_gemm", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd",
 )
 
 GEMM_STORE = 0
@@ -90,6 +90,12 @@ class _QueueInfo(C.Structure):
 class _BatchView(C.Structure):
     _fields_ = [("lane", C.c_int32), ("n_requests", C.c_int32), ("request_ids", C.POINTER(C.c_int64)),
                 ("request_q0", _i32p), ("cost", C.c_int64), ("spec", _Spec)]
+
+
+class LayerWeights(C.Structure):
+    _fields_ = [("hidden", C.c_int32), ("hq", C.c_int32), ("hkv", C.c_int32), ("d", C.c_int32), ("ffn", C.c_int32),
+                ("eps", C.c_float), ("w_in", C.c_void_p), ("wq", C.c_void_p), ("wk", C.c_void_p), ("wv", C.c_void_p),
+                ("wo", C.c_void_p), ("w_post", C.c_void_p), ("wgu", C.c_void_p), ("wd", C.c_void_p)]
 
 
 class _Opts(C.Structure):
@@ -158,6 +164,9 @@ _lib.tree_runtime_destroy.argtypes = [_vp]
 _lib.tree_runtime_step.argtypes = [_vp, C.POINTER(_StepArgs), C.POINTER(PlanInfo), _vp]
 _lib.tree_gemm.argtypes = [_vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
 _lib.tree_rmsnorm.argtypes = [_vp, _vp, _vp, C.c_int32, C.c_int32, C.c_float, _vp]
+_lib.tree_layer_workspace_bytes.argtypes = [_vp, C.POINTER(LayerWeights), C.POINTER(C.c_size_t)]
+_lib.tree_layer_fwd.argtypes = [_vp, _vp, C.POINTER(LayerWeights), _vp, _vp, _vp, _vp, _vp, C.c_int32, _vp, C.c_size_t,
+                                _vp, _vp, _vp]
 _lib.tree_queue_default_opts.argtypes = [C.POINTER(QueueOpts)]
 _lib.tree_queue_create.argtypes = [C.POINTER(QueueOpts), C.POINTER(_vp)]
 _lib.tree_queue_destroy.argtypes = [_vp]
@@ -167,7 +176,7 @@ _lib.tree_queue_info.argtypes = [_vp, C.POINTER(_QueueInfo)]
 _lib.tree_queue_pop.argtypes = [_vp, C.c_double, C.POINTER(_vp)]
 _lib.tree_batch_view.argtypes = [_vp, C.POINTER(_BatchView)]
 _lib.tree_batch_free.argtypes = [_vp]
-for _f in ("tree_gemm", "tree_rmsnorm", "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
+for _f in ("tree_gemm", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd", "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
            "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel", "tree_queue_info",
            "tree_queue_pop", "tree_batch_view", "tree_batch_free"):
     getattr(_lib, _f).restype = C.c_int
@@ -245,6 +254,26 @@ def gemm(a, b, c, m: int, n: int, k: int, epi: int = GEMM_STORE, r=None, status=
 def rmsnorm(x, w, y, rows: int, cols: int, eps: float = 1e-5, stream=None):
     """tree_rmsnorm: y = f16(f16(x / sqrt(mean(x^2) + eps)) * w) per row."""
     _check(_lib.tree_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, cols, eps, _stream(stream)))
+
+
+def layer_weights(hidden: int, hq: int, hkv: int, d: int, ffn: int, tensors: dict, eps: float = 1e-5) -> LayerWeights:
+    """LayerWeights from device tensors keyed w_in, wq, wk, wv, wo, w_post, wgu, wd (kept alive by the caller)."""
+    return LayerWeights(hidden, hq, hkv, d, ffn, eps, *[_ptr(tensors[k]) for k in
+                                                        ("w_in", "wq", "wk", "wv", "wo", "w_post", "wgu", "wd")])
+
+
+def layer_workspace_bytes(plan: "Plan", w: LayerWeights) -> int:
+    n = C.c_size_t()
+    _check(_lib.tree_layer_workspace_bytes(plan.handle, C.byref(w), C.byref(n)))
+    return int(n.value)
+
+
+def layer_fwd(plan: "Plan", plan_dev, w: LayerWeights, x, k_cache, v_cache, y, cos_sin, max_pos: int, workspace,
+              workspace_bytes: int, work=None, status=None, stream=None):
+    """tree_layer_fwd: one Llama layer over the plan's forward tokens (see include/tree_layer.h)."""
+    _check(_lib.tree_layer_fwd(plan.handle, _ptr(plan_dev), C.byref(w), _ptr(x), _ptr(k_cache), _ptr(v_cache), _ptr(y),
+                               _ptr(cos_sin), max_pos, _ptr(workspace), workspace_bytes, _ptr(work), _ptr(status),
+                               _stream(stream)))
 
 
 def queue_default_opts() -> QueueOpts:

@@ -28,6 +28,7 @@ __all__ = [
     "WORKLOAD_NAMES",
     "draw_qkv",
     "draw_logits",
+    "draw_layer",
     "draw_readout_batch",
     "random_forest",
 ]
@@ -248,6 +249,32 @@ def draw_qkv(n_fwd: int, n_tot: int, hq: int, hkv: int, d: int, seed: int):
     k = rng.standard_normal((n_tot, hkv, d), dtype=np.float32).astype(np.float16)
     v = rng.standard_normal((n_tot, hkv, d), dtype=np.float32).astype(np.float16)
     return q, k, v
+
+
+def draw_layer(n_fwd: int, n_res: int, hidden: int, hq: int, hkv: int, d: int, ffn: int, seed: int):
+    """Random-init weights of one Llama layer and its inputs, all f16.
+
+    Linear weights ~ N(0, 1/fan_in) (rows = outputs), norm weights ~ 1 + N(0, 0.1^2);
+    hidden states of the forward tokens ~ N(0,1); the resident tokens' (already
+    rotated) keys and values ~ N(0,1).  There are no trained weights: the shapes
+    are those of the model, the values random.
+    """
+    rng = np.random.default_rng(seed + 4000)
+
+    def lin(n_out, n_in):
+        return (rng.standard_normal((n_out, n_in), dtype=np.float32) / np.sqrt(n_in)).astype(np.float16)
+
+    w = {
+        "w_in": (1.0 + 0.1 * rng.standard_normal(hidden)).astype(np.float16),
+        "wq": lin(hq * d, hidden), "wk": lin(hkv * d, hidden), "wv": lin(hkv * d, hidden),
+        "wo": lin(hidden, hq * d),
+        "w_post": (1.0 + 0.1 * rng.standard_normal(hidden)).astype(np.float16),
+        "wgu": lin(2 * ffn, hidden), "wd": lin(hidden, ffn),
+    }
+    x = rng.standard_normal((n_fwd, hidden), dtype=np.float32).astype(np.float16)
+    res_k = rng.standard_normal((n_res, hkv * d), dtype=np.float32).astype(np.float16)
+    res_v = rng.standard_normal((n_res, hkv * d), dtype=np.float32).astype(np.float16)
+    return w, x, res_k, res_v
 
 
 def draw_logits(n_slots: int, stride: int, sigma: float, seed: int):
