@@ -253,6 +253,77 @@ def measure_attn(lib, torch, B, stream, reps, warmup):
     return ev[0].elapsed_time(ev[1]) / reps
 
 
+# model width and MLP width of the Llama layer around each workload's attention shape
+LAYER_DIMS = {1: (256, 512), 2: (2048, 8192), 3: (4096, 14336), 4: (4096, 14336), 5: (4096, 14336)}
+
+
+def measure_layer(lib, torch, w, dev, stream, reps, warmup):
+    """tree_layer_fwd over the workload's batch with random-init weights, plus each projection GEMM alone.
+
+    Returns a dict: ms per layer, tokens, FLOPs (projections + visible attention pairs) and per-GEMM figures.
+    """
+    hidden, ffn = LAYER_DIMS[w.number]
+    plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd)
+    i = plan.info
+    n_fwd, n_res = i.n_tot - i.n_res, i.n_res
+    wts, x, rk, rv = synth.draw_layer(n_fwd, n_res, hidden, w.hq, w.hkv, w.d, ffn, w.seed)
+    td = {k: torch.from_numpy(v).to(dev) for k, v in wts.items()}
+    lw = lib.layer_weights(hidden, w.hq, w.hkv, w.d, ffn, td)
+    nbytes = lib.layer_workspace_bytes(plan, lw)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    pdev = torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev)
+    plan.upload(pdev, i.dev_bytes, stream)
+    tab = torch.from_numpy(lib.rope_table(i.max_pos, w.d, w.theta)).to(dev)
+    qd, kvd = w.hq * w.d, w.hkv * w.d
+    tx = torch.from_numpy(x).to(dev)
+    kc = torch.zeros(i.n_tot, kvd, dtype=torch.float16, device=dev)
+    vc = torch.zeros_like(kc)
+    kc[:n_res] = torch.from_numpy(rk).to(dev)
+    vc[:n_res] = torch.from_numpy(rv).to(dev)
+    y = torch.empty_like(tx)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    work = torch.zeros(2 * i.n_chunks, dtype=torch.int32, device=dev)
+
+    def run():
+        lib.layer_fwd(plan, pdev, lw, tx, kc, vc, y, tab, i.max_pos, ws, nbytes, work=work, status=st, stream=stream)
+
+    def timed(fn, n):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        for _ in range(n):
+            fn()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / n
+
+    ms = timed(run, reps)
+    assert int(st.item()) == 0, "device status word set"
+    m = n_fwd
+    gemms = {"qkv": (m, qd + 2 * kvd, hidden), "o": (m, hidden, qd), "gate_up": (m, 2 * ffn, hidden),
+             "down": (m, hidden, ffn)}
+    gemm_flops = sum(2.0 * a * b * c for a, b, c in gemms.values())
+    attn_flops = 4.0 * w.d * w.hq * i.pairs
+    # each projection alone, on the workspace buffers (same shapes and epilogues as in the layer)
+    a_ = torch.randn(m, max(hidden, ffn, qd), device=dev, dtype=torch.float16)
+    out = torch.empty(m, max(hidden, ffn, qd + 2 * kvd), device=dev, dtype=torch.float16)
+    per = {}
+    for name, (mm, n, k) in gemms.items():
+        if name == "gate_up":
+            b_, epi, nn, r = td["wgu"], lib.GEMM_SWIGLU, ffn, None
+        elif name == "qkv":
+            b_, epi, nn, r = torch.cat([td["wq"], td["wk"], td["wv"]]), lib.GEMM_STORE, n, None
+        else:
+            b_, epi, nn, r = (td["wo"] if name == "o" else td["wd"]), lib.GEMM_RESIDUAL, n, out
+        av = a_[:, :k].contiguous()
+        t = timed(lambda: lib.gemm(av, b_, out, mm, nn, k, epi, r=r, status=st, stream=stream), reps)
+        per[name] = dict(m=mm, n=n, k=k, us=round(t * 1e3, 1), tflops=round(2.0 * mm * n * k / t / 1e9, 1))
+    return dict(ms=ms, tokens=n_fwd, hidden=hidden, ffn=ffn, flops=gemm_flops + attn_flops, gemm_flops=gemm_flops,
+                attn_flops=attn_flops, gemms=per)
+
+
 def run_only(args):
     """One kernel by itself on cuda:0: a JSON line with its time and roofline."""
     import torch
@@ -273,7 +344,15 @@ def run_only(args):
         B = Batch(lib, torch, w, dev, n_sets=args.sets or N_SETS)
         B.plan.upload(B.pdev, B.info.dev_bytes, stream)
         line.update(workload=w.name, sets=len(B.sets))
-        if args.only == "rope":
+        if args.only == "layer":
+            r = measure_layer(lib, torch, w, dev, stream, args.steps, args.warmup)
+            tf = r["flops"] / (r["ms"] / 1e3) / 1e12
+            line.update(us_per_layer=round(r["ms"] * 1e3, 1), tokens=r["tokens"],
+                        tokens_per_s=round(r["tokens"] / (r["ms"] / 1e3), 1), hidden=r["hidden"], ffn=r["ffn"],
+                        flops=r["flops"], attn_flops=r["attn_flops"], achieved=round(tf, 1), unit="TFLOP/s",
+                        peak=peaks["tc"], frac=round(tf / peaks["tc"], 4), gemms=r["gemms"],
+                        weights="random init (no trained weights)")
+        elif args.only == "rope":
             ms, nbytes = measure_rope(lib, torch, B, stream, reps=args.steps, warmup=args.warmup,
                                       keys_only=args.keys_only)
             line["keys_only"] = args.keys_only
@@ -568,7 +647,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--only", choices=["attn", "rope", "readout"], default=None)
+    ap.add_argument("--only", choices=["attn", "rope", "readout", "layer"], default=None)
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets for --only (0: default)")
     ap.add_argument("--questions", type=int, default=65536, help="questions for --only readout")
     ap.add_argument("--keys-only", action="store_true", help="--only rope: rotate the keys alone")
