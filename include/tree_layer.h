@@ -32,13 +32,15 @@ extern "C" {
 enum tree_gemm_epilogue {
   TREE_GEMM_STORE = 0,    /* C = A B^T */
   TREE_GEMM_RESIDUAL = 1, /* C = A B^T + R   (R [m, n], may be C itself) */
-  TREE_GEMM_SWIGLU = 2    /* C = silu(A G^T) * (A U^T), B = [G; U] with 2n rows, silu(g) = g / (1 + e^-g) */
+  TREE_GEMM_SWIGLU = 2,   /* C = silu(A G^T) * (A U^T), B = [G; U] with 2n rows, silu(g) = g / (1 + e^-g) */
+  TREE_GEMM_STORE_F32 = 3 /* C = A B^T as f32 (C is float [m, n]) */
 };
 
 /*
  * C[m, n] = epilogue(A B^T): A f16 [m, k] (an activation), B f16 [n, k] (a
  * Linear weight, [2n, k] for SWIGLU), f32 accumulation over the whole of k in
- * one fixed order (no split over k), the epilogue in f32, C f16 [m, n].
+ * one fixed order (no split over k), the epilogue in f32, C f16 [m, n]
+ * (f32 for STORE_F32).
  * n and k multiples of 8; m >= 0 (0: nothing to do).  `status` (device int32,
  * may be NULL) receives TREE_ERR_TIMEOUT if a bounded device wait gives up.
  * Errors: TREE_ERR_INVALID_ARG (NULL, sizes, unknown epilogue, RESIDUAL without
@@ -94,6 +96,32 @@ TREE_API int tree_layer_fwd(const tree_plan_t *plan, const void *plan_dev, const
                             const void *x, void *k_cache, void *v_cache, void *y, const float *cos_sin,
                             int32_t max_pos, void *workspace, size_t workspace_bytes, int32_t *work,
                             int32_t *status, tree_stream_t stream);
+
+/*
+ * The final layer with its pruning ("01 / Request path: GPU forward pass": in
+ * the final layer the MLP block and the logits are computed only for readout
+ * positions and answer letters).  The attention block runs over every forward
+ * token (their keys and values are written as in tree_layer_fwd); then only the
+ * plan's readout slots (the last token of each leaf) continue:
+ *
+ *   h_s = x_s + o_s Wo^T;  y_s = h_s + (silu(hn_s Wg^T) * (hn_s Wu^T)) Wd^T
+ *   logits = rmsnorm(y_s, w_final) W_letters^T       (f32, [n_slots, stride])
+ *
+ *   w_final    f16 [hidden]          the model's final RMSNorm
+ *   w_letters  f16 [stride, hidden]  the LM-head rows of the answer letters, gathered once
+ *                                    by the caller (row l = letter l; unused rows may be 0)
+ *   stride     letters per logits row, a multiple of 8 (the readout_decide stride)
+ *   logits     f32 [n_slots, stride] feeds readout_decide with the plan's r1/r2
+ *
+ * Every readout slot must be a forward token (TREE_ERR_INVALID_ARG otherwise).
+ */
+TREE_API int tree_last_layer_workspace_bytes(const tree_plan_t *plan, const tree_layer_weights_t *w, size_t *bytes);
+
+TREE_API int tree_last_layer_fwd(const tree_plan_t *plan, const void *plan_dev, const tree_layer_weights_t *w,
+                                 const void *x, void *k_cache, void *v_cache, const float *cos_sin, int32_t max_pos,
+                                 const void *w_final, const void *w_letters, int32_t stride, float *logits,
+                                 void *workspace, size_t workspace_bytes, int32_t *work, int32_t *status,
+                                 tree_stream_t stream);
 
 #ifdef __cplusplus
 }

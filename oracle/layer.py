@@ -15,7 +15,12 @@ values it reads and rounded to f16 where the product stores a tensor:
 * gemm:     A B^T in float64, the epilogue (+ R; or silu(g) * u with
             silu(g) = g / (1 + e^-g)) in float64, one rounding to f16;
 * layer:    the sequence in tree_layer.h, with tree RoPE and tree attention
-            taken from ``oracle.rope`` and ``oracle.attention``.
+            taken from ``oracle.rope`` and ``oracle.attention``;
+* last_layer: the final layer computed for every token, then the rows of the
+            readout slots (the last token of each leaf) taken, normalised by the
+            model's final RMSNorm and multiplied by the answer letters' LM-head
+            rows: the page's pruning only skips work whose results are never
+            read, so the full layer restricted to those rows is its definition.
 
 Test infrastructure only (see the package docstring).
 """
@@ -87,3 +92,16 @@ def layer(plan, x16, res_k16, res_v16, weights: dict, hq: int, hkv: int, d: int,
     g = gemm(hn, weights["wgu"], "swiglu")
     y = gemm(g, weights["wd"], "residual", h)
     return y, q, k, v, o16, h
+
+
+def letter_logits(plan, y16, w_final16, w_letters16, eps: float = 1e-5) -> np.ndarray:
+    """float64 [n_slots, stride] logits of the readout slots from the final layer's output rows."""
+    rows = np.asarray(plan.slot_tok) - plan.n_res
+    f = rmsnorm(np.asarray(y16, np.float16)[rows], w_final16, eps).astype(np.float64)
+    return f @ np.asarray(w_letters16, np.float16).astype(np.float64).T
+
+
+def last_layer(plan, x16, res_k16, res_v16, weights: dict, hq: int, hkv: int, d: int, theta: float, w_final16,
+               w_letters16, eps: float = 1e-5):
+    y = layer(plan, x16, res_k16, res_v16, weights, hq, hkv, d, theta, eps)[0]
+    return letter_logits(plan, y, w_final16, w_letters16, eps)

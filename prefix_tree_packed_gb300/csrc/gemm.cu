@@ -10,6 +10,7 @@
 //   RESIDUAL  C = A B^T + R            (R f16 [M, N], may be C itself)
 //   SWIGLU    C = silu(A G^T) * (A U^T), B = [G; U] with 2N rows,
 //             silu(g) = g / (1 + e^-g)  (the Llama MLP gate)
+//   STORE_F32 C = A B^T kept in f32 (the letter logits of the final layer)
 //
 // Work decomposition: persistent CTAs (one per SM) walk 128 x 256 output
 // tiles (SWIGLU: 128 x 128 outputs from 128 gate + 128 up columns) in an
@@ -247,6 +248,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 f[2 * e + 1] += r2.y;
               }
             }
+            if (a.epi == TREE_GEMM_STORE_F32) {
+              float *frow = reinterpret_cast<float *>(a.c) + (size_t)row * a.n + c;
+              reinterpret_cast<float4 *>(frow)[0] = make_float4(f[0], f[1], f[2], f[3]);
+              reinterpret_cast<float4 *>(frow)[1] = make_float4(f[4], f[5], f[6], f[7]);
+              continue;
+            }
             uint4 w;
             w.x = pack_f16x2(f[0], f[1]);
             w.y = pack_f16x2(f[2], f[3]);
@@ -276,7 +283,7 @@ extern "C" TREE_API int tree_gemm(const void *a, const void *b, void *c, const v
   using namespace tree;
   if (!a || !b || !c) return fail(TREE_ERR_INVALID_ARG, "tree_gemm: NULL argument");
   if (m < 0 || n <= 0 || k <= 0) return fail(TREE_ERR_INVALID_ARG, "tree_gemm: m %d, n %d, k %d", m, n, k);
-  if (epi != TREE_GEMM_STORE && epi != TREE_GEMM_RESIDUAL && epi != TREE_GEMM_SWIGLU)
+  if (epi != TREE_GEMM_STORE && epi != TREE_GEMM_RESIDUAL && epi != TREE_GEMM_SWIGLU && epi != TREE_GEMM_STORE_F32)
     return fail(TREE_ERR_INVALID_ARG, "tree_gemm: unknown epilogue %d", epi);
   if (epi == TREE_GEMM_RESIDUAL && !r) return fail(TREE_ERR_INVALID_ARG, "tree_gemm: RESIDUAL needs r");
   if (n % 8 || k % 8) return fail(TREE_ERR_UNSUPPORTED, "tree_gemm: n %d and k %d must be multiples of 8", n, k);

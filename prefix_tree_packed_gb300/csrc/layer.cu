@@ -7,6 +7,7 @@
 // which earlier iterations have rotated).
 
 #include "common.cuh"
+#include "sm103.cuh"
 #include "tree_layer.h"
 
 namespace tree {
@@ -28,6 +29,52 @@ LayerWs layout(int64_t n_fwd, const tree_layer_weights_t &w) {
   L.g = L.h + up256((size_t)n_fwd * w.hidden * e);
   L.total = L.g + up256((size_t)n_fwd * w.ffn * e);
   return L;
+}
+
+// Last layer: the attention block over every token (the keys and values of all
+// of them are needed), then only the readout rows (one per readout slot).
+struct LastWs {
+  size_t xn, q, o, xs, os, hs, hns, gs, ys, fs, total;
+};
+
+LastWs last_layout(int64_t n_fwd, int64_t n_slots, const tree_layer_weights_t &w) {
+  LastWs L;
+  const size_t e = 2, S = (size_t)n_slots;
+  L.xn = 0;
+  L.q = L.xn + up256((size_t)n_fwd * w.hidden * e);
+  L.o = L.q + up256((size_t)n_fwd * w.hq * w.d * e);
+  L.xs = L.o + up256((size_t)n_fwd * w.hq * w.d * e);
+  L.os = L.xs + up256(S * w.hidden * e);
+  L.hs = L.os + up256(S * w.hq * w.d * e);
+  L.hns = L.hs + up256(S * w.hidden * e);
+  L.gs = L.hns + up256(S * w.hidden * e);
+  L.ys = L.gs + up256(S * w.ffn * e);
+  L.fs = L.ys + up256(S * w.hidden * e);
+  L.total = L.fs + up256(S * w.hidden * e);
+  return L;
+}
+
+constexpr int kGatherWarps = 8;
+
+// dst[i, :] = src[slot_tok[i] - n_res, :] for the readout slots (rows of 16-byte vectors)
+__global__ void __launch_bounds__(kGatherWarps * 32) gather_slots(const uint4 *src, int vec_per_row,
+                                                                   const int32_t *slot_tok, int n_res, uint4 *dst,
+                                                                   int m) {
+  sm103::griddep_wait();
+  sm103::griddep_launch();
+  const int row = blockIdx.x * kGatherWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= m) return;
+  const size_t s = (size_t)(slot_tok[row] - n_res);
+  for (int i = lane; i < vec_per_row; i += 32) dst[(size_t)row * vec_per_row + i] = src[s * vec_per_row + i];
+}
+
+int gather(const __half *src, int cols, const int32_t *slot_tok, int n_res, __half *dst, int m, cudaStream_t s) {
+  if (m == 0) return TREE_OK;
+  const cudaError_t e = launch_dependent(gather_slots, dim3((m + kGatherWarps - 1) / kGatherWarps),
+                                         dim3(kGatherWarps * 32), 0, s, reinterpret_cast<const uint4 *>(src),
+                                         cols / 8, slot_tok, n_res, reinterpret_cast<uint4 *>(dst), m);
+  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_last_layer_fwd: launch failed: %s", cudaGetErrorString(e));
+  return launch_status("tree_last_layer_fwd");
 }
 
 int check_weights(const tree_layer_weights_t *w) {
@@ -99,4 +146,77 @@ extern "C" TREE_API int tree_layer_fwd(const tree_plan_t *plan, const void *plan
   if ((rc = tree_rmsnorm(h, w->w_post, xn, m, w->hidden, w->eps, stream))) return rc;
   if ((rc = tree_gemm(xn, w->wgu, g, nullptr, m, w->ffn, w->hidden, TREE_GEMM_SWIGLU, status, stream))) return rc;
   return tree_gemm(g, w->wd, y, h, m, w->hidden, w->ffn, TREE_GEMM_RESIDUAL, status, stream);
+}
+
+extern "C" TREE_API int tree_last_layer_workspace_bytes(const tree_plan_t *plan, const tree_layer_weights_t *w,
+                                                        size_t *bytes) {
+  using namespace tree;
+  if (!plan || !bytes) return fail(TREE_ERR_INVALID_ARG, "tree_last_layer_workspace_bytes: NULL argument");
+  int rc = check_weights(w);
+  if (rc) return rc;
+  *bytes = last_layout(plan->p.n_tot - plan->p.n_res, (int64_t)plan->p.slot_tok.size(), *w).total;
+  return TREE_OK;
+}
+
+extern "C" TREE_API int tree_last_layer_fwd(const tree_plan_t *plan, const void *plan_dev,
+                                            const tree_layer_weights_t *w, const void *x, void *k_cache,
+                                            void *v_cache, const float *cos_sin, int32_t max_pos, const void *w_final,
+                                            const void *w_letters, int32_t stride, float *logits, void *workspace,
+                                            size_t workspace_bytes, int32_t *work, int32_t *status,
+                                            tree_stream_t stream) {
+  using namespace tree;
+  if (!plan || !plan_dev || !x || !k_cache || !v_cache || !cos_sin || !w_final || !w_letters || !logits || !workspace)
+    return fail(TREE_ERR_INVALID_ARG, "tree_last_layer_fwd: NULL argument");
+  int rc = check_weights(w);
+  if (rc) return rc;
+  if (stride <= 0 || stride % 8) return fail(TREE_ERR_UNSUPPORTED, "tree_last_layer_fwd: stride %d (multiple of 8)", stride);
+  if (!aligned16(w_final) || !aligned16(w_letters) || !aligned16(logits))
+    return fail(TREE_ERR_UNSUPPORTED, "tree_last_layer_fwd: misaligned pointer");
+  const Plan &P = plan->p;
+  const int64_t n_fwd = P.n_tot - P.n_res;
+  const int S = (int)P.slot_tok.size();
+  for (int i = 0; i < S; ++i)
+    if (P.slot_tok[i] < P.n_res)
+      return fail(TREE_ERR_INVALID_ARG, "tree_last_layer_fwd: readout slot %d is a resident token", i);
+  const LastWs L = last_layout(n_fwd, S, *w);
+  if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return fail(TREE_ERR_INVALID_ARG, "tree_last_layer_fwd: workspace of %zu bytes (need %zu, 256-byte aligned)",
+                workspace_bytes, L.total);
+  if (n_fwd == 0 || S == 0) return TREE_OK;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  auto at = [&](size_t off) { return reinterpret_cast<__half *>(ws + off); };
+  __half *xn = at(L.xn), *q = at(L.q), *o = at(L.o);
+  __half *xs = at(L.xs), *os = at(L.os), *hs = at(L.hs), *hns = at(L.hns), *gs = at(L.gs), *ys = at(L.ys),
+         *fs = at(L.fs);
+  const int qd = w->hq * w->d, kvd = w->hkv * w->d, m = (int)n_fwd;
+  __half *kf = static_cast<__half *>(k_cache) + (size_t)P.n_res * kvd;
+  __half *vf = static_cast<__half *>(v_cache) + (size_t)P.n_res * kvd;
+  const int32_t *slot_tok = reinterpret_cast<const int32_t *>(plan_dev) + P.off_slot_tok;
+  const cudaStream_t s = as_stream(stream);
+  // attention block over every forward token
+  if ((rc = tree_rmsnorm(x, w->w_in, xn, m, w->hidden, w->eps, stream))) return rc;
+  if ((rc = tree_gemm(xn, w->wq, q, nullptr, m, qd, w->hidden, TREE_GEMM_STORE, status, stream))) return rc;
+  if ((rc = tree_gemm(xn, w->wk, kf, nullptr, m, kvd, w->hidden, TREE_GEMM_STORE, status, stream))) return rc;
+  if ((rc = tree_gemm(xn, w->wv, vf, nullptr, m, kvd, w->hidden, TREE_GEMM_STORE, status, stream))) return rc;
+  tree_attn_params_t ap{w->hq, w->hkv, w->d, 0.f, nullptr, 0};
+  for (int c = 0; c < P.n_chunks; ++c) {
+    const size_t r0 = (size_t)(P.chunk_q0[c] - P.n_res);
+    if ((rc = tree_rope(plan, plan_dev, c, q + r0 * qd, k_cache, w->hq, w->hkv, w->d, cos_sin, max_pos, status,
+                        stream)))
+      return rc;
+    ap.work = work ? work + 2 * c : nullptr;
+    if ((rc = tree_attn_fwd(plan, plan_dev, c, q + r0 * qd, k_cache, v_cache, o + r0 * qd, nullptr, &ap, status,
+                            stream)))
+      return rc;
+  }
+  // from here on only the readout rows ("01 / Request path: GPU forward pass": in the final
+  // layer the MLP block and the logits are computed only for readout positions and letters)
+  if ((rc = gather(o, qd, slot_tok, P.n_res, os, S, s))) return rc;
+  if ((rc = gather(static_cast<const __half *>(x), w->hidden, slot_tok, P.n_res, xs, S, s))) return rc;
+  if ((rc = tree_gemm(os, w->wo, hs, xs, S, w->hidden, qd, TREE_GEMM_RESIDUAL, status, stream))) return rc;
+  if ((rc = tree_rmsnorm(hs, w->w_post, hns, S, w->hidden, w->eps, stream))) return rc;
+  if ((rc = tree_gemm(hns, w->wgu, gs, nullptr, S, w->ffn, w->hidden, TREE_GEMM_SWIGLU, status, stream))) return rc;
+  if ((rc = tree_gemm(gs, w->wd, ys, hs, S, w->hidden, w->ffn, TREE_GEMM_RESIDUAL, status, stream))) return rc;
+  if ((rc = tree_rmsnorm(ys, w_final, fs, S, w->hidden, w->eps, stream))) return rc;
+  return tree_gemm(fs, w_letters, logits, nullptr, S, stride, w->hidden, TREE_GEMM_STORE_F32, status, stream);
 }

@@ -29,6 +29,7 @@ __all__ = [
     "draw_qkv",
     "draw_logits",
     "draw_layer",
+    "draw_head",
     "draw_readout_batch",
     "random_forest",
 ]
@@ -275,6 +276,14 @@ def draw_layer(n_fwd: int, n_res: int, hidden: int, hq: int, hkv: int, d: int, f
     res_k = rng.standard_normal((n_res, hkv * d), dtype=np.float32).astype(np.float16)
     res_v = rng.standard_normal((n_res, hkv * d), dtype=np.float32).astype(np.float16)
     return w, x, res_k, res_v
+
+
+def draw_head(hidden: int, stride: int, seed: int):
+    """The final RMSNorm weight and the LM-head rows of the answer letters (f16, random init)."""
+    rng = np.random.default_rng(seed + 5000)
+    w_final = (1.0 + 0.1 * rng.standard_normal(hidden)).astype(np.float16)
+    w_letters = (rng.standard_normal((stride, hidden), dtype=np.float32) / np.sqrt(hidden)).astype(np.float16)
+    return w_final, w_letters
 
 
 def draw_logits(n_slots: int, stride: int, sigma: float, seed: int):

@@ -177,3 +177,87 @@ def test_layer_matches_oracle(wn):
     err = np.abs(y_g.astype(np.float64) - y_ref.astype(np.float64)).max()
     scale = np.abs(y_ref.astype(np.float64)).max()
     assert err <= 2e-2 * max(1.0, scale), (err, scale)
+
+
+def _last_ws_offsets(n_fwd, n_slots, hidden, qd, ffn):
+    up = lambda b: (b + 255) & ~255
+    o = {}
+    o["xn"] = 0
+    o["q"] = o["xn"] + up(n_fwd * hidden * 2)
+    o["o"] = o["q"] + up(n_fwd * qd * 2)
+    o["xs"] = o["o"] + up(n_fwd * qd * 2)
+    o["os"] = o["xs"] + up(n_slots * hidden * 2)
+    o["hs"] = o["os"] + up(n_slots * qd * 2)
+    o["hns"] = o["hs"] + up(n_slots * hidden * 2)
+    o["gs"] = o["hns"] + up(n_slots * hidden * 2)
+    o["ys"] = o["gs"] + up(n_slots * ffn * 2)
+    o["fs"] = o["ys"] + up(n_slots * hidden * 2)
+    o["total"] = o["fs"] + up(n_slots * hidden * 2)
+    return o
+
+
+@pytest.mark.parametrize("wn", [1, 2])
+def test_last_layer_logits_and_readout(wn):
+    """The final layer pruned to the readout rows, its letter logits, and the decision from them."""
+    import synth
+    from oracle import plan as oplan
+    from oracle import readout as ordo
+    dev = torch.device("cuda")
+    w = synth.workload(wn)
+    hidden, ffn = LAYERS[wn]
+    stride = 8
+    plan = lib.Plan.from_forest(w.forest, leaf1=w.leaf1, leaf2=w.leaf2)
+    i = plan.info
+    n_fwd, n_res, S = i.n_tot - i.n_res, i.n_res, i.n_slots
+    wts, x, rk, rv = synth.draw_layer(n_fwd, n_res, hidden, w.hq, w.hkv, w.d, ffn, w.seed)
+    wf, wl = synth.draw_head(hidden, stride, w.seed)
+    td = {k: torch.from_numpy(v).to(dev) for k, v in wts.items()}
+    lw = lib.layer_weights(hidden, w.hq, w.hkv, w.d, ffn, td)
+    nbytes = lib.last_layer_workspace_bytes(plan, lw)
+    qd, kvd = w.hq * w.d, w.hkv * w.d
+    off = _last_ws_offsets(n_fwd, S, hidden, qd, ffn)
+    assert nbytes == off["total"]
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    pdev = torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev)
+    plan.upload(pdev, i.dev_bytes)
+    tab = torch.from_numpy(lib.rope_table(i.max_pos, w.d, w.theta)).to(dev)
+    tx = torch.from_numpy(x).to(dev)
+    kc = torch.zeros(i.n_tot, kvd, dtype=torch.float16, device=dev)
+    vc = torch.zeros_like(kc)
+    kc[:n_res] = torch.from_numpy(rk).to(dev)
+    vc[:n_res] = torch.from_numpy(rv).to(dev)
+    twf, twl = torch.from_numpy(wf).to(dev), torch.from_numpy(wl).to(dev)
+    logits = torch.full((S, stride), float("nan"), device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib.last_layer_fwd(plan, pdev, lw, tx, kc, vc, tab, i.max_pos, twf, twl, stride, logits, ws, nbytes, status=st)
+    # the decision from the logits, on the device (the plan's question -> slot maps)
+    p_cal = torch.empty((i.n_questions, stride), device=dev)
+    choice = torch.empty(i.n_questions, dtype=torch.int32, device=dev)
+    base = pdev.data_ptr()
+    lib.readout_decide(logits, stride, base + i.off_r1, base + i.off_r2, torch.from_numpy(w.n_letters).to(dev),
+                       torch.from_numpy(w.temperature).to(dev), i.n_questions, p_cal, None, choice, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    lg = logits.cpu().numpy().astype(np.float64)
+
+    op, qmap = oplan.plan_forest(w.forest, leaf1=w.leaf1, leaf2=w.leaf2)
+    # step: the letter logits from the library's own final-layer rows (one f16 rounding of the
+    # normalised row, then an f32 dot product)
+    ys = ws[off["ys"]: off["ys"] + S * hidden * 2].view(torch.float16).view(S, hidden).cpu().numpy()
+    fs_ref = ol.rmsnorm(ys, wf, 1e-5).astype(np.float64)
+    step_ref = fs_ref @ wl.astype(np.float64).T
+    row_scale = np.abs(fs_ref) @ np.abs(wl.astype(np.float64)).T
+    assert (np.abs(lg - step_ref) <= 2 * 2 ** -10 * row_scale + 1e-4).all()
+    # end to end against the oracle's full final layer restricted to the readout rows
+    ref = ol.last_layer(op, x, rk, rv, wts, w.hq, w.hkv, w.d, w.theta, wf, wl)
+    err = np.abs(lg - ref).max()
+    assert err <= 2e-2 * max(1.0, np.abs(ref).max()), err
+    # decisions: equal wherever the oracle's two best probabilities are apart by more than the
+    # probability change that error can make
+    ref_pc, ref_p, ref_choice = ordo.decide(ref, qmap["r1"], qmap["r2"], w.n_letters, w.temperature, stride)
+    assert np.abs(p_cal.cpu().numpy() - ref_pc).max() <= 5e-2
+    got = choice.cpu().numpy()
+    for qi in range(i.n_questions):
+        srt = np.sort(ref_p[qi][: w.n_letters[qi]])
+        if len(srt) < 2 or srt[-1] - srt[-2] > 5e-2:
+            assert got[qi] == ref_choice[qi], qi

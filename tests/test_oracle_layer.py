@@ -51,3 +51,16 @@ def test_swiglu_closed_forms():
     a1[:, 0] = 1
     got = ol.gemm(a1, np.concatenate([g, u_one]), "swiglu")
     np.testing.assert_array_equal(got, ol.silu(a1.astype(np.float64) @ g.astype(np.float64).T).astype(np.float16))
+
+
+def test_letter_logits_special_case():
+    # rows of +-1 normalise to +-1 (eps 0) times the final weight; logits are then a plain matmul
+    from types import SimpleNamespace
+    rng = np.random.default_rng(4)
+    y = np.where(rng.random((6, 16)) < 0.5, -1.0, 1.0).astype(np.float16)
+    wf = rng.integers(-2, 3, 16).astype(np.float16)
+    wl = rng.integers(-3, 4, (8, 16)).astype(np.float16)
+    plan = SimpleNamespace(slot_tok=np.array([7, 3, 5]), n_res=2)
+    got = ol.letter_logits(plan, y, wf, wl, eps=0.0)
+    rows = y[[5, 1, 3]].astype(np.int64) * wf.astype(np.int64)
+    np.testing.assert_array_equal(got, rows @ wl.astype(np.int64).T)
