@@ -123,6 +123,25 @@ TREE_API int tree_last_layer_fwd(const tree_plan_t *plan, const void *plan_dev, 
                                  void *workspace, size_t workspace_bytes, int32_t *work, int32_t *status,
                                  tree_stream_t stream);
 
+/*
+ * A whole decision forward: n_layers Llama layers over the planned batch, the
+ * last one pruned to the readout rows, ending in the letter logits
+ * (readout_decide then takes them with the plan's r1 / r2).
+ *
+ *   layers    [n_layers] weights, host array of device pointers (layer l reads layers[l])
+ *   x         f16 [n_fwd, hidden] the forward tokens' input hidden states (embeddings)
+ *   k_caches, v_caches  host arrays [n_layers] of f16 [n_tot, hkv * d] caches (as in tree_layer_fwd)
+ *   workspace tree_model_workspace_bytes bytes, 256-byte aligned
+ * Every layer must have the same sizes.  Launches only; nothing is synchronised.
+ */
+TREE_API int tree_model_workspace_bytes(const tree_plan_t *plan, const tree_layer_weights_t *w, size_t *bytes);
+
+TREE_API int tree_model_fwd(const tree_plan_t *plan, const void *plan_dev, const tree_layer_weights_t *layers,
+                            int32_t n_layers, const void *x, void *const *k_caches, void *const *v_caches,
+                            const float *cos_sin, int32_t max_pos, const void *w_final, const void *w_letters,
+                            int32_t stride, float *logits, void *workspace, size_t workspace_bytes, int32_t *work,
+                            int32_t *status, tree_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

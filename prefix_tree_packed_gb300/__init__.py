@@ -41,7 +41,7 @@ EXPORTS = (
     "tree_queue_info", "tree_queue_pop", "tree_batch_view", "tree_batch_free",
     # include/tree_layer.h
     "tree_gemm", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd", "tree_last_layer_workspace_bytes",
-    "tree_last_layer_fwd",
+    "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd",
 )
 
 GEMM_STORE = 0
@@ -172,6 +172,9 @@ _lib.tree_layer_fwd.argtypes = [_vp, _vp, C.POINTER(LayerWeights), _vp, _vp, _vp
 _lib.tree_last_layer_workspace_bytes.argtypes = [_vp, C.POINTER(LayerWeights), C.POINTER(C.c_size_t)]
 _lib.tree_last_layer_fwd.argtypes = [_vp, _vp, C.POINTER(LayerWeights), _vp, _vp, _vp, _vp, C.c_int32, _vp, _vp,
                                      C.c_int32, _vp, _vp, C.c_size_t, _vp, _vp, _vp]
+_lib.tree_model_workspace_bytes.argtypes = [_vp, C.POINTER(LayerWeights), C.POINTER(C.c_size_t)]
+_lib.tree_model_fwd.argtypes = [_vp, _vp, C.POINTER(LayerWeights), C.c_int32, _vp, C.POINTER(_vp), C.POINTER(_vp),
+                                _vp, C.c_int32, _vp, _vp, C.c_int32, _vp, _vp, C.c_size_t, _vp, _vp, _vp]
 _lib.tree_queue_default_opts.argtypes = [C.POINTER(QueueOpts)]
 _lib.tree_queue_create.argtypes = [C.POINTER(QueueOpts), C.POINTER(_vp)]
 _lib.tree_queue_destroy.argtypes = [_vp]
@@ -182,7 +185,8 @@ _lib.tree_queue_pop.argtypes = [_vp, C.c_double, C.POINTER(_vp)]
 _lib.tree_batch_view.argtypes = [_vp, C.POINTER(_BatchView)]
 _lib.tree_batch_free.argtypes = [_vp]
 for _f in ("tree_gemm", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd",
-           "tree_last_layer_workspace_bytes", "tree_last_layer_fwd", "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
+           "tree_last_layer_workspace_bytes", "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd",
+           "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
            "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel", "tree_queue_info",
            "tree_queue_pop", "tree_batch_view", "tree_batch_free"):
     getattr(_lib, _f).restype = C.c_int
@@ -295,6 +299,24 @@ def last_layer_fwd(plan: "Plan", plan_dev, w: LayerWeights, x, k_cache, v_cache,
     _check(_lib.tree_last_layer_fwd(plan.handle, _ptr(plan_dev), C.byref(w), _ptr(x), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(cos_sin), max_pos, _ptr(w_final), _ptr(w_letters), stride, _ptr(logits),
                                     _ptr(workspace), workspace_bytes, _ptr(work), _ptr(status), _stream(stream)))
+
+
+def model_workspace_bytes(plan: "Plan", w: LayerWeights) -> int:
+    n = C.c_size_t()
+    _check(_lib.tree_model_workspace_bytes(plan.handle, C.byref(w), C.byref(n)))
+    return int(n.value)
+
+
+def model_fwd(plan: "Plan", plan_dev, layers, x, k_caches, v_caches, cos_sin, max_pos: int, w_final, w_letters,
+              stride: int, logits, workspace, workspace_bytes: int, work=None, status=None, stream=None):
+    """tree_model_fwd: every layer (the last pruned to the readout rows) and the letter logits."""
+    n = len(layers)
+    arr = (LayerWeights * n)(*layers)
+    kc = (_vp * n)(*[_ptr(t) for t in k_caches])
+    vc = (_vp * n)(*[_ptr(t) for t in v_caches])
+    _check(_lib.tree_model_fwd(plan.handle, _ptr(plan_dev), arr, n, _ptr(x), kc, vc, _ptr(cos_sin), max_pos,
+                               _ptr(w_final), _ptr(w_letters), stride, _ptr(logits), _ptr(workspace), workspace_bytes,
+                               _ptr(work), _ptr(status), _stream(stream)))
 
 
 def queue_default_opts() -> QueueOpts:

@@ -220,3 +220,70 @@ extern "C" TREE_API int tree_last_layer_fwd(const tree_plan_t *plan, const void 
   if ((rc = tree_rmsnorm(ys, w_final, fs, S, w->hidden, w->eps, stream))) return rc;
   return tree_gemm(fs, w_letters, logits, nullptr, S, stride, w->hidden, TREE_GEMM_STORE_F32, status, stream);
 }
+
+// ---------------------------------------------------------------------------
+// tree_model_fwd: layers 0 .. n-2 through tree_layer_fwd (hidden states in two
+// buffers taken in turn), the last through tree_last_layer_fwd.
+
+namespace tree {
+namespace {
+
+size_t model_bytes(const Plan &P, const tree_layer_weights_t &w) {
+  const int64_t n_fwd = P.n_tot - P.n_res;
+  const size_t hid = up256((size_t)n_fwd * w.hidden * 2);
+  const size_t a = layout(n_fwd, w).total, b = last_layout(n_fwd, (int64_t)P.slot_tok.size(), w).total;
+  return 2 * hid + (a > b ? a : b);
+}
+
+}  // namespace
+}  // namespace tree
+
+extern "C" TREE_API int tree_model_workspace_bytes(const tree_plan_t *plan, const tree_layer_weights_t *w,
+                                                   size_t *bytes) {
+  using namespace tree;
+  if (!plan || !bytes) return fail(TREE_ERR_INVALID_ARG, "tree_model_workspace_bytes: NULL argument");
+  int rc = check_weights(w);
+  if (rc) return rc;
+  *bytes = model_bytes(plan->p, *w);
+  return TREE_OK;
+}
+
+extern "C" TREE_API int tree_model_fwd(const tree_plan_t *plan, const void *plan_dev,
+                                       const tree_layer_weights_t *layers, int32_t n_layers, const void *x,
+                                       void *const *k_caches, void *const *v_caches, const float *cos_sin,
+                                       int32_t max_pos, const void *w_final, const void *w_letters, int32_t stride,
+                                       float *logits, void *workspace, size_t workspace_bytes, int32_t *work,
+                                       int32_t *status, tree_stream_t stream) {
+  using namespace tree;
+  if (!plan || !layers || n_layers < 1 || !x || !k_caches || !v_caches || !workspace)
+    return fail(TREE_ERR_INVALID_ARG, "tree_model_fwd: NULL argument or n_layers %d", n_layers);
+  const tree_layer_weights_t &w0 = layers[0];
+  int rc = check_weights(&w0);
+  if (rc) return rc;
+  for (int l = 1; l < n_layers; ++l)
+    if (layers[l].hidden != w0.hidden || layers[l].hq != w0.hq || layers[l].hkv != w0.hkv || layers[l].d != w0.d ||
+        layers[l].ffn != w0.ffn)
+      return fail(TREE_ERR_INVALID_ARG, "tree_model_fwd: layer %d has other sizes than layer 0", l);
+  const Plan &P = plan->p;
+  const size_t need = model_bytes(P, w0);
+  if (workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return fail(TREE_ERR_INVALID_ARG, "tree_model_fwd: workspace of %zu bytes (need %zu, 256-byte aligned)",
+                workspace_bytes, need);
+  const int64_t n_fwd = P.n_tot - P.n_res;
+  const size_t hid = up256((size_t)n_fwd * w0.hidden * 2);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  void *buf[2] = {ws, ws + hid};
+  uint8_t *inner = ws + 2 * hid;
+  const size_t inner_bytes = workspace_bytes - 2 * hid;
+  const void *cur = x;
+  for (int l = 0; l + 1 < n_layers; ++l) {
+    void *next = buf[l & 1];
+    if ((rc = tree_layer_fwd(plan, plan_dev, &layers[l], cur, k_caches[l], v_caches[l], next, cos_sin, max_pos,
+                             inner, inner_bytes, work, status, stream)))
+      return rc;
+    cur = next;
+  }
+  const int l = n_layers - 1;
+  return tree_last_layer_fwd(plan, plan_dev, &layers[l], cur, k_caches[l], v_caches[l], cos_sin, max_pos, w_final,
+                             w_letters, stride, logits, inner, inner_bytes, work, status, stream);
+}

@@ -261,3 +261,68 @@ def test_last_layer_logits_and_readout(wn):
         srt = np.sort(ref_p[qi][: w.n_letters[qi]])
         if len(srt) < 2 or srt[-1] - srt[-2] > 5e-2:
             assert got[qi] == ref_choice[qi], qi
+
+
+def test_model_fwd_equals_layer_calls_and_oracle():
+    """Three layers on the tiny tree: bit-identical to calling the layers one by one, and near the oracle."""
+    import synth
+    from oracle import plan as oplan
+    dev = torch.device("cuda")
+    w = synth.workload(1)
+    hidden, ffn = LAYERS[1]
+    stride, L = 8, 3
+    plan = lib.Plan.from_forest(w.forest, leaf1=w.leaf1, leaf2=w.leaf2)
+    i = plan.info
+    n_fwd, n_res, S = i.n_tot - i.n_res, i.n_res, i.n_slots
+    qd, kvd = w.hq * w.d, w.hkv * w.d
+    layers, tds, x = [], [], None
+    for l in range(L):
+        wts, x_l, _, _ = synth.draw_layer(n_fwd, n_res, hidden, w.hq, w.hkv, w.d, ffn, w.seed + 17 * l)
+        x = x_l if x is None else x
+        td = {k: torch.from_numpy(v).to(dev) for k, v in wts.items()}
+        tds.append((wts, td))
+        layers.append(lib.layer_weights(hidden, w.hq, w.hkv, w.d, ffn, td))
+    wf, wl = synth.draw_head(hidden, stride, w.seed)
+    twf, twl = torch.from_numpy(wf).to(dev), torch.from_numpy(wl).to(dev)
+    pdev = torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev)
+    plan.upload(pdev, i.dev_bytes)
+    tab = torch.from_numpy(lib.rope_table(i.max_pos, w.d, w.theta)).to(dev)
+    tx = torch.from_numpy(x).to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def caches():
+        return ([torch.zeros(i.n_tot, kvd, dtype=torch.float16, device=dev) for _ in range(L)],
+                [torch.zeros(i.n_tot, kvd, dtype=torch.float16, device=dev) for _ in range(L)])
+
+    kc, vc = caches()
+    nb = lib.model_workspace_bytes(plan, layers[0])
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    logits = torch.empty((S, stride), device=dev)
+    lib.model_fwd(plan, pdev, layers, tx, kc, vc, tab, i.max_pos, twf, twl, stride, logits, ws, nb, status=st)
+    # the same layers called one by one
+    kc2, vc2 = caches()
+    nl = lib.layer_workspace_bytes(plan, layers[0])
+    ws2 = torch.empty(max(nl, lib.last_layer_workspace_bytes(plan, layers[0])), dtype=torch.uint8, device=dev)
+    cur = tx
+    for l in range(L - 1):
+        nxt = torch.empty_like(tx)
+        lib.layer_fwd(plan, pdev, layers[l], cur, kc2[l], vc2[l], nxt, tab, i.max_pos, ws2, ws2.numel(), status=st)
+        cur = nxt
+    logits2 = torch.empty((S, stride), device=dev)
+    lib.last_layer_fwd(plan, pdev, layers[-1], cur, kc2[-1], vc2[-1], tab, i.max_pos, twf, twl, stride, logits2, ws2,
+                       ws2.numel(), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(logits, logits2)
+    for l in range(L):
+        assert torch.equal(kc[l], kc2[l]) and torch.equal(vc[l], vc2[l])
+    # the oracle model: layer after layer in float64 with f16 storage
+    op, _ = oplan.plan_forest(w.forest, leaf1=w.leaf1, leaf2=w.leaf2)
+    empty = np.zeros((0, kvd), np.float16)
+    h = x
+    for l in range(L - 1):
+        h = ol.layer(op, h, empty, empty, tds[l][0], w.hq, w.hkv, w.d, w.theta)[0]
+    ref = ol.last_layer(op, h, empty, empty, tds[-1][0], w.hq, w.hkv, w.d, w.theta, wf, wl)
+    err = np.abs(logits.cpu().numpy().astype(np.float64) - ref).max()
+    # each layer contributes the single-layer bound
+    assert err <= L * 2e-2 * max(1.0, np.abs(ref).max()), err
