@@ -324,6 +324,87 @@ def measure_layer(lib, torch, w, dev, stream, reps, warmup):
                 attn_flops=attn_flops, gemms=per)
 
 
+def decision_forest():
+    """The page's six-prompt example as one request: template 53 (resident) -> state 120 ->
+    3 questions of 24 -> 2 option orders of 18; 4 letters per question."""
+    parent, length, resident = [-1, 0], [53, 120], [1, 0]
+    leaf1, leaf2 = [], []
+    for _ in range(3):
+        parent.append(1)
+        length.append(24)
+        resident.append(0)
+        qb = len(parent) - 1
+        for o in range(2):
+            parent.append(qb)
+            length.append(18)
+            resident.append(0)
+            (leaf1 if o == 0 else leaf2).append(len(parent) - 1)
+    return dict(parent=parent, length=length, resident=resident, leaf1=leaf1, leaf2=leaf2,
+                n_letters=np.full(3, 4, np.int32), temperature=np.ones(3, np.float32))
+
+
+def measure_model(lib, torch, dev, stream, spec: dict, d: int, hq: int, hkv: int, theta: float, n_layers: int,
+                  reps: int, warmup: int, seed: int, stride: int = 8):
+    """tree_model_fwd + readout_decide on one planned batch; random-init weights drawn on the device."""
+    hidden, ffn = (2048, 8192) if d == 64 else (4096, 14336)
+    plan = lib.Plan(spec["parent"], spec["length"], spec.get("key"), spec["resident"], spec["leaf1"], spec["leaf2"])
+    i = plan.info
+    n_fwd, n_res = i.n_tot - i.n_res, i.n_res
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def rnd(*shape, scale=1.0, off=0.0):
+        return (torch.randn(*shape, generator=g, device=dev, dtype=torch.float32) * scale + off).to(torch.float16)
+
+    qd, kvd = hq * d, hkv * d
+    keep, layers, kcs, vcs = [], [], [], []
+    for _ in range(n_layers):
+        t = {"w_in": rnd(hidden, scale=0.1, off=1.0), "wq": rnd(qd, hidden, scale=hidden ** -0.5),
+             "wk": rnd(kvd, hidden, scale=hidden ** -0.5), "wv": rnd(kvd, hidden, scale=hidden ** -0.5),
+             "wo": rnd(hidden, qd, scale=qd ** -0.5), "w_post": rnd(hidden, scale=0.1, off=1.0),
+             "wgu": rnd(2 * ffn, hidden, scale=hidden ** -0.5), "wd": rnd(hidden, ffn, scale=ffn ** -0.5)}
+        keep.append(t)
+        layers.append(lib.layer_weights(hidden, hq, hkv, d, ffn, t))
+        kcs.append(rnd(i.n_tot, kvd))
+        vcs.append(rnd(i.n_tot, kvd))
+    w_final, w_letters = rnd(hidden, scale=0.1, off=1.0), rnd(stride, hidden, scale=hidden ** -0.5)
+    x = rnd(n_fwd, hidden)
+    pdev = torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev)
+    plan.upload(pdev, i.dev_bytes, stream)
+    tab = torch.from_numpy(lib.rope_table(i.max_pos, d, theta)).to(dev)
+    nb = lib.model_workspace_bytes(plan, layers[0])
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    logits = torch.empty((i.n_slots, stride), device=dev)
+    p_cal = torch.empty((i.n_questions, stride), device=dev)
+    choice = torch.empty(i.n_questions, dtype=torch.int32, device=dev)
+    has_q = spec["leaf1"] is not None and spec["n_letters"] is not None and i.n_questions > 0
+    nl = torch.from_numpy(spec["n_letters"]).to(dev) if has_q else None
+    temp = torch.from_numpy(spec["temperature"]).to(dev) if has_q else None
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    work = torch.zeros(2 * i.n_chunks, dtype=torch.int32, device=dev)
+    base = pdev.data_ptr()
+
+    def run():
+        lib.model_fwd(plan, pdev, layers, x, kcs, vcs, tab, i.max_pos, w_final, w_letters, stride, logits, ws, nb,
+                      work=work, status=st, stream=stream)
+        if has_q:
+            lib.readout_decide(logits, stride, base + i.off_r1, base + i.off_r2, nl, temp, i.n_questions, p_cal,
+                               None, choice, st, stream)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record(stream)
+    for _ in range(reps):
+        run()
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "device status word set"
+    ms = ev[0].elapsed_time(ev[1]) / reps
+    return dict(ms=ms, tokens=n_fwd, resident=n_res, questions=i.n_questions if has_q else 0, hidden=hidden, ffn=ffn)
+
+
 def run_only(args):
     """One kernel by itself on cuda:0: a JSON line with its time and roofline."""
     import torch
@@ -333,6 +414,28 @@ def run_only(args):
     stream = torch.cuda.current_stream()
     peaks = _peaks()
     line = {"kernel": args.only, "steps": args.steps, "warmup": args.warmup}
+    if args.only == "model":
+        w = synth.workload(args.workload)
+        spec = dict(parent=w.forest.parent, length=w.forest.length, key=w.forest.key, resident=w.forest.resident,
+                    leaf1=w.leaf1,
+                    leaf2=w.leaf2, n_letters=w.n_letters, temperature=w.temperature)
+        batch = measure_model(lib, torch, dev, stream, spec, w.d, w.hq, w.hkv, w.theta, args.layers, args.steps,
+                              args.warmup, seed=w.seed)
+        one = measure_model(lib, torch, dev, stream, decision_forest(), w.d, w.hq, w.hkv, w.theta, args.layers,
+                            args.steps, args.warmup, seed=w.seed + 1)
+        line.update(workload=w.name, layers=args.layers, hidden=batch["hidden"], ffn=batch["ffn"],
+                    weights="random init (no trained weights)",
+                    batch=dict(ms=round(batch["ms"], 3), forward_tokens=batch["tokens"], questions=batch["questions"],
+                               tokens_per_s=round(batch["tokens"] / (batch["ms"] / 1e3), 1),
+                               decisions_per_s=round(batch["questions"] / (batch["ms"] / 1e3), 1),
+                               readout_slots=int(lib.Plan(spec["parent"], spec["length"], spec["key"],
+                                                          spec["resident"]).info.n_slots)),
+                    one_request=dict(what="the page's six-prompt example: template 53 resident, state 120, "
+                                          "3 questions x (24 + 2 orders x 18), 4 letters",
+                                     ms=round(one["ms"], 3), forward_tokens=one["tokens"], questions=one["questions"]))
+        line["peak_source"] = peaks["src"]
+        print(json.dumps(line), flush=True)
+        return
     if args.only == "readout":
         ms, nbytes = measure_readout(lib, torch, dev, stream, reps=args.steps, n_sets=args.sets or 16,
                                      warmup=args.warmup, n_questions=args.questions)
@@ -647,7 +750,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--only", choices=["attn", "rope", "readout", "layer"], default=None)
+    ap.add_argument("--only", choices=["attn", "rope", "readout", "layer", "model"], default=None)
+    ap.add_argument("--layers", type=int, default=16, help="layers for --only model (Llama-1B: 16)")
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets for --only (0: default)")
     ap.add_argument("--questions", type=int, default=65536, help="questions for --only readout")
     ap.add_argument("--keys-only", action="store_true", help="--only rope: rotate the keys alone")

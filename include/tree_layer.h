@@ -142,6 +142,36 @@ TREE_API int tree_model_fwd(const tree_plan_t *plan, const void *plan_dev, const
                             int32_t stride, float *logits, void *workspace, size_t workspace_bytes, int32_t *work,
                             int32_t *status, tree_stream_t stream);
 
+/*
+ * Long-request lane ("04 / Scheduling": a request over long_tokens runs in its
+ * own lane that shares the GPU with short batches and yields it between layers:
+ * after a layer, if it has run for at least long_slice_ms, it gives the GPU back
+ * and later resumes at the next layer with the same tensors).
+ *
+ * A session is tree_model_fwd cut at layer boundaries.  It keeps the caller's
+ * buffers (arguments as tree_model_fwd; they must stay valid and untouched
+ * until the session is done) and the next layer to run; the plan is built once
+ * and serves every layer.  tree_session_run enqueues whole layers on `stream`,
+ * waiting for each layer's end (an event), until the wall time since the call
+ * began reaches slice_ms or the last layer (with the logits) is done.  It always
+ * runs at least one layer.  The results equal tree_model_fwd's bit for bit,
+ * however the layers are cut into slices and whatever runs on the GPU between
+ * slices.
+ */
+typedef struct tree_session tree_session_t;
+
+TREE_API int tree_session_create(const tree_plan_t *plan, const void *plan_dev, const tree_layer_weights_t *layers,
+                                 int32_t n_layers, const void *x, void *const *k_caches, void *const *v_caches,
+                                 const float *cos_sin, int32_t max_pos, const void *w_final, const void *w_letters,
+                                 int32_t stride, float *logits, void *workspace, size_t workspace_bytes,
+                                 int32_t *work, int32_t *status, tree_session_t **out);
+
+/* *layers_run = layers this call ran; *done = 1 once the last layer has run. */
+TREE_API int tree_session_run(tree_session_t *s, double slice_ms, tree_stream_t stream, int32_t *layers_run,
+                              int32_t *done);
+
+TREE_API int tree_session_destroy(tree_session_t *s);
+
 #ifdef __cplusplus
 }
 #endif

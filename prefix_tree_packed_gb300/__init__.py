@@ -41,7 +41,8 @@ EXPORTS = (
     "tree_queue_info", "tree_queue_pop", "tree_batch_view", "tree_batch_free",
     # include/tree_layer.h
     "tree_gemm", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd", "tree_last_layer_workspace_bytes",
-    "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd",
+    "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd", "tree_session_create", "tree_session_run",
+    "tree_session_destroy",
 )
 
 GEMM_STORE = 0
@@ -175,6 +176,11 @@ _lib.tree_last_layer_fwd.argtypes = [_vp, _vp, C.POINTER(LayerWeights), _vp, _vp
 _lib.tree_model_workspace_bytes.argtypes = [_vp, C.POINTER(LayerWeights), C.POINTER(C.c_size_t)]
 _lib.tree_model_fwd.argtypes = [_vp, _vp, C.POINTER(LayerWeights), C.c_int32, _vp, C.POINTER(_vp), C.POINTER(_vp),
                                 _vp, C.c_int32, _vp, _vp, C.c_int32, _vp, _vp, C.c_size_t, _vp, _vp, _vp]
+_lib.tree_session_create.argtypes = [_vp, _vp, C.POINTER(LayerWeights), C.c_int32, _vp, C.POINTER(_vp),
+                                     C.POINTER(_vp), _vp, C.c_int32, _vp, _vp, C.c_int32, _vp, _vp, C.c_size_t, _vp,
+                                     _vp, C.POINTER(_vp)]
+_lib.tree_session_run.argtypes = [_vp, C.c_double, _vp, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]
+_lib.tree_session_destroy.argtypes = [_vp]
 _lib.tree_queue_default_opts.argtypes = [C.POINTER(QueueOpts)]
 _lib.tree_queue_create.argtypes = [C.POINTER(QueueOpts), C.POINTER(_vp)]
 _lib.tree_queue_destroy.argtypes = [_vp]
@@ -186,6 +192,7 @@ _lib.tree_batch_view.argtypes = [_vp, C.POINTER(_BatchView)]
 _lib.tree_batch_free.argtypes = [_vp]
 for _f in ("tree_gemm", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd",
            "tree_last_layer_workspace_bytes", "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd",
+           "tree_session_create", "tree_session_run", "tree_session_destroy",
            "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
            "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel", "tree_queue_info",
            "tree_queue_pop", "tree_batch_view", "tree_batch_free"):
@@ -317,6 +324,35 @@ def model_fwd(plan: "Plan", plan_dev, layers, x, k_caches, v_caches, cos_sin, ma
     _check(_lib.tree_model_fwd(plan.handle, _ptr(plan_dev), arr, n, _ptr(x), kc, vc, _ptr(cos_sin), max_pos,
                                _ptr(w_final), _ptr(w_letters), stride, _ptr(logits), _ptr(workspace), workspace_bytes,
                                _ptr(work), _ptr(status), _stream(stream)))
+
+
+class Session:
+    """``tree_session``: a decision forward of the long-request lane, run in slices of whole layers."""
+
+    def __init__(self, plan: "Plan", plan_dev, layers, x, k_caches, v_caches, cos_sin, max_pos: int, w_final,
+                 w_letters, stride: int, logits, workspace, workspace_bytes: int, work=None, status=None):
+        n = len(layers)
+        self._arr = (LayerWeights * n)(*layers)
+        kc = (_vp * n)(*[_ptr(t) for t in k_caches])
+        vc = (_vp * n)(*[_ptr(t) for t in v_caches])
+        self._s = _vp()
+        _check(_lib.tree_session_create(plan.handle, _ptr(plan_dev), self._arr, n, _ptr(x), kc, vc, _ptr(cos_sin),
+                                        max_pos, _ptr(w_final), _ptr(w_letters), stride, _ptr(logits),
+                                        _ptr(workspace), workspace_bytes, _ptr(work), _ptr(status), C.byref(self._s)))
+
+    def run(self, slice_ms: float, stream=None) -> tuple[int, bool]:
+        """Run whole layers until slice_ms of wall time has passed; returns (layers run, done)."""
+        ran, done = C.c_int32(), C.c_int32()
+        _check(_lib.tree_session_run(self._s, float(slice_ms), _stream(stream), C.byref(ran), C.byref(done)))
+        return int(ran.value), bool(done.value)
+
+    def close(self):
+        if self._s:
+            _lib.tree_session_destroy(self._s)
+            self._s = _vp()
+
+    def __del__(self):
+        self.close()
 
 
 def queue_default_opts() -> QueueOpts:

@@ -6,6 +6,9 @@
 // attention run per forward chunk (chunk c reads the keys of chunks <= c,
 // which earlier iterations have rotated).
 
+#include <chrono>
+#include <vector>
+
 #include "common.cuh"
 #include "sm103.cuh"
 #include "tree_layer.h"
@@ -286,4 +289,117 @@ extern "C" TREE_API int tree_model_fwd(const tree_plan_t *plan, const void *plan
   const int l = n_layers - 1;
   return tree_last_layer_fwd(plan, plan_dev, &layers[l], cur, k_caches[l], v_caches[l], cos_sin, max_pos, w_final,
                              w_letters, stride, logits, inner, inner_bytes, work, status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Long-lane sessions: tree_model_fwd's layer loop, resumable between layers.
+
+struct tree_session {
+  const tree_plan_t *plan = nullptr;
+  const void *plan_dev = nullptr;
+  std::vector<tree_layer_weights_t> layers;
+  std::vector<void *> kc, vc;
+  const void *x = nullptr;
+  const float *cos_sin = nullptr;
+  int32_t max_pos = 0, stride = 0;
+  const void *w_final = nullptr, *w_letters = nullptr;
+  float *logits = nullptr;
+  uint8_t *ws = nullptr;
+  size_t ws_bytes = 0, hid = 0;
+  int32_t *work = nullptr, *status = nullptr;
+  int next = 0;  // the next layer to run
+  cudaEvent_t ev = nullptr;
+};
+
+extern "C" TREE_API int tree_session_create(const tree_plan_t *plan, const void *plan_dev,
+                                            const tree_layer_weights_t *layers, int32_t n_layers, const void *x,
+                                            void *const *k_caches, void *const *v_caches, const float *cos_sin,
+                                            int32_t max_pos, const void *w_final, const void *w_letters,
+                                            int32_t stride, float *logits, void *workspace, size_t workspace_bytes,
+                                            int32_t *work, int32_t *status, tree_session_t **out) {
+  using namespace tree;
+  if (!out) return fail(TREE_ERR_INVALID_ARG, "tree_session_create: NULL out");
+  *out = nullptr;
+  if (!plan || !plan_dev || !layers || n_layers < 1 || !x || !k_caches || !v_caches || !cos_sin || !w_final ||
+      !w_letters || !logits || !workspace)
+    return fail(TREE_ERR_INVALID_ARG, "tree_session_create: NULL argument or n_layers %d", n_layers);
+  int rc = check_weights(&layers[0]);
+  if (rc) return rc;
+  const size_t need = model_bytes(plan->p, layers[0]);
+  if (workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return fail(TREE_ERR_INVALID_ARG, "tree_session_create: workspace of %zu bytes (need %zu, 256-byte aligned)",
+                workspace_bytes, need);
+  auto *s = new tree_session;
+  s->plan = plan;
+  s->plan_dev = plan_dev;
+  s->layers.assign(layers, layers + n_layers);
+  s->kc.assign(k_caches, k_caches + n_layers);
+  s->vc.assign(v_caches, v_caches + n_layers);
+  s->x = x;
+  s->cos_sin = cos_sin;
+  s->max_pos = max_pos;
+  s->w_final = w_final;
+  s->w_letters = w_letters;
+  s->stride = stride;
+  s->logits = logits;
+  s->ws = static_cast<uint8_t *>(workspace);
+  s->ws_bytes = workspace_bytes;
+  s->hid = up256((size_t)(plan->p.n_tot - plan->p.n_res) * layers[0].hidden * 2);
+  s->work = work;
+  s->status = status;
+  const cudaError_t e = cudaEventCreateWithFlags(&s->ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    delete s;
+    return fail(TREE_ERR_CUDA, "tree_session_create: %s", cudaGetErrorString(e));
+  }
+  *out = s;
+  return TREE_OK;
+}
+
+extern "C" TREE_API int tree_session_run(tree_session_t *s, double slice_ms, tree_stream_t stream,
+                                         int32_t *layers_run, int32_t *done) {
+  using namespace tree;
+  if (!s) return fail(TREE_ERR_INVALID_ARG, "tree_session_run: NULL session");
+  const int n = (int)s->layers.size();
+  int ran = 0;
+  const auto t0 = std::chrono::steady_clock::now();
+  void *buf[2] = {s->ws, s->ws + s->hid};
+  uint8_t *inner = s->ws + 2 * s->hid;
+  const size_t inner_bytes = s->ws_bytes - 2 * s->hid;
+  int rc = TREE_OK;
+  while (s->next < n) {
+    const int l = s->next;
+    // layer l reads the input (l = 0) or the buffer layer l - 1 wrote, exactly as in tree_model_fwd
+    const void *cur = l == 0 ? s->x : buf[(l - 1) & 1];
+    if (l + 1 < n)
+      rc = tree_layer_fwd(s->plan, s->plan_dev, &s->layers[l], cur, s->kc[l], s->vc[l], buf[l & 1], s->cos_sin,
+                          s->max_pos, inner, inner_bytes, s->work, s->status, stream);
+    else
+      rc = tree_last_layer_fwd(s->plan, s->plan_dev, &s->layers[l], cur, s->kc[l], s->vc[l], s->cos_sin, s->max_pos,
+                               s->w_final, s->w_letters, s->stride, s->logits, inner, inner_bytes, s->work, s->status,
+                               stream);
+    if (rc) break;
+    ++s->next;
+    ++ran;
+    // the layer's end, then the slice check: yield once the slice is used up
+    cudaError_t e = cudaEventRecord(s->ev, as_stream(stream));
+    if (e == cudaSuccess) e = cudaEventSynchronize(s->ev);
+    if (e != cudaSuccess) {
+      rc = fail(TREE_ERR_CUDA, "tree_session_run: %s", cudaGetErrorString(e));
+      break;
+    }
+    const double ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+    if (ms >= slice_ms) break;
+  }
+  if (layers_run) *layers_run = ran;
+  if (done) *done = s->next >= n ? 1 : 0;
+  return rc;
+}
+
+extern "C" TREE_API int tree_session_destroy(tree_session_t *s) {
+  if (s) {
+    if (s->ev) cudaEventDestroy(s->ev);
+    delete s;
+  }
+  return TREE_OK;
 }

@@ -326,3 +326,77 @@ def test_model_fwd_equals_layer_calls_and_oracle():
     err = np.abs(logits.cpu().numpy().astype(np.float64) - ref).max()
     # each layer contributes the single-layer bound
     assert err <= L * 2e-2 * max(1.0, np.abs(ref).max()), err
+
+
+def test_long_session_slices_equal_model_fwd():
+    """A long request run one layer per slice, with a short batch run between slices, gives the
+    same logits bit for bit as the whole forward in one call; so does the short batch."""
+    import synth
+    dev = torch.device("cuda")
+    hidden, ffn, stride, L = 256, 512, 8, 4
+
+    def setup(wn, seed):
+        w = synth.workload(wn)
+        plan = lib.Plan.from_forest(w.forest, leaf1=w.leaf1, leaf2=w.leaf2, max_fwd=w.max_fwd)
+        i = plan.info
+        n_fwd, n_res = i.n_tot - i.n_res, i.n_res
+        kvd = w.hkv * w.d
+        layers, keep = [], []
+        x = None
+        for l in range(L):
+            wts, x_l, rk, rv = synth.draw_layer(n_fwd, n_res, hidden, w.hq, w.hkv, w.d, ffn, seed + 31 * l)
+            x = x_l if x is None else x
+            td = {k: torch.from_numpy(v).to(dev) for k, v in wts.items()}
+            keep.append(td)
+            layers.append(lib.layer_weights(hidden, w.hq, w.hkv, w.d, ffn, td))
+        wf, wl = synth.draw_head(hidden, stride, seed)
+        pdev = torch.empty(i.dev_bytes, dtype=torch.uint8, device=dev)
+        plan.upload(pdev, i.dev_bytes)
+        tab = torch.from_numpy(lib.rope_table(i.max_pos, w.d, w.theta)).to(dev)
+        env = dict(w=w, plan=plan, i=i, layers=layers, keep=keep, x=torch.from_numpy(x).to(dev), pdev=pdev, tab=tab,
+                   wf=torch.from_numpy(wf).to(dev), wl=torch.from_numpy(wl).to(dev), kvd=kvd, rk=rk, rv=rv)
+        return env
+
+    def buffers(env):
+        i, kvd = env["i"], env["kvd"]
+        kc = [torch.zeros(i.n_tot, kvd, dtype=torch.float16, device=dev) for _ in range(L)]
+        vc = [torch.zeros(i.n_tot, kvd, dtype=torch.float16, device=dev) for _ in range(L)]
+        for t in kc:
+            t[:i.n_res] = torch.from_numpy(env["rk"]).to(dev)
+        for t in vc:
+            t[:i.n_res] = torch.from_numpy(env["rv"]).to(dev)
+        nb = lib.model_workspace_bytes(env["plan"], env["layers"][0])
+        return kc, vc, torch.empty(nb, dtype=torch.uint8, device=dev), nb, torch.empty((i.n_slots, stride), device=dev)
+
+    def whole(env):
+        kc, vc, ws, nb, lg = buffers(env)
+        lib.model_fwd(env["plan"], env["pdev"], env["layers"], env["x"], kc, vc, env["tab"], env["i"].max_pos,
+                      env["wf"], env["wl"], stride, lg, ws, nb)
+        return lg
+
+    long_env = setup(4, 400)    # the 32,768-token row in 4 chunks: the long lane
+    short_env = setup(1, 100)   # the tiny tree: a short batch
+    ref_long, ref_short = whole(long_env), whole(short_env)
+    kc, vc, ws, nb, lg = buffers(long_env)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    sess = lib.Session(long_env["plan"], long_env["pdev"], long_env["layers"], long_env["x"], kc, vc, long_env["tab"],
+                       long_env["i"].max_pos, long_env["wf"], long_env["wl"], stride, lg, ws, nb, status=st)
+    slices, done, shorts = 0, False, []
+    while not done:
+        ran, done = sess.run(0.0)   # a zero slice: yield after every layer
+        assert ran == 1
+        slices += 1
+        shorts.append(whole(short_env))   # a short batch takes the GPU between slices
+    sess.close()
+    torch.cuda.synchronize()
+    assert slices == L and int(st.item()) == 0
+    assert torch.equal(lg, ref_long)
+    for s_ in shorts:
+        assert torch.equal(s_, ref_short)
+    # a long slice runs every layer at once
+    kc, vc, ws, nb, lg2 = buffers(long_env)
+    sess = lib.Session(long_env["plan"], long_env["pdev"], long_env["layers"], long_env["x"], kc, vc, long_env["tab"],
+                       long_env["i"].max_pos, long_env["wf"], long_env["wl"], stride, lg2, ws, nb)
+    assert sess.run(1e9) == (L, True)
+    sess.close()
+    assert torch.equal(lg2, ref_long)
