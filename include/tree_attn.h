@@ -108,6 +108,11 @@ typedef struct {
   int32_t max_fwd;   /* tokens per forward chunk, multiple of 128 [8192] */
   int32_t max_depth; /* blocks on a root-to-leaf path [8] */
   int32_t max_row;   /* tokens in one tree [32768] */
+  int32_t tiling;    /* key tiles of the attention: 0 = 128 consecutive packed keys [0];
+                        1 = by position: each query sees its keys in tiles of 128 positions of
+                        its own prompt (key at position p in slot p % 128, tiles in increasing
+                        position), so its result does not depend on the other prompts of the
+                        batch ("05 / Reproducibility": attention tiled by position) */
 } tree_plan_opts_t;
 
 typedef struct tree_plan tree_plan_t;
@@ -152,6 +157,8 @@ typedef struct {
   /* byte offsets of the device image's arrays (int32 each) */
   size_t off_pos, off_send, off_qtile, off_ent, off_order, off_chunk, off_slot_tok, off_r1, off_r2;
   size_t off_runs;       /* run tables of the key tiles (see tree_plan_host_view_t.runs) */
+  int32_t tiling;        /* as in tree_plan_opts_t */
+  size_t off_vkeys, off_vruns; /* tiling 1: per entry its 128 gathered keys and its run table */
 } tree_plan_info_t;
 
 TREE_API int tree_plan_query(const tree_plan_t *plan, tree_plan_info_t *info);
@@ -188,6 +195,14 @@ typedef struct {
                            send, words 20 + 4r .. 23 + 4r its keys as a 128-bit mask (key c of the
                            tile is bit c % 32 of word c / 32); all else 0.  A query i sees the keys
                            of run r, apart from keys after i, iff i < send of r. */
+  /* tiling 1 only (else NULL).  Entry e of the tile lists (ent[e] = (e << 1) | 1) is a virtual
+     key tile: vkeys[128 e + c] = the packed key in slot c (0 for an empty slot, which no query
+     sees); vruns[72 e ..]: word 0 the number of runs n (<= 16), words 4-7 the 128-bit mask of
+     the query tile's rows that take their keys of this position range from this entry, then per
+     run r words 8 + 4r .. 11 + 4r = {first slot c0, last slot c1, packed key j0 in c0, its send}:
+     the run's slots hold the consecutive keys j0 + (c - c0) of one block.  Query i of an
+     assigned row sees slot c of run r iff c - c0 <= i - j0 and j0 <= i < send. */
+  const int32_t *vkeys, *vruns;
 } tree_plan_host_view_t;
 
 TREE_API int tree_plan_tables(const tree_plan_t *plan, tree_plan_host_view_t *view);

@@ -102,7 +102,7 @@ class LayerWeights(C.Structure):
 
 
 class _Opts(C.Structure):
-    _fields_ = [("max_fwd", C.c_int32), ("max_depth", C.c_int32), ("max_row", C.c_int32)]
+    _fields_ = [("max_fwd", C.c_int32), ("max_depth", C.c_int32), ("max_row", C.c_int32), ("tiling", C.c_int32)]
 
 
 class PlanInfo(C.Structure):
@@ -111,7 +111,8 @@ class PlanInfo(C.Structure):
         "n_entries", "n_slots", "n_questions", "max_fwd", "bm", "bn", "max_pos")] + [
         ("pairs", C.c_int64), ("dev_bytes", C.c_size_t)] + [(n, C.c_size_t) for n in (
         "off_pos", "off_send", "off_qtile", "off_ent", "off_order", "off_chunk", "off_slot_tok",
-        "off_r1", "off_r2", "off_runs")]
+        "off_r1", "off_r2", "off_runs")] + [("tiling", C.c_int32), ("off_vkeys", C.c_size_t),
+                                            ("off_vruns", C.c_size_t)]
 
 
 class ChunkInfo(C.Structure):
@@ -127,7 +128,7 @@ _VIEW_FIELDS = ("block_map", "blk_start", "blk_len", "blk_parent", "blk_depth", 
 
 class _View(C.Structure):
     _fields_ = [(n, _i32p) for n in _VIEW_FIELDS] + [("image", C.c_void_p), ("image_bytes", C.c_size_t),
-                                                     ("runs", _i32p)]
+                                                     ("runs", _i32p), ("vkeys", _i32p), ("vruns", _i32p)]
 
 
 class AttnParams(C.Structure):
@@ -232,7 +233,7 @@ class Spec:
     """A batch's forest as the planner reads it (arrays kept alive, struct built once)."""
 
     def __init__(self, parent, length, key=None, resident=None, leaf1=None, leaf2=None,
-                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0):
+                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0, tiling: int = 0):
         self._keep = []
         par = np.ascontiguousarray(parent, np.int32)
         ln = np.ascontiguousarray(length, np.int32)
@@ -256,7 +257,7 @@ class Spec:
             self.spec.leaf1 = l1.ctypes.data_as(_i32p)
             self.spec.leaf2 = l2.ctypes.data_as(_i32p)
             self._keep += [l1, l2]
-        self.opts = _Opts(max_fwd, max_depth, max_row)
+        self.opts = _Opts(max_fwd, max_depth, max_row, tiling)
 
     @classmethod
     def from_forest(cls, forest, **kw):
@@ -478,7 +479,7 @@ class Plan:
     """A packed batch: owns the library's host plan (``tree_pack_plan``)."""
 
     def __init__(self, parent, length, key=None, resident=None, leaf1=None, leaf2=None,
-                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0):
+                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0, tiling: int = 0):
         self._keep = []
         par = np.ascontiguousarray(parent, np.int32)
         ln = np.ascontiguousarray(length, np.int32)
@@ -502,7 +503,7 @@ class Plan:
             spec.leaf1 = l1.ctypes.data_as(_i32p)
             spec.leaf2 = l2.ctypes.data_as(_i32p)
             self._keep += [l1, l2]
-        opts = _Opts(max_fwd, max_depth, max_row)
+        opts = _Opts(max_fwd, max_depth, max_row, tiling)
         h = _vp()
         _check(_lib.tree_pack_plan(C.byref(spec), C.byref(opts), C.byref(h)))
         self._keep = []
@@ -548,6 +549,9 @@ class Plan:
         out["image"] = np.ctypeslib.as_array(C.cast(v.image, C.POINTER(C.c_uint8)),
                                              shape=(v.image_bytes,)).copy()
         out["runs"] = np.ctypeslib.as_array(v.runs, shape=(n_kvt, 84)).copy()
+        if i.tiling == 1 and i.n_entries > 0:
+            out["vkeys"] = np.ctypeslib.as_array(v.vkeys, shape=(i.n_entries, 128)).copy()
+            out["vruns"] = np.ctypeslib.as_array(v.vruns, shape=(i.n_entries, 72)).copy()
         return out
 
     def upload(self, dev_buf, nbytes: int, stream=None):

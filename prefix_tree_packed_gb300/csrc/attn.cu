@@ -60,6 +60,7 @@ constexpr uint64_t kSelfTestNs = 2000000ull;
 struct AttnArgs {
   const int32_t *send;
   const int32_t *runs;  // run tables of the key tiles
+  const int32_t *vkeys, *vruns;  // tiling by position: each entry's gathered keys and run table
   const QTile *qtiles;
   const int32_t *ent;
   const int32_t *order;
@@ -183,7 +184,7 @@ TREE_DEV Item item_at(const AttnArgs &a, int w) {
 // every barrier phase follows that count (or the item count for per-item
 // barriers), so the producer and MMA warps run ahead into the next item while
 // the softmax warps finish the current one.
-template <int D, int NH>
+template <int D, int NH, bool G>
 __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     tree_attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo, const AttnArgs a) {
@@ -259,7 +260,9 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   };
 
   if (warp >= 4 * NH) {
-    if (NH == 2) regs_dec<C::SERVICE_REGS>();
+    // (the position-tiled kernels keep the launch budget: with the split, their gathering
+    // producer at d = 128 gave wrong tiles; both groups skip it, so the budget stays balanced)
+    if (NH == 2 && !G) regs_dec<C::SERVICE_REGS>();
     if (warp == C::PROD_WARP) {
       // ---------------------------------------------------------- producer (whole warp, one lane issues)
       if (elect_one()) {
@@ -329,6 +332,29 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         for (int i = 0; i < it.n; ++i, ++t) {
           const int st = t % C::STAGES;
           if (t >= C::STAGES && !(ok = wait_bar_warp(b_e(st), ((t / C::STAGES) - 1) & 1, abort, a.status))) break;
+          if (G) {
+            // tiling by position: the entry's 128 keys gathered row by row (lane l
+            // loads slots 4l .. 4l + 3), its run table with the keys
+            const int e = __ldg(a.ent + it.qt.ent0 + i) >> 1;
+            const int4 rows = __ldg(reinterpret_cast<const int4 *>(a.vkeys + (size_t)e * BN) + lane);
+            const uint32_t v_bar = C::KV_ONE ? b_k(st) : b_v(st);
+            if (lane == 0) {
+              mbar_expect_tx(b_k(st), (C::KV_ONE ? 2 : 1) * C::CB * BOX_BYTES + kVRunWords * 4);
+              bulk_load(s_base + C::RUNS_OFF + st * 512, a.vruns + (size_t)e * kVRunWords, kVRunWords * 4, b_k(st));
+              if (!C::KV_ONE) mbar_expect_tx(v_bar, C::CB * BOX_BYTES);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < C::CB; ++c)
+              tma_gather4(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mk, it.g * D + 64 * c,
+                          rows, b_k(st));
+#pragma unroll
+            for (int c = 0; c < C::CB; ++c)
+              tma_gather4(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mv, it.g * D + 64 * c,
+                          rows, v_bar);
+            __syncwarp();
+            continue;
+          }
           const int j0 = (__ldg(a.ent + it.qt.ent0 + i) >> 1) * BN;
           if (elect_one()) {
             // with three stages K, the keys' subtree ends and V complete one
@@ -502,7 +528,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    if (NH == 2) regs_inc<C::SOFTMAX_REGS>();
+    if (NH == 2 && !G) regs_inc<C::SOFTMAX_REGS>();
     const int h = warp >> 2;
     const int r = 32 * (warp & 3) + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -607,7 +633,31 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           if (h == 1 && !(ok = wait_bar_warp(other_turn, T & 1, abort, a.status))) break;
           if (h == 0 && T > 0 && !(ok = wait_bar_warp(other_turn, (T - 1) & 1, abort, a.status))) break;
         }
-        if (e & 1) {
+        if (G) {
+          // tiling by position: rows not assigned to this entry take nothing from it;
+          // an assigned row sees slot c of run r iff c - c0 <= iq - j0 and j0 <= iq < send
+          const int32_t *tb = sRuns + st * 128;
+          uint32_t mw[4] = {0u, 0u, 0u, 0u};
+          if ((tb[4 + (r >> 5)] >> (r & 31)) & 1) {
+            const int R = tb[0];
+#pragma unroll
+            for (int rr = 0; rr < kMaxRuns; ++rr) {
+              if (rr >= R) break;
+              const int4 run = reinterpret_cast<const int4 *>(tb + 8)[rr];  // c0, c1, j0, send
+              if (iq >= run.z && iq < run.w) {
+                const int lo = run.x, hi = min(run.y, run.x + (iq - run.z));
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  const int a0 = max(lo, 32 * q4) - 32 * q4, a1 = min(hi, 32 * q4 + 31) - 32 * q4;
+                  if (a0 <= a1) mw[q4] |= (0xffffffffu >> (31 - (a1 - a0))) << a0;
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            s[c] = (mw[c >> 5] & (1u << (c & 31))) ? s[c] : __float_as_uint(-INFINITY);
+        } else if (e & 1) {
           // partial tile: key j = j0 + c is visible iff j <= iq < send[j].  The
           // row's 128-bit mask (the runs of the tile that end after the query,
           // cut at the query's own column), then one bit test per score.
@@ -748,24 +798,27 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
               float *lse, int hq, int hkv, float scale, int32_t *work, int32_t self_test, int32_t *status,
               cudaStream_t s) {
   using C = Cfg<D, NH>;
-  static bool attr_set = false;
-  auto kern = tree_attn_tc<D, NH>;
-  if (!attr_set) {
+  static bool attr_set[2] = {false, false};
+  const bool gather = P.tiling == 1;
+  auto kern = gather ? tree_attn_tc<D, NH, true> : tree_attn_tc<D, NH, false>;
+  if (!attr_set[gather]) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd: %s", cudaGetErrorString(e));
-    attr_set = true;
+    attr_set[gather] = true;
   }
   const int32_t q0 = P.chunk_q0[chunk], nq = P.chunk_q1[chunk] - q0;
   CUtensorMap mq, mk, mv, mo;
   int rc;
   if ((rc = make_map(&mq, q, (int64_t)hq * D, nq, "tree_attn_fwd")) ||
-      (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
-      (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
+      (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", gather ? 1 : 128)) ||
+      (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", gather ? 1 : 128)) ||
       (rc = make_map(&mo, o, (int64_t)hq * D, nq, "tree_attn_fwd")))
     return rc;
   AttnArgs a;
   a.send = img + P.off_send;
   a.runs = img + P.off_runs;
+  a.vkeys = img + P.off_vkeys;
+  a.vruns = img + P.off_vruns;
   a.qtiles = reinterpret_cast<const QTile *>(img + P.off_qtile);
   a.ent = img + P.off_ent;
   a.order = img + P.off_order;

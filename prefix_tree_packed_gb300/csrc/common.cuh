@@ -27,10 +27,11 @@ inline cudaStream_t as_stream(tree_stream_t s) { return reinterpret_cast<cudaStr
 // Number of SMs of the current device (cached per process; GB300 has 152).
 int sm_count();
 
-// 2-D TMA map over a row-major [rows, cols] f16 matrix: 128-row x 64-column
-// boxes (128-byte rows), 128-byte swizzle, zero fill outside the matrix.
-// `who` names the caller in error messages.
-int make_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, const char *who);
+// 2-D TMA map over a row-major [rows, cols] f16 matrix: box_rows x 64-column
+// boxes (128-byte rows), 128-byte swizzle, zero fill outside the matrix
+// (box_rows 1: the map of tile::gather4 loads).  `who` names the caller in
+// error messages.
+int make_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, const char *who, int box_rows = 128);
 
 // Launch `kernel` on `s` allowed to start while the stream's previous kernel is
 // still running (programmatic dependent launch): the kernel must execute

@@ -33,12 +33,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-int make_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, const char *who) {
+int make_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, const char *who, int box_rows) {
   auto enc = encode_fn();
   if (!enc) return fail(TREE_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", who);
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

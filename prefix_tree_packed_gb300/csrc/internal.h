@@ -31,6 +31,10 @@ struct Plan {
   std::vector<int32_t> image;
   size_t off_pos = 0, off_send = 0, off_qtile = 0, off_ent = 0, off_order = 0, off_chunk = 0,
          off_slot_tok = 0, off_r1 = 0, off_r2 = 0, off_runs = 0;  // in int32 words
+  // tiling by position: per entry its gathered keys and run table (see tree_plan_host_view_t)
+  int32_t tiling = 0;
+  std::vector<int32_t> vkeys, vruns;
+  size_t off_vkeys = 0, off_vruns = 0;
 };
 
 // Run table of a 128-key tile, in the device image (kRunWords int32 words per
@@ -43,6 +47,9 @@ struct Plan {
 //   words 20-83   bits[kMaxRuns][4]: key c of the tile is bit c%32 of word c/32
 constexpr int kMaxRuns = 16;
 constexpr int kRunWords = 84;  // 336 bytes, a multiple of 16
+// Run table of a virtual key tile (tiling by position): word 0 n, words 4-7 the
+// assigned query rows, words 8 + 4r .. 11 + 4r run r = {c0, c1, j0, send}.
+constexpr int kVRunWords = 72;  // 288 bytes
 
 // Device image record for one query tile (off_qtile points at an array of these).
 struct QTile {

@@ -46,10 +46,11 @@ constexpr int32_t kTile = 128;
 
 size_t align4(size_t words) { return (words + 3) & ~size_t(3); }
 
-int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_row, Plan &P) {
+int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_row, int32_t tiling, Plan &P) {
   const int32_t nb = s.n_blocks;
   P.n_input_blocks = nb;
   P.max_fwd = max_fwd;
+  P.tiling = tiling;
   // ---- validation of the input forest
   for (int32_t b = 0; b < nb; ++b) {
     const int32_t p = s.parent[b];
@@ -252,6 +253,78 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   }
   if (P.n_tot % kTile) kt_min[n_kvt - 1] = 0;
 
+  // ---- tiling by position: virtual key tiles.  For a query tile [i0, i1) and
+  // position range t ([128t, 128t + 128)), every row takes the keys of its own
+  // prompt in that range from exactly one entry, key at position p in slot
+  // p % 128; entries follow in increasing t.  An entry gathers the keys of the
+  // chain root -> d, d the deepest block of some row's chain that reaches into
+  // the range; rows whose own such block is an ancestor of d ride along (their
+  // keys of the range are a prefix of the entry's, in the same slots, and the
+  // entry's other keys belong to blocks that are not their ancestors: not
+  // visible to them).
+  auto is_anc_or_self = [&](int32_t b, int32_t d) {
+    for (int32_t x = d; x >= 0; x = P.blk_parent[x])
+      if (x == b) return true;
+    return false;
+  };
+  auto add_position_tiles = [&](int32_t i0, int32_t i1) {
+    std::vector<int32_t> tb;  // blocks with rows in the tile, packed order
+    for (int32_t b = block_of(i0); b < nbc && bstart[b] < i1; ++b)
+      if (bstart[b] + blen[b] > i0) tb.push_back(b);
+    auto pos_max = [&](int32_t b) { return bpos0[b] + (std::min(i1, bstart[b] + blen[b]) - 1 - bstart[b]); };
+    int32_t tmax = 0;
+    for (int32_t b : tb) tmax = std::max(tmax, pos_max(b) / kTile);
+    std::vector<std::pair<int32_t, int32_t>> made;  // (entry, block) of this t
+    for (int32_t t = 0; t <= tmax; ++t) {
+      made.clear();
+      for (size_t k = tb.size(); k-- > 0;) {
+        const int32_t b = tb[k];
+        if (pos_max(b) < t * kTile) continue;  // its rows see no key in this range
+        // the deepest block of b's chain that reaches into the range: the keys of the
+        // range on b's chain are those of the chain root -> db
+        int32_t db = b;
+        while (bpos0[db] >= (t + 1) * kTile) db = P.blk_parent[db];
+        int32_t e = -1;
+        for (const auto &m : made)
+          if (is_anc_or_self(db, m.second)) {
+            e = m.first;
+            break;
+          }
+        if (e < 0) {
+          e = (int32_t)P.ent.size();
+          P.ent.push_back((e << 1) | 1);
+          const size_t kb = P.vkeys.size(), rb = P.vruns.size();
+          P.vkeys.resize(kb + kTile, 0);
+          P.vruns.resize(rb + kVRunWords, 0);
+          // the chain root -> db, root first
+          int32_t chain[64], nch = 0;
+          for (int32_t x = db; x >= 0 && nch < 64; x = P.blk_parent[x]) chain[nch++] = x;
+          int32_t n = 0;
+          for (int32_t c = nch; c-- > 0;) {
+            const int32_t blk = chain[c];
+            const int32_t lo = std::max(bpos0[blk], t * kTile), hi = std::min(bpos0[blk] + blen[blk], (t + 1) * kTile);
+            if (lo >= hi) continue;
+            const int32_t c0 = lo - t * kTile, c1 = hi - 1 - t * kTile, j0 = bstart[blk] + (lo - bpos0[blk]);
+            for (int32_t q = c0; q <= c1; ++q) P.vkeys[kb + q] = j0 + (q - c0);
+            int32_t *run = P.vruns.data() + rb + 8 + 4 * n;
+            run[0] = c0;
+            run[1] = c1;
+            run[2] = j0;
+            run[3] = bsend[blk];
+            ++n;
+          }
+          P.vruns[rb] = n;  // at most the depth of the tree (<= max_depth <= 16)
+          made.emplace_back(e, db);
+        }
+        // the rows of b at positions >= 128 t take this range from entry e
+        int32_t *rows = P.vruns.data() + (size_t)e * kVRunWords + 4;
+        const int32_t r_lo = std::max(i0, bstart[b]), r_hi = std::min(i1, bstart[b] + blen[b]);
+        const int32_t first = std::max(r_lo, bstart[b] + (t * kTile - bpos0[b]));
+        for (int32_t i = first; i < r_hi; ++i) rows[(i - i0) >> 5] |= (int32_t)(1u << ((i - i0) & 31));
+      }
+    }
+  };
+
   // ---- chunks, query tiles, tile lists
   const int32_t n_fwd = P.n_tot - P.n_res;
   P.n_chunks = (n_fwd + max_fwd - 1) / max_fwd;
@@ -275,6 +348,11 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
       P.qt_row0.push_back(i0);
       P.qt_row1.push_back(i1);
       P.qt_ent0.push_back((int32_t)P.ent.size());
+      if (tiling == 1) {
+        add_position_tiles(i0, i1);
+        P.qt_ent1.push_back((int32_t)P.ent.size());
+        continue;
+      }
       const int32_t last = (i1 - 1) / kTile;
       for (int32_t kt = 0; kt <= last; ++kt) {
         const int32_t j0 = kt * kTile, j1 = j0 + kTile;
@@ -348,6 +426,10 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   w = align4(w + P.r2.size());
   P.off_runs = w;
   w = align4(w + (size_t)n_kvt * kRunWords);
+  P.off_vkeys = w;
+  w = align4(w + P.vkeys.size());
+  P.off_vruns = w;
+  w = align4(w + P.vruns.size());
   P.image.resize(w);
   int32_t *im = P.image.data();
   std::fill(im, im + 16, 0);
@@ -413,7 +495,11 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   zero_gap(P.off_slot_tok + P.slot_tok.size(), P.off_r1);
   zero_gap(P.off_r1 + P.r1.size(), P.off_r2);
   zero_gap(P.off_r2 + P.r2.size(), P.off_runs);
-  zero_gap(P.off_runs + (size_t)n_kvt * kRunWords, w);
+  std::copy(P.vkeys.begin(), P.vkeys.end(), im + P.off_vkeys);
+  std::copy(P.vruns.begin(), P.vruns.end(), im + P.off_vruns);
+  zero_gap(P.off_runs + (size_t)n_kvt * kRunWords, P.off_vkeys);
+  zero_gap(P.off_vkeys + P.vkeys.size(), P.off_vruns);
+  zero_gap(P.off_vruns + P.vruns.size(), w);
   return TREE_OK;
 }
 
@@ -433,18 +519,22 @@ int tree_pack_plan(const tree_spec_t *spec, const tree_plan_opts_t *opts, tree_p
     return tree::fail(TREE_ERR_INVALID_ARG, "tree_pack_plan: empty forest or NULL parent/length");
   if (spec->n_questions < 0 || (spec->n_questions > 0 && (!spec->leaf1 || !spec->leaf2)))
     return tree::fail(TREE_ERR_INVALID_ARG, "tree_pack_plan: bad question arrays");
-  int32_t max_fwd = 8192, max_depth = 8, max_row = 32768;
+  int32_t max_fwd = 8192, max_depth = 8, max_row = 32768, tiling = 0;
   if (opts) {
     if (opts->max_fwd) max_fwd = opts->max_fwd;
     if (opts->max_depth) max_depth = opts->max_depth;
     if (opts->max_row) max_row = opts->max_row;
+    tiling = opts->tiling;
   }
   if (max_fwd <= 0 || max_fwd % 128 != 0)
     return tree::fail(TREE_ERR_UNSUPPORTED, "max_fwd %d is not a positive multiple of 128", max_fwd);
   if (max_depth <= 0 || max_row <= 0) return tree::fail(TREE_ERR_INVALID_ARG, "bad limits");
+  if (tiling != 0 && tiling != 1) return tree::fail(TREE_ERR_INVALID_ARG, "tiling %d is neither 0 nor 1", tiling);
+  if (tiling == 1 && max_depth > tree::kMaxRuns)
+    return tree::fail(TREE_ERR_UNSUPPORTED, "tiling by position needs max_depth <= %d", tree::kMaxRuns);
   auto *pl = new (std::nothrow) tree_plan;
   if (!pl) return tree::fail(TREE_ERR_INVALID_ARG, "out of host memory");
-  const int rc = tree::build(*spec, max_fwd, max_depth, max_row, pl->p);
+  const int rc = tree::build(*spec, max_fwd, max_depth, max_row, tiling, pl->p);
   if (rc != TREE_OK) {
     delete pl;
     return rc;
@@ -488,6 +578,9 @@ int tree_plan_query(const tree_plan_t *plan, tree_plan_info_t *info) {
   info->off_r1 = P.off_r1 * 4;
   info->off_r2 = P.off_r2 * 4;
   info->off_runs = P.off_runs * 4;
+  info->tiling = P.tiling;
+  info->off_vkeys = P.off_vkeys * 4;
+  info->off_vruns = P.off_vruns * 4;
   return TREE_OK;
 }
 
@@ -520,6 +613,8 @@ int tree_plan_tables(const tree_plan_t *plan, tree_plan_host_view_t *v) {
   v->pos = P.image.data() + P.off_pos;
   v->send = P.image.data() + P.off_send;
   v->runs = P.image.data() + P.off_runs;
+  v->vkeys = P.tiling == 1 ? P.image.data() + P.off_vkeys : nullptr;
+  v->vruns = P.tiling == 1 ? P.image.data() + P.off_vruns : nullptr;
   v->chunk_q0 = P.chunk_q0.data();
   v->chunk_q1 = P.chunk_q1.data();
   v->chunk_t0 = P.chunk_t0.data();

@@ -71,6 +71,15 @@ TREE_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, ui
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// Rows y.x, y.y, y.z, y.w (columns x .. x + box width) of a 2-D map whose box is
+// one row high, written as four consecutive rows at dst (tile::gather4).
+TREE_DEV void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int4 y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y.x), "r"(y.y), "r"(y.z), "r"(y.w), "r"(bar)
+      : "memory");
+}
 TREE_DEV void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)

@@ -214,3 +214,92 @@ def test_rope_table_matches_double_precision(lib):
     np.testing.assert_array_max_ulp(tab[..., 1], np.sin(a).astype(np.float32), maxulp=1)
     with pytest.raises(lib.TreeError):
         lib.rope_table(0, 64, 1e4)
+
+
+# ---------------------------------------------------------------- tiling by position
+
+def _position_tiles_of(plan, t_):
+    """Per forward row: list of (entry order, position tile, {slot: key}) the row takes its keys from."""
+    i = plan.info
+    out = {}
+    vk, vr = t_["vkeys"], t_["vruns"]
+    for q in range(i.n_qtiles):
+        r0, r1 = int(t_["qt_row0"][q]), int(t_["qt_row1"][q])
+        for k, e in enumerate(range(int(t_["qt_ent0"][q]), int(t_["qt_ent1"][q]))):
+            assert t_["ent"][e] == (e << 1) | 1
+            run = vr[e]
+            n = int(run[0])
+            rows = run[4:8].astype(np.uint32)
+            for row in range(r1 - r0):
+                if not (rows[row >> 5] >> (row & 31)) & 1:
+                    continue
+                iq = r0 + row
+                seen = {}
+                for rr in range(n):
+                    c0, c1, j0, se = (int(x) for x in run[8 + 4 * rr: 12 + 4 * rr])
+                    assert (vk[e][c0:c1 + 1] == np.arange(j0, j0 + c1 - c0 + 1)).all()
+                    if not (j0 <= iq < se):
+                        continue
+                    for c in range(c0, min(c1, c0 + iq - j0) + 1):
+                        assert c not in seen
+                        seen[c] = j0 + c - c0
+                out.setdefault(iq, []).append((k, seen))
+    return out
+
+
+def _check_position_tiling(plan, mask):
+    t_ = plan.tables()
+    i = plan.info
+    pos = t_["pos"]
+    per_row = _position_tiles_of(plan, t_)
+    for iq in range(i.n_res, i.n_tot):
+        got = {}
+        tiles = []
+        for k, seen in per_row.get(iq, []):
+            if not seen:
+                continue
+            ts = {int(pos[j]) // 128 for j in seen.values()}
+            assert len(ts) == 1               # one position range per entry
+            t = ts.pop()
+            tiles.append(t)
+            for c, j in seen.items():
+                assert c == int(pos[j]) % 128  # key at position p in slot p % 128
+                assert j not in got            # each key once
+                got[j] = c
+        assert tiles == sorted(tiles) and len(set(tiles)) == len(tiles)
+        want = set(np.nonzero(mask[iq])[0].tolist())
+        assert set(got) == want, iq
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_position_tiling_random_forests(lib, seed):
+    rng = np.random.default_rng(900 + seed)
+    f = synth.random_forest(rng, n_roots=int(rng.integers(1, 4)), max_blocks=int(rng.integers(4, 40)),
+                            max_len=[3, 9, 60, 200][seed % 4], resident_root=bool(seed % 2))
+    try:
+        ref, _ = oplan.plan_forest(f, max_fwd=8192)
+    except oplan.PlanError:
+        pytest.skip("forest has no forward tokens")
+    plan = lib.Plan.from_forest(f, max_fwd=8192, tiling=1)
+    assert plan.info.tiling == 1
+    # same packing as the packed tiling
+    t0 = lib.Plan.from_forest(f, max_fwd=8192).tables()
+    np.testing.assert_array_equal(plan.tables()["pos"], t0["pos"])
+    _check_position_tiling(plan, oplan.brute_mask(ref))
+
+
+def test_position_tiling_workload1_and_alone_equals_packed(lib):
+    w = synth.workload(1)
+    ref, _ = oplan.plan_forest(w.forest, max_fwd=w.max_fwd)
+    plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, tiling=1)
+    _check_position_tiling(plan, oplan.brute_mask(ref))
+    # one prompt alone: the position tiles are the packed tiles (packed index = position)
+    alone = lib.Plan([-1, 0], [200, 90], tiling=1)
+    t_ = alone.tables()
+    assert alone.info.n_entries == lib.Plan([-1, 0], [200, 90]).info.n_entries
+    for e in range(alone.info.n_entries):
+        run = t_["vruns"][e]
+        assert run[0] >= 1
+    assert lib.Plan([-1], [10], tiling=1).info.n_entries == 1
+    with pytest.raises(lib.TreeError):
+        lib.Plan([-1], [10], tiling=2)

@@ -38,10 +38,10 @@ def _dev(x):
 class Run:
     """A plan on the device plus helpers to call the library."""
 
-    def __init__(self, lib, forest, max_fwd=8192, leaf1=None, leaf2=None):
+    def __init__(self, lib, forest, max_fwd=8192, leaf1=None, leaf2=None, tiling=0):
         self.lib = lib
         kw = dict(leaf1=leaf1, leaf2=leaf2) if leaf1 is not None else {}
-        self.plan = lib.Plan.from_forest(forest, max_fwd=max_fwd, **kw)
+        self.plan = lib.Plan.from_forest(forest, max_fwd=max_fwd, tiling=tiling, **kw)
         self.oplan, self.oq = oplan.plan_forest(forest, max_fwd=max_fwd, **kw)
         i = self.plan.info
         self.dev = torch.empty(i.dev_bytes, dtype=torch.uint8, device="cuda")
@@ -211,8 +211,8 @@ def test_rope_keys_only(lib):
 # ---------------------------------------------------------------- attention
 
 def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per_chunk=48, lse=True,
-                dynamic=True):
-    r = Run(lib, forest, max_fwd)
+                dynamic=True, tiling=0):
+    r = Run(lib, forest, max_fwd, tiling=tiling)
     work = torch.zeros(2, dtype=torch.int32, device="cuda") if dynamic else None
     p = r.oplan
     q, k, v = synth.draw_qkv(p.n_fwd, p.n_tot, hq, hkv, d, seed)
@@ -256,15 +256,17 @@ def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per
     return got
 
 
+@pytest.mark.parametrize("tiling", [0, 1])
 @pytest.mark.parametrize("n", [1, 2, 3, 5])
-def test_attention_workloads_full(lib, n):
+def test_attention_workloads_full(lib, n, tiling):
     w = synth.workload(n)
-    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=True)
+    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=True, tiling=tiling)
 
 
-def test_attention_long_row_four_chunks_sampled(lib):
+@pytest.mark.parametrize("tiling", [0, 1])
+def test_attention_long_row_four_chunks_sampled(lib, tiling):
     w = synth.workload(4)
-    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=False, rows_per_chunk=40)
+    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=False, rows_per_chunk=40, tiling=tiling)
 
 
 @pytest.mark.parametrize("seed", range(8))
@@ -277,7 +279,8 @@ def test_attention_random_forests(lib, seed):
     except oplan.PlanError:
         pytest.skip("forest has no forward tokens")
     hq, hkv, d = [(4, 4, 64), (8, 2, 128), (4, 1, 64), (6, 3, 128)][seed % 4]
-    _attn_check(lib, f, hq, hkv, d, seed, max_fwd=int(rng.choice([128, 256, 8192])), dynamic=bool(seed % 2))
+    _attn_check(lib, f, hq, hkv, d, seed, max_fwd=int(rng.choice([128, 256, 8192])), dynamic=bool(seed % 2),
+                tiling=seed // 4)
 
 
 @pytest.mark.parametrize("n", [2, 5])
