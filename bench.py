@@ -119,12 +119,12 @@ class Batch:
     plan buffers alternating so that the host plans step s+1 while the GPU runs step s.
     """
 
-    def __init__(self, lib, torch, w: synth.Workload, dev, n_sets=N_SETS):
+    def __init__(self, lib, torch, w: synth.Workload, dev, n_sets=N_SETS, tiling=0):
         self.lib, self.torch, self.w, self.dev = lib, torch, w, dev
         kw = dict(leaf1=w.leaf1, leaf2=w.leaf2) if w.leaf1 is not None else {}
         self.kw = kw
-        self.spec = lib.Spec.from_forest(w.forest, max_fwd=w.max_fwd, **kw)
-        self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, **kw)
+        self.spec = lib.Spec.from_forest(w.forest, max_fwd=w.max_fwd, tiling=tiling, **kw)
+        self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, tiling=tiling, **kw)
         i = self.plan.info
         self.info = i
         self.rt = lib.Runtime(i.dev_bytes + 4096, max(i.n_chunks, 1))
@@ -444,9 +444,9 @@ def run_only(args):
                     achieved=round(gbs, 1), unit="GB/s", peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4))
     else:
         w = synth.workload(args.workload)
-        B = Batch(lib, torch, w, dev, n_sets=args.sets or N_SETS)
+        B = Batch(lib, torch, w, dev, n_sets=args.sets or N_SETS, tiling=args.tiling)
         B.plan.upload(B.pdev, B.info.dev_bytes, stream)
-        line.update(workload=w.name, sets=len(B.sets))
+        line.update(workload=w.name, sets=len(B.sets), tiling=args.tiling)
         if args.only == "layer":
             r = measure_layer(lib, torch, w, dev, stream, args.steps, args.warmup)
             tf = r["flops"] / (r["ms"] / 1e3) / 1e12
@@ -755,6 +755,8 @@ def main():
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets for --only (0: default)")
     ap.add_argument("--questions", type=int, default=65536, help="questions for --only readout")
     ap.add_argument("--keys-only", action="store_true", help="--only rope: rotate the keys alone")
+    ap.add_argument("--tiling", type=int, default=0, choices=[0, 1],
+                    help="--only attn: key tiles of 128 packed keys (0) or by position (1, batch-invariant)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

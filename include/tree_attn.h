@@ -195,8 +195,10 @@ typedef struct {
                            send, words 20 + 4r .. 23 + 4r its keys as a 128-bit mask (key c of the
                            tile is bit c % 32 of word c / 32); all else 0.  A query i sees the keys
                            of run r, apart from keys after i, iff i < send of r. */
-  /* tiling 1 only (else NULL).  Entry e of the tile lists (ent[e] = (e << 1) | 1) is a virtual
-     key tile: vkeys[128 e + c] = the packed key in slot c (0 for an empty slot, which no query
+  /* tiling 1 only (else NULL).  Entry e of the tile lists is a virtual key tile.  ent[e] =
+     (e << 2) | contiguous << 1 | 1 (contiguous: its slots hold the consecutive packed keys
+     vkeys[128 e] + c), or (j0 << 2) | 2 when every row of the query tile takes this range from it
+     and sees every slot, slot c holding key j0 + c (no mask: a packed key tile).  Per entry: vkeys[128 e + c] = the packed key in slot c (0 for an empty slot, which no query
      sees); vruns[72 e ..]: word 0 the number of runs n (<= 16), words 4-7 the 128-bit mask of
      the query tile's rows that take their keys of this position range from this entry, then per
      run r words 8 + 4r .. 11 + 4r = {first slot c0, last slot c1, packed key j0 in c0, its send}:

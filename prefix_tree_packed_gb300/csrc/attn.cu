@@ -187,7 +187,8 @@ TREE_DEV Item item_at(const AttnArgs &a, int w) {
 template <int D, int NH, bool G>
 __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     tree_attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                 const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo, const AttnArgs a) {
+                 const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
+                 const __grid_constant__ CUtensorMap mkg, const __grid_constant__ CUtensorMap mvg, const AttnArgs a) {
   using C = Cfg<D, NH>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
@@ -269,6 +270,10 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         prefetch_map(&mq);
         prefetch_map(&mk);
         prefetch_map(&mv);
+        if (G) {
+          prefetch_map(&mkg);
+          prefetch_map(&mvg);
+        }
       }
       __syncwarp();
       // Q, K, V may come from the kernel before this one in the stream (RoPE):
@@ -333,10 +338,29 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           const int st = t % C::STAGES;
           if (t >= C::STAGES && !(ok = wait_bar_warp(b_e(st), ((t / C::STAGES) - 1) & 1, abort, a.status))) break;
           if (G) {
-            // tiling by position: the entry's 128 keys gathered row by row (lane l
-            // loads slots 4l .. 4l + 3), its run table with the keys
-            const int e = __ldg(a.ent + it.qt.ent0 + i) >> 1;
+            // tiling by position: a contiguous entry is one tiled box like a packed key
+            // tile; otherwise its 128 keys are gathered row by row (lane l loads slots
+            // 4l .. 4l + 3).  Its run table comes with the keys.
+            const int ev = __ldg(a.ent + it.qt.ent0 + i);
+            if ((ev & 3) == 2) {
+              // a full contiguous range: one tiled box of keys from (ev >> 2), no run table
+              if (elect_one()) {
+                const uint32_t vb = C::KV_ONE ? b_k(st) : b_v(st);
+                mbar_expect_tx(b_k(st), (C::KV_ONE ? 2 : 1) * C::CB * BOX_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::CB; ++c)
+                  tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES, &mk, it.g * D + 64 * c, ev >> 2, b_k(st));
+                if (!C::KV_ONE) mbar_expect_tx(vb, C::CB * BOX_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::CB; ++c)
+                  tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, it.g * D + 64 * c, ev >> 2, vb);
+              }
+              __syncwarp();
+              continue;
+            }
+            const int e = ev >> 2;
             const int4 rows = __ldg(reinterpret_cast<const int4 *>(a.vkeys + (size_t)e * BN) + lane);
+            const int jc = __shfl_sync(0xffffffffu, rows.x, 0);  // slot 0's key
             const uint32_t v_bar = C::KV_ONE ? b_k(st) : b_v(st);
             if (lane == 0) {
               mbar_expect_tx(b_k(st), (C::KV_ONE ? 2 : 1) * C::CB * BOX_BYTES + kVRunWords * 4);
@@ -344,14 +368,25 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
               if (!C::KV_ONE) mbar_expect_tx(v_bar, C::CB * BOX_BYTES);
             }
             __syncwarp();
+            if (ev & 2) {
+              if (lane == 0) {
 #pragma unroll
-            for (int c = 0; c < C::CB; ++c)
-              tma_gather4(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mk, it.g * D + 64 * c,
-                          rows, b_k(st));
+                for (int c = 0; c < C::CB; ++c)
+                  tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES, &mk, it.g * D + 64 * c, jc, b_k(st));
 #pragma unroll
-            for (int c = 0; c < C::CB; ++c)
-              tma_gather4(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mv, it.g * D + 64 * c,
-                          rows, v_bar);
+                for (int c = 0; c < C::CB; ++c)
+                  tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, it.g * D + 64 * c, jc, v_bar);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < C::CB; ++c)
+                tma_gather4(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mkg, it.g * D + 64 * c,
+                            rows, b_k(st));
+#pragma unroll
+              for (int c = 0; c < C::CB; ++c)
+                tma_gather4(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mvg, it.g * D + 64 * c,
+                            rows, v_bar);
+            }
             __syncwarp();
             continue;
           }
@@ -633,7 +668,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           if (h == 1 && !(ok = wait_bar_warp(other_turn, T & 1, abort, a.status))) break;
           if (h == 0 && T > 0 && !(ok = wait_bar_warp(other_turn, (T - 1) & 1, abort, a.status))) break;
         }
-        if (G) {
+        if (G && (e & 1)) {
           // tiling by position: rows not assigned to this entry take nothing from it;
           // an assigned row sees slot c of run r iff c - c0 <= iq - j0 and j0 <= iq < send
           const int32_t *tb = sRuns + st * 128;
@@ -807,11 +842,13 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
     attr_set[gather] = true;
   }
   const int32_t q0 = P.chunk_q0[chunk], nq = P.chunk_q1[chunk] - q0;
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mkg, mvg;
   int rc;
   if ((rc = make_map(&mq, q, (int64_t)hq * D, nq, "tree_attn_fwd")) ||
-      (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", gather ? 1 : 128)) ||
-      (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", gather ? 1 : 128)) ||
+      (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
+      (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
+      (rc = make_map(&mkg, k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", 1)) ||
+      (rc = make_map(&mvg, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", 1)) ||
       (rc = make_map(&mo, o, (int64_t)hq * D, nq, "tree_attn_fwd")))
     return rc;
   AttnArgs a;
@@ -838,7 +875,7 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
   a.work = work;
   if (a.n_items == 0) return TREE_OK;
   const dim3 grid((unsigned)std::min(a.n_items, sm_count()));
-  const cudaError_t e = launch_dependent(kern, grid, dim3(C::THREADS), C::SMEM, s, mq, mk, mv, mo, a);
+  const cudaError_t e = launch_dependent(kern, grid, dim3(C::THREADS), C::SMEM, s, mq, mk, mv, mo, mkg, mvg, a);
   if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd: launch failed: %s", cudaGetErrorString(e));
   return launch_status("tree_attn_fwd");
 }

@@ -292,7 +292,7 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
           }
         if (e < 0) {
           e = (int32_t)P.ent.size();
-          P.ent.push_back((e << 1) | 1);
+          P.ent.push_back((e << 2) | 1);  // flags finished below, once every row is assigned
           const size_t kb = P.vkeys.size(), rb = P.vruns.size();
           P.vkeys.resize(kb + kTile, 0);
           P.vruns.resize(rb + kVRunWords, 0);
@@ -321,6 +321,22 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
         const int32_t r_lo = std::max(i0, bstart[b]), r_hi = std::min(i1, bstart[b] + blen[b]);
         const int32_t first = std::max(r_lo, bstart[b] + (t * kTile - bpos0[b]));
         for (int32_t i = first; i < r_hi; ++i) rows[(i - i0) >> 5] |= (int32_t)(1u << ((i - i0) & 31));
+      }
+      // entries of this range: contiguous (slot c holds packed key j0 + c: one tiled load)
+      // and full (every row of the tile is served by it and sees every slot: no mask)
+      for (const auto &m : made) {
+        const int32_t e = m.first;
+        const int32_t *vk = P.vkeys.data() + (size_t)e * kTile;
+        const int32_t *run = P.vruns.data() + (size_t)e * kVRunWords;
+        const bool contig = run[0] == 1 && run[8] == 0 && run[9] == kTile - 1;
+        bool full = contig && vk[kTile - 1] <= i0;
+        if (full) {
+          for (int32_t i = i0; i < i1 && full; ++i) full = (run[4 + ((i - i0) >> 5)] >> ((i - i0) & 31)) & 1;
+          full = full && run[11] > i1 - 1;
+        }
+        // a full contiguous entry needs neither its gather list nor its run table: it names
+        // its first key instead, like a packed key tile
+        P.ent[(size_t)e] = full ? ((vk[0] << 2) | 2) : ((e << 2) | (contig ? 2 : 0) | 1);
       }
     }
   };

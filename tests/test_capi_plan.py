@@ -226,10 +226,17 @@ def _position_tiles_of(plan, t_):
     for q in range(i.n_qtiles):
         r0, r1 = int(t_["qt_row0"][q]), int(t_["qt_row1"][q])
         for k, e in enumerate(range(int(t_["qt_ent0"][q]), int(t_["qt_ent1"][q]))):
-            assert t_["ent"][e] == (e << 1) | 1
+            ev = int(t_["ent"][e])
+            if ev & 3 == 2:   # full and contiguous: names its first key
+                assert ev >> 2 == vk[e][0]
+            else:
+                assert ev >> 2 == e
             run = vr[e]
             n = int(run[0])
             rows = run[4:8].astype(np.uint32)
+            if ev & 2:   # contiguous: one tiled box of consecutive keys
+                assert (vk[e] == vk[e][0] + np.arange(128)).all()
+            full = not (ev & 1)
             for row in range(r1 - r0):
                 if not (rows[row >> 5] >> (row & 31)) & 1:
                     continue
@@ -243,7 +250,11 @@ def _position_tiles_of(plan, t_):
                     for c in range(c0, min(c1, c0 + iq - j0) + 1):
                         assert c not in seen
                         seen[c] = j0 + c - c0
+                if full:   # no mask: every row of the tile is served and sees every slot
+                    assert len(seen) == 128
                 out.setdefault(iq, []).append((k, seen))
+            if full:
+                assert all((rows[x >> 5] >> (x & 31)) & 1 for x in range(r1 - r0))
     return out
 
 
