@@ -40,7 +40,7 @@ EXPORTS = (
     "tree_queue_default_opts", "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel",
     "tree_queue_info", "tree_queue_pop", "tree_batch_view", "tree_batch_free",
     # include/tree_layer.h
-    "tree_gemm", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd", "tree_last_layer_workspace_bytes",
+    "tree_gemm", "tree_gemm_ex", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd", "tree_last_layer_workspace_bytes",
     "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd", "tree_session_create", "tree_session_run",
     "tree_session_destroy",
 )
@@ -167,6 +167,7 @@ _lib.tree_runtime_create.argtypes = [C.c_size_t, C.c_int32, C.POINTER(_vp)]
 _lib.tree_runtime_destroy.argtypes = [_vp]
 _lib.tree_runtime_step.argtypes = [_vp, C.POINTER(_StepArgs), C.POINTER(PlanInfo), _vp]
 _lib.tree_gemm.argtypes = [_vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
+_lib.tree_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
 _lib.tree_rmsnorm.argtypes = [_vp, _vp, _vp, C.c_int32, C.c_int32, C.c_float, _vp]
 _lib.tree_layer_workspace_bytes.argtypes = [_vp, C.POINTER(LayerWeights), C.POINTER(C.c_size_t)]
 _lib.tree_layer_fwd.argtypes = [_vp, _vp, C.POINTER(LayerWeights), _vp, _vp, _vp, _vp, _vp, C.c_int32, _vp, C.c_size_t,
@@ -191,7 +192,7 @@ _lib.tree_queue_info.argtypes = [_vp, C.POINTER(_QueueInfo)]
 _lib.tree_queue_pop.argtypes = [_vp, C.c_double, C.POINTER(_vp)]
 _lib.tree_batch_view.argtypes = [_vp, C.POINTER(_BatchView)]
 _lib.tree_batch_free.argtypes = [_vp]
-for _f in ("tree_gemm", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd",
+for _f in ("tree_gemm", "tree_gemm_ex", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd",
            "tree_last_layer_workspace_bytes", "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd",
            "tree_session_create", "tree_session_run", "tree_session_destroy",
            "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
@@ -264,9 +265,9 @@ class Spec:
         return cls(forest.parent, forest.length, forest.key, forest.resident, **kw)
 
 
-def gemm(a, b, c, m: int, n: int, k: int, epi: int = GEMM_STORE, r=None, status=None, stream=None):
-    """tree_gemm: C[m, n] = epilogue(A[m, k] B^T), f16 in and out, f32 accumulation."""
-    _check(_lib.tree_gemm(_ptr(a), _ptr(b), _ptr(c), _ptr(r), m, n, k, epi, _ptr(status), _stream(stream)))
+def gemm(a, b, c, m: int, n: int, k: int, epi: int = GEMM_STORE, r=None, status=None, stream=None, tile_n: int = 0):
+    """tree_gemm_ex: C[m, n] = epilogue(A[m, k] B^T), f16 in and out, f32 accumulation (tile_n 0: automatic)."""
+    _check(_lib.tree_gemm_ex(_ptr(a), _ptr(b), _ptr(c), _ptr(r), m, n, k, epi, tile_n, _ptr(status), _stream(stream)))
 
 
 def rmsnorm(x, w, y, rows: int, cols: int, eps: float = 1e-5, stream=None):

@@ -33,12 +33,22 @@ namespace {
 
 using namespace sm103;
 
-constexpr int GBM = 128, GBN = 256, GBK = 64, GSTAGES = 4;
-constexpr uint32_t G_A_BYTES = GBM * GBK * 2;          // 16 KB
-constexpr uint32_t G_B_BYTES = GBN * GBK * 2;          // 32 KB
-constexpr uint32_t G_STAGE = G_A_BYTES + G_B_BYTES;    // 48 KB
-constexpr uint32_t G_SMEM = GSTAGES * G_STAGE + 1024;  // + alignment slack
-constexpr int G_THREADS = 192;                          // producer, MMA, 4 epilogue warps
+constexpr int GBM = 128, GBK = 64;
+constexpr uint32_t G_A_BYTES = GBM * GBK * 2;  // 16 KB
+constexpr int G_THREADS = 192;                  // producer, MMA, 4 epilogue warps
+constexpr int G_MAX_STAGES = 8;
+
+// Tile width BN = the MMA's N: 256 (large m: few, long tiles) or 64 (small m:
+// enough tiles to spread the weight reads over the SMs).  Either way every
+// output is the same f32 sum over K in the same order.
+template <int BN>
+struct GCfg {
+  static constexpr uint32_t B_BYTES = BN * GBK * 2;
+  static constexpr uint32_t STAGE = G_A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 8;
+  static constexpr uint32_t SMEM = STAGES * STAGE + 1024;  // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 2 * BN;             // two accumulators
+};
 constexpr int G_GROUP_M = 16;                           // M tiles per raster group
 constexpr uint64_t kGemmWaitNs = 2000000000ull;
 constexpr uint64_t kGemmDrainNs = 500000000ull;
@@ -54,7 +64,7 @@ struct GemmArgs {
 };
 
 struct GBars {
-  uint64_t full[GSTAGES], empty[GSTAGES], acc_full[2], acc_empty[2];
+  uint64_t full[G_MAX_STAGES], empty[G_MAX_STAGES], acc_full[2], acc_empty[2];
   uint32_t tmem;
   int32_t abort;
 };
@@ -94,8 +104,13 @@ __device__ __forceinline__ void tile_of(const GemmArgs &a, int t, int &tm, int &
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
 
+template <int BN>
 __global__ void __launch_bounds__(G_THREADS, 1)
     gemm_tc(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb, const GemmArgs a) {
+  using Cf = GCfg<BN>;
+  constexpr int GSTAGES = Cf::STAGES;
+  constexpr uint32_t G_STAGE = Cf::STAGE;
+  constexpr uint32_t G_B_BYTES = Cf::B_BYTES;
   extern __shared__ uint8_t g_smem_raw[];
   __shared__ GBars bars;
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(g_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -119,7 +134,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     bars.abort = 0;
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(&bars.tmem), 512);
+  if (warp == 1) tmem_alloc(smem_u32(&bars.tmem), Cf::TMEM_COLS);
   fence_before();
   __syncthreads();
   fence_after();
@@ -139,7 +154,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       int tm, tn;
       tile_of(a, t, tm, tn);
       const int m0 = tm * GBM, n0 = tn * a.bn;
-      const int nb2 = a.epi == TREE_GEMM_SWIGLU ? a.n + n0 : n0 + 128;  // rows of the second B box
+      const int nb2 = a.epi == TREE_GEMM_SWIGLU ? a.n + n0 : n0 + BN / 2;  // rows of the second B box
       for (int kb = 0; kb < a.nk; ++kb, ++it) {
         const int s = it % GSTAGES;
         if (it >= GSTAGES && !(ok = gwait_warp(b_empty(s), ((it / GSTAGES) - 1) & 1, abort, a.status))) break;
@@ -159,14 +174,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       gwait(b_full(u % GSTAGES), (u / GSTAGES) & 1, abort, nullptr, kGemmDrainNs, false);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_f16(GBM, GBN, false);
+    constexpr uint32_t idesc = idesc_f16(GBM, BN, false);
     int it = 0, tc = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x, ++tc) {
       const int b = tc & 1;
       if (tc >= 2 && !(ok = gwait_warp(b_ae(b), ((tc / 2) - 1) & 1, abort, a.status))) break;
       fence_after();
-      const uint32_t d = tmem + (uint32_t)(b * GBN);
+      const uint32_t d = tmem + (uint32_t)(b * BN);
       for (int kb = 0; kb < a.nk; ++kb, ++it) {
         const int s = it % GSTAGES;
         if (!(ok = gwait_warp(b_full(s), (it / GSTAGES) & 1, abort, a.status))) break;
@@ -203,12 +218,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const int row = tm * GBM + 32 * qd + lane, n0 = tn * a.bn;
       const bool row_ok = row < a.m;
       __half *crow = a.c + (size_t)row * a.n;
-      const uint32_t acc = t_lane + (uint32_t)(b * GBN);
+      const uint32_t acc = t_lane + (uint32_t)(b * BN);
       if (a.epi == TREE_GEMM_SWIGLU) {
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < BN / 64; ++ch) {
           uint32_t g[32], u[32];
           tmem_ld32(acc + 32 * ch, g);
-          tmem_ld32(acc + 128 + 32 * ch, u);
+          tmem_ld32(acc + BN / 2 + 32 * ch, u);
           tmem_wait_ld();
           const int c0 = n0 + 32 * ch;
 #pragma unroll
@@ -226,7 +241,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         }
       } else {
         const __half *rrow = a.r ? a.r + (size_t)row * a.n : nullptr;
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int ch = 0; ch < BN / 32; ++ch) {
           uint32_t x[32];
           tmem_ld32(acc + 32 * ch, x);
           tmem_wait_ld();
@@ -271,40 +286,35 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, Cf::TMEM_COLS);
   }
 }
 
 }  // namespace
 }  // namespace tree
 
-extern "C" TREE_API int tree_gemm(const void *a, const void *b, void *c, const void *r, int32_t m, int32_t n,
-                                  int32_t k, int32_t epi, int32_t *status, tree_stream_t stream) {
-  using namespace tree;
-  if (!a || !b || !c) return fail(TREE_ERR_INVALID_ARG, "tree_gemm: NULL argument");
-  if (m < 0 || n <= 0 || k <= 0) return fail(TREE_ERR_INVALID_ARG, "tree_gemm: m %d, n %d, k %d", m, n, k);
-  if (epi != TREE_GEMM_STORE && epi != TREE_GEMM_RESIDUAL && epi != TREE_GEMM_SWIGLU && epi != TREE_GEMM_STORE_F32)
-    return fail(TREE_ERR_INVALID_ARG, "tree_gemm: unknown epilogue %d", epi);
-  if (epi == TREE_GEMM_RESIDUAL && !r) return fail(TREE_ERR_INVALID_ARG, "tree_gemm: RESIDUAL needs r");
-  if (n % 8 || k % 8) return fail(TREE_ERR_UNSUPPORTED, "tree_gemm: n %d and k %d must be multiples of 8", n, k);
-  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (r && !aligned16(r)))
-    return fail(TREE_ERR_UNSUPPORTED, "tree_gemm: tensors must be 16-byte aligned");
-  if (m == 0) return TREE_OK;
+namespace tree {
+namespace {
+
+template <int BN>
+int launch_gemm(const void *a, const void *b, void *c, const void *r, int32_t m, int32_t n, int32_t k, int32_t epi,
+                int32_t *status, cudaStream_t s) {
+  using Cf = GCfg<BN>;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G_SMEM);
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
     if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_gemm: %s", cudaGetErrorString(e));
     attr_set = true;
   }
   const int nb_rows = epi == TREE_GEMM_SWIGLU ? 2 * n : n;
   CUtensorMap ma, mb;
   int rc;
-  if ((rc = make_map(&ma, a, k, m, "tree_gemm")) || (rc = make_map(&mb, b, k, nb_rows, "tree_gemm"))) return rc;
+  if ((rc = make_map(&ma, a, k, m, "tree_gemm")) || (rc = make_map(&mb, b, k, nb_rows, "tree_gemm", BN / 2))) return rc;
   GemmArgs g;
   g.m = m;
   g.n = n;
   g.k = k;
-  g.bn = epi == TREE_GEMM_SWIGLU ? GBN / 2 : GBN;
+  g.bn = epi == TREE_GEMM_SWIGLU ? BN / 2 : BN;
   g.tiles_m = (m + GBM - 1) / GBM;
   g.tiles_n = (n + g.bn - 1) / g.bn;
   g.n_tiles = g.tiles_m * g.tiles_n;
@@ -314,7 +324,41 @@ extern "C" TREE_API int tree_gemm(const void *a, const void *b, void *c, const v
   g.r = reinterpret_cast<const __half *>(r);
   g.status = status;
   const dim3 grid((unsigned)std::min(g.n_tiles, sm_count()));
-  const cudaError_t e = launch_dependent(gemm_tc, grid, dim3(G_THREADS), G_SMEM, as_stream(stream), ma, mb, g);
+  const cudaError_t e = launch_dependent(gemm_tc<BN>, grid, dim3(G_THREADS), Cf::SMEM, s, ma, mb, g);
   if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_gemm: launch failed: %s", cudaGetErrorString(e));
   return launch_status("tree_gemm");
+}
+
+}  // namespace
+}  // namespace tree
+
+extern "C" TREE_API int tree_gemm_ex(const void *a, const void *b, void *c, const void *r, int32_t m, int32_t n,
+                                     int32_t k, int32_t epi, int32_t tile_n, int32_t *status, tree_stream_t stream) {
+  using namespace tree;
+  if (!a || !b || !c) return fail(TREE_ERR_INVALID_ARG, "tree_gemm: NULL argument");
+  if (m < 0 || n <= 0 || k <= 0) return fail(TREE_ERR_INVALID_ARG, "tree_gemm: m %d, n %d, k %d", m, n, k);
+  if (epi != TREE_GEMM_STORE && epi != TREE_GEMM_RESIDUAL && epi != TREE_GEMM_SWIGLU && epi != TREE_GEMM_STORE_F32)
+    return fail(TREE_ERR_INVALID_ARG, "tree_gemm: unknown epilogue %d", epi);
+  if (epi == TREE_GEMM_RESIDUAL && !r) return fail(TREE_ERR_INVALID_ARG, "tree_gemm: RESIDUAL needs r");
+  if (tile_n != 0 && tile_n != 64 && tile_n != 256)
+    return fail(TREE_ERR_INVALID_ARG, "tree_gemm: tile_n %d not in {0, 64, 256}", tile_n);
+  if (n % 8 || k % 8) return fail(TREE_ERR_UNSUPPORTED, "tree_gemm: n %d and k %d must be multiples of 8", n, k);
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (r && !aligned16(r)))
+    return fail(TREE_ERR_UNSUPPORTED, "tree_gemm: tensors must be 16-byte aligned");
+  if (m == 0) return TREE_OK;
+  if (tile_n == 0) {
+    // wide tiles, unless m is small (the weights' reads dominate) and wide tiles would
+    // leave SMs without work
+    const int64_t wide = (int64_t)((m + GBM - 1) / GBM) * ((n + (epi == TREE_GEMM_SWIGLU ? 127 : 255)) /
+                                                           (epi == TREE_GEMM_SWIGLU ? 128 : 256));
+    tile_n = (m <= 2048 && wide < sm_count()) ? 64 : 256;
+  }
+  const cudaStream_t s = as_stream(stream);
+  return tile_n == 256 ? launch_gemm<256>(a, b, c, r, m, n, k, epi, status, s)
+                       : launch_gemm<64>(a, b, c, r, m, n, k, epi, status, s);
+}
+
+extern "C" TREE_API int tree_gemm(const void *a, const void *b, void *c, const void *r, int32_t m, int32_t n,
+                                  int32_t k, int32_t epi, int32_t *status, tree_stream_t stream) {
+  return tree_gemm_ex(a, b, c, r, m, n, k, epi, 0, status, stream);
 }

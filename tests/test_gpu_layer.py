@@ -32,9 +32,10 @@ def _inputs(m, n_b, k, seed):
 SHAPES = [(128, 256, 64), (300, 264, 136), (1000, 768, 520), (2048, 3072, 2048), (77, 8, 8), (129, 520, 4096)]
 
 
+@pytest.mark.parametrize("tile_n", [0, 64, 256])
 @pytest.mark.parametrize("m,n,k", SHAPES)
 @pytest.mark.parametrize("epi", ["store", "residual", "swiglu"])
-def test_gemm_matches_oracle(m, n, k, epi):
+def test_gemm_matches_oracle(m, n, k, epi, tile_n):
     dev = torch.device("cuda")
     n_b = 2 * n if epi == "swiglu" else n
     a, b, r = _inputs(m, n_b, k, seed=m + n + k)
@@ -44,12 +45,31 @@ def test_gemm_matches_oracle(m, n, k, epi):
     tc = torch.full((m, n), float("nan"), dtype=torch.float16, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     code = {"store": lib.GEMM_STORE, "residual": lib.GEMM_RESIDUAL, "swiglu": lib.GEMM_SWIGLU}[epi]
-    lib.gemm(ta, tb, tc, m, n, k, code, r=tr if epi == "residual" else None, status=st)
+    lib.gemm(ta, tb, tc, m, n, k, code, r=tr if epi == "residual" else None, status=st, tile_n=tile_n)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     ref = ol.gemm(a, b, epi, r)
     # f32 accumulation against float64: one f16 rounding apart, plus the f32 sum's error
     _close16(tc.cpu().numpy(), ref, extra=1e-4)
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 264, 136), (1000, 768, 520), (77, 8, 8), (129, 520, 4096)])
+@pytest.mark.parametrize("epi", ["store", "residual", "swiglu"])
+def test_gemm_tile_width_changes_nothing(m, n, k, epi):
+    """Narrow and wide tiles give bit-identical outputs (each is the same f32 sum over k)."""
+    dev = torch.device("cuda")
+    n_b = 2 * n if epi == "swiglu" else n
+    a, b, r = _inputs(m, n_b, k, seed=3 * m + n)
+    r = r[:, :n].copy()
+    ta, tb, tr = (torch.from_numpy(x).to(dev) for x in (a, b, r))
+    code = {"store": lib.GEMM_STORE, "residual": lib.GEMM_RESIDUAL, "swiglu": lib.GEMM_SWIGLU}[epi]
+    outs = []
+    for tile_n in (64, 256):
+        tc = torch.empty((m, n), dtype=torch.float16, device=dev)
+        lib.gemm(ta, tb, tc, m, n, k, code, r=tr if epi == "residual" else None, tile_n=tile_n)
+        outs.append(tc)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
 
 
 def test_gemm_residual_in_place_and_empty():
