@@ -314,7 +314,7 @@ def measure_layer(lib, torch, w, dev, stream, reps, warmup):
         if name == "gate_up":
             b_, epi, nn, r = td["wgu"], lib.GEMM_SWIGLU, ffn, None
         elif name == "qkv":
-            b_, epi, nn, r = torch.cat([td["wq"], td["wk"], td["wv"]]), lib.GEMM_STORE, n, None
+            b_, epi, nn, r = td["wqkv"], lib.GEMM_STORE, n, None
         else:
             b_, epi, nn, r = (td["wo"] if name == "o" else td["wd"]), lib.GEMM_RESIDUAL, n, out
         av = a_[:, :k].contiguous()
@@ -359,8 +359,7 @@ def measure_model(lib, torch, dev, stream, spec: dict, d: int, hq: int, hkv: int
     qd, kvd = hq * d, hkv * d
     keep, layers, kcs, vcs = [], [], [], []
     for _ in range(n_layers):
-        t = {"w_in": rnd(hidden, scale=0.1, off=1.0), "wq": rnd(qd, hidden, scale=hidden ** -0.5),
-             "wk": rnd(kvd, hidden, scale=hidden ** -0.5), "wv": rnd(kvd, hidden, scale=hidden ** -0.5),
+        t = {"w_in": rnd(hidden, scale=0.1, off=1.0), "wqkv": rnd(qd + 2 * kvd, hidden, scale=hidden ** -0.5),
              "wo": rnd(hidden, qd, scale=qd ** -0.5), "w_post": rnd(hidden, scale=0.1, off=1.0),
              "wgu": rnd(2 * ffn, hidden, scale=hidden ** -0.5), "wd": rnd(hidden, ffn, scale=ffn ** -0.5)}
         keep.append(t)

@@ -7,7 +7,7 @@
  * padding.  A layer over the packed tokens of a batch is
  *
  *     xn = rmsnorm(x, w_in)                      tree_rmsnorm
- *     q, k, v = xn Wq^T, xn Wk^T, xn Wv^T        tree_gemm STORE (k, v into the cache rows)
+ *     q, k, v = xn [Wq; Wk; Wv]^T               tree_gemm_qkv (k, v into the cache rows)
  *     q, k rotated at tree positions             tree_rope           (tree_attn.h)
  *     o = attention over tree blocks             tree_attn_fwd       (tree_attn.h)
  *     h = x + o Wo^T                             tree_gemm RESIDUAL
@@ -61,6 +61,15 @@ TREE_API int tree_gemm_ex(const void *a, const void *b, void *c, const void *r, 
                           int32_t epi, int32_t tile_n, int32_t *status, tree_stream_t stream);
 
 /*
+ * The three projections of the attention block in one GEMM: W = [Wq; Wk; Wv]
+ * f16 [nq + 2 nkv, k]; the output columns go to q f16 [m, nq], k and v f16
+ * [m, nkv] (e.g. the forward rows of the caches).  Each output is the same f32
+ * sum as tree_gemm's.  nq, nkv, k multiples of 8.
+ */
+TREE_API int tree_gemm_qkv(const void *a, const void *wqkv, void *q, void *k, void *v, int32_t m, int32_t nq,
+                           int32_t nkv, int32_t kdim, int32_t *status, tree_stream_t stream);
+
+/*
  * y[i, :] = f16( f16(x[i, :] / sqrt(mean_j x[i, j]^2 + eps)) * w ), the Llama
  * RMSNorm with its f32 statistics: the normalised row is rounded to f16 before
  * the f16 weight multiplies it.  x, y f16 [rows, cols] (y may be x), w f16
@@ -74,8 +83,7 @@ typedef struct {
   int32_t hidden, hq, hkv, d, ffn; /* model width, query / kv heads, head dim (64 or 128), MLP width */
   float eps;                       /* RMSNorm epsilon (Llama: 1e-5) */
   const void *w_in;                /* [hidden]            RMSNorm before attention */
-  const void *wq;                  /* [hq * d, hidden] */
-  const void *wk, *wv;             /* [hkv * d, hidden] */
+  const void *wqkv;                /* [(hq + 2 hkv) d, hidden]: the q rows, then the k rows, then the v rows */
   const void *wo;                  /* [hidden, hq * d] */
   const void *w_post;              /* [hidden]            RMSNorm before the MLP */
   const void *wgu;                 /* [2 * ffn, hidden]   gate rows, then up rows */

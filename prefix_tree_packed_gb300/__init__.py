@@ -40,7 +40,7 @@ EXPORTS = (
     "tree_queue_default_opts", "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel",
     "tree_queue_info", "tree_queue_pop", "tree_batch_view", "tree_batch_free",
     # include/tree_layer.h
-    "tree_gemm", "tree_gemm_ex", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd", "tree_last_layer_workspace_bytes",
+    "tree_gemm", "tree_gemm_ex", "tree_gemm_qkv", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd", "tree_last_layer_workspace_bytes",
     "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd", "tree_session_create", "tree_session_run",
     "tree_session_destroy",
 )
@@ -97,7 +97,7 @@ class _BatchView(C.Structure):
 
 class LayerWeights(C.Structure):
     _fields_ = [("hidden", C.c_int32), ("hq", C.c_int32), ("hkv", C.c_int32), ("d", C.c_int32), ("ffn", C.c_int32),
-                ("eps", C.c_float), ("w_in", C.c_void_p), ("wq", C.c_void_p), ("wk", C.c_void_p), ("wv", C.c_void_p),
+                ("eps", C.c_float), ("w_in", C.c_void_p), ("wqkv", C.c_void_p),
                 ("wo", C.c_void_p), ("w_post", C.c_void_p), ("wgu", C.c_void_p), ("wd", C.c_void_p)]
 
 
@@ -168,6 +168,7 @@ _lib.tree_runtime_destroy.argtypes = [_vp]
 _lib.tree_runtime_step.argtypes = [_vp, C.POINTER(_StepArgs), C.POINTER(PlanInfo), _vp]
 _lib.tree_gemm.argtypes = [_vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
 _lib.tree_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
+_lib.tree_gemm_qkv.argtypes = [_vp, _vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
 _lib.tree_rmsnorm.argtypes = [_vp, _vp, _vp, C.c_int32, C.c_int32, C.c_float, _vp]
 _lib.tree_layer_workspace_bytes.argtypes = [_vp, C.POINTER(LayerWeights), C.POINTER(C.c_size_t)]
 _lib.tree_layer_fwd.argtypes = [_vp, _vp, C.POINTER(LayerWeights), _vp, _vp, _vp, _vp, _vp, C.c_int32, _vp, C.c_size_t,
@@ -192,7 +193,7 @@ _lib.tree_queue_info.argtypes = [_vp, C.POINTER(_QueueInfo)]
 _lib.tree_queue_pop.argtypes = [_vp, C.c_double, C.POINTER(_vp)]
 _lib.tree_batch_view.argtypes = [_vp, C.POINTER(_BatchView)]
 _lib.tree_batch_free.argtypes = [_vp]
-for _f in ("tree_gemm", "tree_gemm_ex", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd",
+for _f in ("tree_gemm", "tree_gemm_ex", "tree_gemm_qkv", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd",
            "tree_last_layer_workspace_bytes", "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd",
            "tree_session_create", "tree_session_run", "tree_session_destroy",
            "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
@@ -270,15 +271,21 @@ def gemm(a, b, c, m: int, n: int, k: int, epi: int = GEMM_STORE, r=None, status=
     _check(_lib.tree_gemm_ex(_ptr(a), _ptr(b), _ptr(c), _ptr(r), m, n, k, epi, tile_n, _ptr(status), _stream(stream)))
 
 
+def gemm_qkv(a, wqkv, q, k, v, m: int, nq: int, nkv: int, kdim: int, status=None, stream=None):
+    """tree_gemm_qkv: the q, k, v projections in one GEMM, written to three outputs."""
+    _check(_lib.tree_gemm_qkv(_ptr(a), _ptr(wqkv), _ptr(q), _ptr(k), _ptr(v), m, nq, nkv, kdim, _ptr(status),
+                              _stream(stream)))
+
+
 def rmsnorm(x, w, y, rows: int, cols: int, eps: float = 1e-5, stream=None):
     """tree_rmsnorm: y = f16(f16(x / sqrt(mean(x^2) + eps)) * w) per row."""
     _check(_lib.tree_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, cols, eps, _stream(stream)))
 
 
 def layer_weights(hidden: int, hq: int, hkv: int, d: int, ffn: int, tensors: dict, eps: float = 1e-5) -> LayerWeights:
-    """LayerWeights from device tensors keyed w_in, wq, wk, wv, wo, w_post, wgu, wd (kept alive by the caller)."""
+    """LayerWeights from device tensors keyed w_in, wqkv, wo, w_post, wgu, wd (kept alive by the caller)."""
     return LayerWeights(hidden, hq, hkv, d, ffn, eps, *[_ptr(tensors[k]) for k in
-                                                        ("w_in", "wq", "wk", "wv", "wo", "w_post", "wgu", "wd")])
+                                                        ("w_in", "wqkv", "wo", "w_post", "wgu", "wd")])
 
 
 def layer_workspace_bytes(plan: "Plan", w: LayerWeights) -> int:

@@ -53,8 +53,12 @@ constexpr int G_GROUP_M = 16;                           // M tiles per raster gr
 constexpr uint64_t kGemmWaitNs = 2000000000ull;
 constexpr uint64_t kGemmDrainNs = 500000000ull;
 
+constexpr int kEpiQKV = 16;  // internal: STORE with the columns split over three outputs (tree_gemm_qkv)
+
 struct GemmArgs {
   int m, n, k;         // C is m x n; B has n rows (2n for SWIGLU)
+  int n1, n2;          // kEpiQKV: columns [0, n1) -> c, [n1, n1 + n2) -> c2, [n1 + n2, n) -> c3
+  __half *c2, *c3;
   int tiles_m, tiles_n, n_tiles, nk;
   int bn;              // output columns per tile (256, SWIGLU 128)
   int epi;
@@ -274,7 +278,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             w.y = pack_f16x2(f[2], f[3]);
             w.z = pack_f16x2(f[4], f[5]);
             w.w = pack_f16x2(f[6], f[7]);
-            *reinterpret_cast<uint4 *>(crow + c) = w;
+            __half *dst = crow + c;
+            if (a.epi == kEpiQKV)
+              dst = c < a.n1 ? a.c + (size_t)row * a.n1 + c
+                             : (c < a.n1 + a.n2 ? a.c2 + (size_t)row * a.n2 + (c - a.n1)
+                                                : a.c3 + (size_t)row * a.n2 + (c - a.n1 - a.n2));
+            *reinterpret_cast<uint4 *>(dst) = w;
           }
         }
       }
@@ -298,7 +307,8 @@ namespace {
 
 template <int BN>
 int launch_gemm(const void *a, const void *b, void *c, const void *r, int32_t m, int32_t n, int32_t k, int32_t epi,
-                int32_t *status, cudaStream_t s) {
+                int32_t *status, cudaStream_t s, int32_t n1 = 0, int32_t n2 = 0, void *c2 = nullptr,
+                void *c3 = nullptr) {
   using Cf = GCfg<BN>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -323,6 +333,10 @@ int launch_gemm(const void *a, const void *b, void *c, const void *r, int32_t m,
   g.c = reinterpret_cast<__half *>(c);
   g.r = reinterpret_cast<const __half *>(r);
   g.status = status;
+  g.n1 = n1;
+  g.n2 = n2;
+  g.c2 = reinterpret_cast<__half *>(c2);
+  g.c3 = reinterpret_cast<__half *>(c3);
   const dim3 grid((unsigned)std::min(g.n_tiles, sm_count()));
   const cudaError_t e = launch_dependent(gemm_tc<BN>, grid, dim3(G_THREADS), Cf::SMEM, s, ma, mb, g);
   if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_gemm: launch failed: %s", cudaGetErrorString(e));
@@ -361,4 +375,23 @@ extern "C" TREE_API int tree_gemm_ex(const void *a, const void *b, void *c, cons
 extern "C" TREE_API int tree_gemm(const void *a, const void *b, void *c, const void *r, int32_t m, int32_t n,
                                   int32_t k, int32_t epi, int32_t *status, tree_stream_t stream) {
   return tree_gemm_ex(a, b, c, r, m, n, k, epi, 0, status, stream);
+}
+
+extern "C" TREE_API int tree_gemm_qkv(const void *a, const void *wqkv, void *q, void *k, void *v, int32_t m,
+                                      int32_t nq, int32_t nkv, int32_t kdim, int32_t *status, tree_stream_t stream) {
+  using namespace tree;
+  if (!a || !wqkv || !q || !k || !v) return fail(TREE_ERR_INVALID_ARG, "tree_gemm_qkv: NULL argument");
+  if (m < 0 || nq <= 0 || nkv <= 0 || kdim <= 0)
+    return fail(TREE_ERR_INVALID_ARG, "tree_gemm_qkv: m %d, nq %d, nkv %d, k %d", m, nq, nkv, kdim);
+  if (nq % 8 || nkv % 8 || kdim % 8)
+    return fail(TREE_ERR_UNSUPPORTED, "tree_gemm_qkv: nq, nkv and k must be multiples of 8");
+  if (!aligned16(a) || !aligned16(wqkv) || !aligned16(q) || !aligned16(k) || !aligned16(v))
+    return fail(TREE_ERR_UNSUPPORTED, "tree_gemm_qkv: tensors must be 16-byte aligned");
+  if (m == 0) return TREE_OK;
+  const int n = nq + 2 * nkv;
+  const int64_t wide = (int64_t)((m + GBM - 1) / GBM) * ((n + 255) / 256);
+  const cudaStream_t s = as_stream(stream);
+  return (m <= 2048 && wide < sm_count())
+             ? launch_gemm<64>(a, wqkv, q, nullptr, m, n, kdim, kEpiQKV, status, s, nq, nkv, k, v)
+             : launch_gemm<256>(a, wqkv, q, nullptr, m, n, kdim, kEpiQKV, status, s, nq, nkv, k, v);
 }

@@ -86,7 +86,7 @@ int check_weights(const tree_layer_weights_t *w) {
     return fail(TREE_ERR_INVALID_ARG, "tree_layer: hidden %d, hq %d, hkv %d, ffn %d", w->hidden, w->hq, w->hkv, w->ffn);
   if (w->d != 64 && w->d != 128) return fail(TREE_ERR_UNSUPPORTED, "tree_layer: head dim %d", w->d);
   if (w->hidden % 8 || w->ffn % 8) return fail(TREE_ERR_UNSUPPORTED, "tree_layer: hidden and ffn must be multiples of 8");
-  if (!w->w_in || !w->wq || !w->wk || !w->wv || !w->wo || !w->w_post || !w->wgu || !w->wd)
+  if (!w->w_in || !w->wqkv || !w->wo || !w->w_post || !w->wgu || !w->wd)
     return fail(TREE_ERR_INVALID_ARG, "tree_layer: NULL weight");
   return TREE_OK;
 }
@@ -130,9 +130,7 @@ extern "C" TREE_API int tree_layer_fwd(const tree_plan_t *plan, const void *plan
   __half *vf = static_cast<__half *>(v_cache) + (size_t)P.n_res * kvd;
   // attention block
   if ((rc = tree_rmsnorm(x, w->w_in, xn, m, w->hidden, w->eps, stream))) return rc;
-  if ((rc = tree_gemm(xn, w->wq, q, nullptr, m, qd, w->hidden, TREE_GEMM_STORE, status, stream))) return rc;
-  if ((rc = tree_gemm(xn, w->wk, kf, nullptr, m, kvd, w->hidden, TREE_GEMM_STORE, status, stream))) return rc;
-  if ((rc = tree_gemm(xn, w->wv, vf, nullptr, m, kvd, w->hidden, TREE_GEMM_STORE, status, stream))) return rc;
+  if ((rc = tree_gemm_qkv(xn, w->wqkv, q, kf, vf, m, qd, kvd, w->hidden, status, stream))) return rc;
   tree_attn_params_t ap{w->hq, w->hkv, w->d, 0.f, nullptr, 0};
   for (int c = 0; c < P.n_chunks; ++c) {
     const size_t r0 = (size_t)(P.chunk_q0[c] - P.n_res);
@@ -198,9 +196,7 @@ extern "C" TREE_API int tree_last_layer_fwd(const tree_plan_t *plan, const void 
   const cudaStream_t s = as_stream(stream);
   // attention block over every forward token
   if ((rc = tree_rmsnorm(x, w->w_in, xn, m, w->hidden, w->eps, stream))) return rc;
-  if ((rc = tree_gemm(xn, w->wq, q, nullptr, m, qd, w->hidden, TREE_GEMM_STORE, status, stream))) return rc;
-  if ((rc = tree_gemm(xn, w->wk, kf, nullptr, m, kvd, w->hidden, TREE_GEMM_STORE, status, stream))) return rc;
-  if ((rc = tree_gemm(xn, w->wv, vf, nullptr, m, kvd, w->hidden, TREE_GEMM_STORE, status, stream))) return rc;
+  if ((rc = tree_gemm_qkv(xn, w->wqkv, q, kf, vf, m, qd, kvd, w->hidden, status, stream))) return rc;
   tree_attn_params_t ap{w->hq, w->hkv, w->d, 0.f, nullptr, 0};
   for (int c = 0; c < P.n_chunks; ++c) {
     const size_t r0 = (size_t)(P.chunk_q0[c] - P.n_res);

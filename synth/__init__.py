@@ -272,6 +272,7 @@ def draw_layer(n_fwd: int, n_res: int, hidden: int, hq: int, hkv: int, d: int, f
         "w_post": (1.0 + 0.1 * rng.standard_normal(hidden)).astype(np.float16),
         "wgu": lin(2 * ffn, hidden), "wd": lin(hidden, ffn),
     }
+    w["wqkv"] = np.concatenate([w["wq"], w["wk"], w["wv"]])  # the fused projection's layout
     x = rng.standard_normal((n_fwd, hidden), dtype=np.float32).astype(np.float16)
     res_k = rng.standard_normal((n_res, hkv * d), dtype=np.float32).astype(np.float16)
     res_v = rng.standard_normal((n_res, hkv * d), dtype=np.float32).astype(np.float16)

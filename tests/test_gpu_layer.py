@@ -420,3 +420,23 @@ def test_long_session_slices_equal_model_fwd():
     assert sess.run(1e9) == (L, True)
     sess.close()
     assert torch.equal(lg2, ref_long)
+
+
+@pytest.mark.parametrize("m", [300, 2048, 5000])
+def test_gemm_qkv_split_equals_separate_gemms(m):
+    """One GEMM over [Wq; Wk; Wv] writes the three outputs bit-identical to three GEMMs."""
+    dev = torch.device("cuda")
+    nq, nkv, k = 512, 128, 256
+    a, b, _ = _inputs(m, nq + 2 * nkv, k, seed=m)
+    ta, tb = torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)
+    q = torch.empty((m, nq), dtype=torch.float16, device=dev)
+    kk = torch.empty((m, nkv), dtype=torch.float16, device=dev)
+    v = torch.empty((m, nkv), dtype=torch.float16, device=dev)
+    lib.gemm_qkv(ta, tb, q, kk, v, m, nq, nkv, k)
+    ref = [torch.empty((m, n), dtype=torch.float16, device=dev) for n in (nq, nkv, nkv)]
+    lib.gemm(ta, tb[:nq].contiguous(), ref[0], m, nq, k)
+    lib.gemm(ta, tb[nq:nq + nkv].contiguous(), ref[1], m, nkv, k)
+    lib.gemm(ta, tb[nq + nkv:].contiguous(), ref[2], m, nkv, k)
+    torch.cuda.synchronize()
+    assert torch.equal(q, ref[0]) and torch.equal(kk, ref[1]) and torch.equal(v, ref[2])
+    _close16(q.cpu().numpy(), ol.gemm(a, b[:nq]), extra=1e-4)
