@@ -163,3 +163,41 @@ def test_runtime_capacity_checked(lib):
         rt.step(spec, x, x, x, x, torch.zeros(16, device="cuda"), 1 << 20, 32, 8, 128)
     assert e.value.code == lib.TREE_ERR_UNSUPPORTED
     rt.close()
+
+
+def test_queue_batches_run_through_the_runtime(lib):
+    """Requests -> queue -> batches (merged prefix trees) -> one runtime step each; every step equals
+    the separate calls on the same batch, and the attention equals the oracle on the batch's forest."""
+    q = lib.Queue(resident_keys=[1])
+    rng = np.random.default_rng(31)
+    for rid in range(12):
+        doc = int(rng.integers(0, 3))
+        prompts, qs = [], []
+        for qi in range(int(rng.integers(1, 3))):
+            qkey = int(rng.integers(1, 1 << 40))
+            for o in range(2):
+                prompts.append([(1, 53), (100 + doc, 1500 + 1000 * doc), (qkey, int(rng.integers(10, 60))),
+                                (int(rng.integers(1, 1 << 40)), int(rng.integers(5, 20)))])
+            qs.append((len(prompts) - 2, len(prompts) - 1))
+        q.push(rid, float(rid), prompts, qs)
+    rt = _rt(lib, max_chunks=8)
+    steps = 0
+    now = 20.0
+    while True:
+        b = q.pop(now)
+        if b is None:
+            break
+        forest = synth.Forest(b.parent, b.length, b.key, b.resident)
+        bt = Batch(lib, forest, 8, 2, 64, 40 + steps, leaf1=b.leaf1, leaf2=b.leaf2)
+        assert bt.info.n_fwd == b.cost
+        got = bt.buffers()
+        bt.step(rt, got)
+        torch.cuda.synchronize()
+        _same(got, bt.reference(), bt.nq)
+        p, _ = oplan.plan_forest(forest, leaf1=b.leaf1, leaf2=b.leaf2)
+        qr, kr = orope.apply_plan(p, bt.q, bt.k, 500000.0)
+        assert np.abs(got["o"].float().cpu().numpy() - oatt.attend_paths(p, qr, kr, bt.v)).max() <= 2e-3
+        steps += 1
+        now += 5.0
+    assert steps >= 2 and q.info() == (0, 0)
+    rt.close()
