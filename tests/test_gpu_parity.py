@@ -139,6 +139,46 @@ def test_readout_sizes(lib, stride, nmax):
     _check_readout(lib, logits, 2 * np.arange(nq), 2 * np.arange(nq) + 1, n, T, stride)
 
 
+def test_readout_every_exact_stride_scattered_rows(lib):
+    """Strides 1..16 each have their own kernel instance: every one, with the two orders' rows
+    scattered over the logits buffer (a random permutation) and a ragged last tile."""
+    for stride in range(1, 17):
+        rng = np.random.default_rng(100 + stride)
+        nq = 32 * 9 + 7
+        logits = (rng.standard_normal((2 * nq + 5, stride)) * 3).astype(np.float32)
+        rows = rng.permutation(2 * nq + 5)[:2 * nq]
+        n = rng.integers(1, stride + 1, nq)
+        n[0] = stride
+        T = rng.choice([0.5, 1.0, 2.0], nq)
+        _check_readout(lib, logits, rows[:nq], rows[nq:], n, T, stride)
+
+
+@pytest.mark.parametrize("stride", [10, 7, 20])
+def test_readout_unaligned_buffers(lib, stride):
+    """Logits, p_cal and p_avg at 4-byte (not 8- or 16-byte) aligned addresses: the kernels fall
+    back from letter-pair loads and 16-byte stores to single floats, with the same results."""
+    rng = np.random.default_rng(7 + stride)
+    nq = 32 * 5 + 19
+    logits = (rng.standard_normal((2 * nq, stride)) * 3).astype(np.float32)
+    n = rng.integers(1, min(stride, 10) + 1, nq)
+    T = rng.choice([0.5, 1.0, 2.0], nq)
+    lg = torch.zeros(2 * nq * stride + 1, device="cuda")
+    lg[1:] = _dev(logits).reshape(-1)
+    pcb = torch.full((nq * stride + 1,), -7.0, device="cuda")
+    pab = torch.full((nq * stride + 1,), -7.0, device="cuda")
+    ch = torch.full((nq,), -9, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r1, r2 = np.arange(nq) * 2, np.arange(nq) * 2 + 1
+    lib.readout_decide(lg[1:], stride, _dev(np.int32(r1)), _dev(np.int32(r2)), _dev(np.int32(n)),
+                       _dev(np.float32(T)), nq, pcb[1:], pab[1:], ch, st, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_pc, ref_pa, _ = ordo.decide(logits, r1, r2, n, T, stride)
+    assert float(pcb[0]) == -7.0 and float(pab[0]) == -7.0
+    assert np.abs(pcb[1:].cpu().numpy().reshape(nq, stride) - ref_pc).max() <= ATOL_P
+    assert np.abs(pab[1:].cpu().numpy().reshape(nq, stride) - ref_pa).max() <= ATOL_P
+
+
 def test_readout_bad_arguments_flagged(lib):
     logits = np.zeros((4, 6), np.float32)
     pc = torch.full((2, 6), -7.0, device="cuda")
