@@ -226,6 +226,22 @@ def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None, n_
     return ms, nbytes
 
 
+def measure_h2d(torch, dev, stream, nbytes, reps=10):
+    """Host -> device copy rate from page-locked memory (one cudaMemcpyAsync per rep): GB/s."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        ev[1].record(stream)
+    torch.cuda.synchronize()
+    return nbytes * reps / (ev[0].elapsed_time(ev[1]) * 1e6)
+
+
 def measure_attn(lib, torch, B, stream, reps, warmup):
     """tree_attn_fwd alone over the rotating input sets, one work counter per chunk.
 
@@ -538,55 +554,40 @@ def run_gpu(args):
     attn_ms = [a.elapsed_time(b) for a, b in evs]
     assert int(B.status.item()) == 0, "device status word set"
 
-    # ---- end to end: inputs from pinned host memory, decisions back to the host.
-    # Two device input sets: the inputs of step s+1 are copied on a copy stream while
-    # step s computes (every copy lies inside the timed region).
+    # ---- end to end: inputs from pinned host memory, decisions back to the host, through
+    # tree_runtime_step_host: the runtime uploads each step's inputs into one of its two
+    # device sets on its own copy stream (while the previous step computes) and copies the
+    # decisions back on the compute stream; every copy lies inside the timed region.
     h = B.host
     pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in h.items()}
-    e2e_sets = []
-    for _ in range(2):
-        x = dict(q=torch.empty_like(B.sets[0]["q"]), k=torch.empty_like(B.sets[0]["k"]),
-                 v=torch.empty_like(B.sets[0]["v"]), o=torch.empty_like(B.sets[0]["o"]))
-        if B.nq:
-            x.update(logits=torch.empty_like(B.logits), n=torch.empty_like(B.nl), T=torch.empty_like(B.T))
-        e2e_sets.append(x)
-    copy_stream = torch.cuda.Stream(device=dev)
-    up = [torch.cuda.Event() for _ in range(2)]     # the copies into set b have run
-    done = [torch.cuda.Event() for _ in range(2)]   # the step reading set b has run
+    B.rt.attach_io(max_fwd=i.n_fwd, max_tot=i.n_tot, hq=w.hq, hkv=w.hkv, d=w.d,
+                   stride=w.letter_stride if B.nq else 0, max_slots=i.n_slots if B.nq else 0,
+                   max_questions=B.nq)
     out_pc = torch.empty(tuple(B.p_cal.shape), dtype=torch.float32).pin_memory() if B.nq else None
     out_ch = torch.empty(B.nq, dtype=torch.int32).pin_memory() if B.nq else None
     h2d = sum(v.numel() * v.element_size() for v in pin.values()) + i.dev_bytes
     d2h = (out_pc.numel() * 4 + out_ch.numel() * 4) if B.nq else 0
 
-    def e2e_step(s):
-        b = s & 1
-        x = e2e_sets[b]
-        copy_stream.wait_event(done[b])  # the step before the previous one no longer reads set b
-        with torch.cuda.stream(copy_stream):
-            for key in ("q", "k", "v", "logits", "n", "T"):
-                if key in x:
-                    x[key].copy_(pin[key], non_blocking=True)
-        up[b].record(copy_stream)
-        stream.wait_event(up[b])
-        B.step(0, stream, bufs=x)
-        done[b].record(stream)
-        if B.nq:
-            out_pc.copy_(B.p_cal, non_blocking=True)
-            out_ch.copy_(B.choice, non_blocking=True)
+    def e2e_step():
+        B.rt.step_host(B.spec, pin["q"], pin["k"], pin["v"], B.tab, i.max_pos, logits=pin.get("logits"),
+                       n_letters=pin.get("n"), temperature=pin.get("T"), p_cal=out_pc, choice=out_ch,
+                       status=B.status, stream=stream)
 
     for s in range(max(2, args.warmup)):
-        e2e_step(s)
+        e2e_step()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    copy_stream.wait_event(a)  # the first copies start inside the timed region
+    torch.cuda.synchronize()  # the runtime's copy stream starts the first upload after `a`
     for s in range(args.steps):
-        e2e_step(s)
-    b.record(stream)
+        e2e_step()
+    b.record(stream)  # after the last step's copies back (the step waited for its uploads)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b)
+    assert int(B.status.item()) == 0, "device status word set"
+    link_gbs = measure_h2d(torch, dev, stream, int(h2d))
 
     # ---- max over ranks
     total_ms, e2e_ms = max_over_ranks(dist, [total_ms, e2e_ms], dev)
@@ -618,7 +619,10 @@ def run_gpu(args):
                      "kernel": "tree_attn_fwd", "peak_source": f"{peaks['src']} bf16 sustained x 1 (f16 = bf16 rate)",
                      "launch_ms": round(attn_launch_ms, 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4)},
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4),
+                "call": "tree_runtime_step_host (page-locked host inputs, decisions back to the host)",
+                "h2d_link_gbs": round(link_gbs, 1),
+                "frac_of_link": round(h2d / (e2e_ms / args.steps * 1e6) / link_gbs, 4)},
         "gpu_launches": B.launches_per_step() * args.steps,
         "host_enqueue_ms_per_step": round(host_ms / args.steps, 4),
         "clocks": clk,

@@ -413,6 +413,63 @@ typedef struct {
 TREE_API int tree_runtime_step(tree_runtime_t *rt, const tree_step_args_t *args, tree_plan_info_t *info_out,
                                tree_stream_t stream);
 
+/*
+ * Host-buffer steps.  tree_runtime_attach_io gives the runtime two device sets
+ * of input and output buffers sized by `caps`, a copy stream of its own and
+ * the events that order them (it synchronises the device; calling it again
+ * replaces the sets).  tree_runtime_step_host then takes one batch whose
+ * inputs and outputs live in HOST memory:
+ *
+ *   copy stream:  wait until the step two calls back has finished with set b
+ *                 (b alternates), then q, k, v, logits, n_letters, temperature
+ *                 host -> set b (one cudaMemcpyAsync each)
+ *   stream:       wait for those copies, tree_runtime_step on set b, then the
+ *                 decisions (choice, p_cal, p_avg) and o, where the caller
+ *                 passes host buffers for them, device -> host
+ *
+ * so the upload of batch s+1 runs while batch s computes when the caller
+ * issues step s+1 before synchronising on `stream`.  The call returns once the
+ * work is enqueued: the host outputs are valid after `stream` has completed
+ * the step, and the host inputs may be rewritten once the step has reached
+ * `stream` (the copies of step s run before step s's compute starts).  Host
+ * buffers should be page-locked; pageable ones work but their copies do not
+ * overlap.  Resident key rows arrive with the keys as they are (already
+ * rotated, as for tree_runtime_step).  Errors: TREE_ERR_INVALID_ARG (no
+ * buffers attached, NULL inputs, sizes above caps or heads/d/stride different
+ * from caps), those of tree_runtime_step.
+ */
+typedef struct {
+  int32_t max_fwd;       /* forward (query) rows per batch */
+  int32_t max_tot;       /* key rows per batch (resident + forward) */
+  int32_t hq, hkv, d;    /* heads and head dimension of every step */
+  int32_t stride;        /* letters per logits row; 0 = no readout buffers */
+  int32_t max_slots;     /* readout slots (logits rows) per batch */
+  int32_t max_questions; /* questions per batch */
+} tree_io_caps_t;
+
+TREE_API int tree_runtime_attach_io(tree_runtime_t *rt, const tree_io_caps_t *caps);
+
+typedef struct {
+  const tree_spec_t *spec;        /* the batch (host memory, read during the call) */
+  const tree_plan_opts_t *opts;   /* may be NULL: defaults */
+  const void *q;                  /* host f16 [n_fwd, hq, d] pre-RoPE queries */
+  const void *k;                  /* host f16 [n_tot, hkv, d] keys (resident rows rotated) */
+  const void *v;                  /* host f16 [n_tot, hkv, d] */
+  void *o;                        /* host f16 [n_fwd, hq, d] output, or NULL: not copied back */
+  const float *cos_sin;           /* tree_rope_table on the device */
+  int32_t max_pos;
+  float scale;                    /* 0 = 1/sqrt(d) */
+  const float *logits;            /* host f32 [n_slots, stride]; the readout arguments may be NULL */
+  const int32_t *n_letters;       /*   when the batch has no questions: host [n_questions]        */
+  const float *temperature;       /* host [n_questions] */
+  float *p_cal, *p_avg;           /* host [n_questions, stride]; either may be NULL: not copied back */
+  int32_t *choice;                /* host [n_questions] or NULL */
+  int32_t *status;                /* device int32 or NULL */
+} tree_host_step_args_t;
+
+TREE_API int tree_runtime_step_host(tree_runtime_t *rt, const tree_host_step_args_t *args,
+                                    tree_plan_info_t *info_out, tree_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,7 +35,7 @@ EXPORTS = (
     "tree_plan_chunk", "tree_plan_tables", "tree_plan_upload", "tree_plan_upload_staged", "tree_rope_table",
     "tree_rope",
     "tree_attn_fwd", "tree_attn_fwd_noalloc", "readout_decide", "tree_runtime_create", "tree_runtime_destroy",
-    "tree_runtime_step",
+    "tree_runtime_step", "tree_runtime_attach_io", "tree_runtime_step_host",
     # include/tree_queue.h
     "tree_queue_default_opts", "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel",
     "tree_queue_info", "tree_queue_pop", "tree_batch_view", "tree_batch_free",
@@ -145,6 +145,20 @@ class _StepArgs(C.Structure):
                 ("status", C.c_void_p), ("attn_events", C.c_void_p * 2)]
 
 
+class IoCaps(C.Structure):
+    """``tree_io_caps_t``: sizes of the runtime's device sets for host-buffer steps."""
+    _fields_ = [(n, C.c_int32) for n in ("max_fwd", "max_tot", "hq", "hkv", "d", "stride", "max_slots",
+                                         "max_questions")]
+
+
+class _HostStepArgs(C.Structure):
+    _fields_ = [("spec", C.c_void_p), ("opts", C.c_void_p), ("q", C.c_void_p), ("k", C.c_void_p),
+                ("v", C.c_void_p), ("o", C.c_void_p), ("cos_sin", C.c_void_p), ("max_pos", C.c_int32),
+                ("scale", C.c_float), ("logits", C.c_void_p), ("n_letters", C.c_void_p),
+                ("temperature", C.c_void_p), ("p_cal", C.c_void_p), ("p_avg", C.c_void_p), ("choice", C.c_void_p),
+                ("status", C.c_void_p)]
+
+
 _vp = C.c_void_p
 _lib.tree_last_error.restype = C.c_char_p
 _lib.tree_version.restype = C.c_int
@@ -166,6 +180,8 @@ _lib.readout_decide.argtypes = [_vp, C.c_int32, _vp, _vp, _vp, _vp, C.c_int32, _
 _lib.tree_runtime_create.argtypes = [C.c_size_t, C.c_int32, C.POINTER(_vp)]
 _lib.tree_runtime_destroy.argtypes = [_vp]
 _lib.tree_runtime_step.argtypes = [_vp, C.POINTER(_StepArgs), C.POINTER(PlanInfo), _vp]
+_lib.tree_runtime_attach_io.argtypes = [_vp, C.POINTER(IoCaps)]
+_lib.tree_runtime_step_host.argtypes = [_vp, C.POINTER(_HostStepArgs), C.POINTER(PlanInfo), _vp]
 _lib.tree_gemm.argtypes = [_vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
 _lib.tree_gemm_ex.argtypes = [_vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
 _lib.tree_gemm_qkv.argtypes = [_vp, _vp, _vp, _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
@@ -196,7 +212,8 @@ _lib.tree_batch_free.argtypes = [_vp]
 for _f in ("tree_gemm", "tree_gemm_ex", "tree_gemm_qkv", "tree_rmsnorm", "tree_layer_workspace_bytes", "tree_layer_fwd",
            "tree_last_layer_workspace_bytes", "tree_last_layer_fwd", "tree_model_workspace_bytes", "tree_model_fwd",
            "tree_session_create", "tree_session_run", "tree_session_destroy",
-           "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_queue_default_opts",
+           "tree_runtime_create", "tree_runtime_destroy", "tree_runtime_step", "tree_runtime_attach_io",
+           "tree_runtime_step_host", "tree_queue_default_opts",
            "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel", "tree_queue_info",
            "tree_queue_pop", "tree_batch_view", "tree_batch_free"):
     getattr(_lib, _f).restype = C.c_int
@@ -480,6 +497,23 @@ class Runtime:
                 raise ValueError("attn_events: record each event once first (torch creates them lazily)")
             a.attn_events[0], a.attn_events[1] = h0, h1
         _check(_lib.tree_runtime_step(self.handle, C.byref(a), C.byref(self.info), _stream(stream)))
+        return self.info
+
+    def attach_io(self, max_fwd: int, max_tot: int, hq: int, hkv: int, d: int, stride: int = 0,
+                  max_slots: int = 0, max_questions: int = 0):
+        """Two device input/output sets and a copy stream for ``step_host`` (synchronises the device)."""
+        self.caps = IoCaps(max_fwd, max_tot, hq, hkv, d, stride, max_slots, max_questions)
+        _check(_lib.tree_runtime_attach_io(self.handle, C.byref(self.caps)))
+
+    def step_host(self, spec: Spec, q, k, v, cos_sin, max_pos: int, o=None, logits=None, n_letters=None,
+                  temperature=None, p_cal=None, p_avg=None, choice=None, status=None, stream=None,
+                  scale: float = 0.0) -> PlanInfo:
+        """One batch whose inputs and outputs are host buffers (page-locked torch tensors or raw
+        addresses).  Returns once enqueued: the outputs are valid after ``stream`` completes."""
+        a = _HostStepArgs(C.addressof(spec.spec), C.addressof(spec.opts), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                          _ptr(cos_sin), max_pos, scale, _ptr(logits), _ptr(n_letters), _ptr(temperature),
+                          _ptr(p_cal), _ptr(p_avg), _ptr(choice), _ptr(status))
+        _check(_lib.tree_runtime_step_host(self.handle, C.byref(a), C.byref(self.info), _stream(stream)))
         return self.info
 
 

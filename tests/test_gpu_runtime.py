@@ -201,3 +201,79 @@ def test_queue_batches_run_through_the_runtime(lib):
         now += 5.0
     assert steps >= 2 and q.info() == (0, 0)
     rt.close()
+
+
+def _pinned(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+
+
+def test_runtime_host_buffer_steps(lib):
+    """tree_runtime_step_host: inputs and outputs in page-locked host memory, batches issued back to
+    back (the runtime's two device sets in turn, uploads on its copy stream); every batch's output
+    and decisions equal the separate calls on the same batch bit for bit, p_avg the oracle's."""
+    w = synth.workload(2)
+    stride = 8
+    batches = [Batch(lib, w.forest, w.hq, w.hkv, w.d, w.seed + s, leaf1=w.leaf1, leaf2=w.leaf2, theta=w.theta,
+                     stride=stride) for s in range(3)]
+    rng = np.random.default_rng(12)
+    while True:  # a batch without questions, several chunks
+        f = synth.random_forest(rng, n_roots=3, max_blocks=20, max_len=150, resident_root=True)
+        try:
+            oplan.plan_forest(f, max_fwd=8192)
+            break
+        except oplan.PlanError:
+            continue
+    batches.insert(1, Batch(lib, f, w.hq, w.hkv, w.d, 99, theta=w.theta, stride=stride))
+    rt = _rt(lib)
+    with pytest.raises(lib.TreeError) as e:   # no device sets yet
+        bt = batches[0]
+        rt.step_host(bt.spec, _pinned(bt.q), _pinned(bt.k), _pinned(bt.v), bt.tab, bt.info.max_pos)
+    assert e.value.code == lib.TREE_ERR_INVALID_ARG
+    rt.attach_io(max_fwd=max(b.info.n_fwd for b in batches), max_tot=max(b.info.n_tot for b in batches), hq=w.hq,
+                 hkv=w.hkv, d=w.d, stride=stride, max_slots=max(b.info.n_slots for b in batches),
+                 max_questions=max(b.nq for b in batches))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for bt in batches + batches[:2]:
+        i, nq = bt.info, bt.nq
+        h = dict(q=_pinned(bt.q), k=_pinned(bt.k), v=_pinned(bt.v), logits=_pinned(bt.logits), n=_pinned(bt.n),
+                 T=_pinned(bt.T), o=torch.full((i.n_fwd, bt.hq, bt.d), 7.0, dtype=torch.float16).pin_memory(),
+                 pc=torch.full((max(nq, 1), stride), -1.0).pin_memory(),
+                 pa=torch.full((max(nq, 1), stride), -1.0).pin_memory(),
+                 ch=torch.full((max(nq, 1),), -9, dtype=torch.int32).pin_memory())
+        info = rt.step_host(bt.spec, h["q"], h["k"], h["v"], bt.tab, i.max_pos, o=h["o"], logits=h["logits"],
+                            n_letters=h["n"], temperature=h["T"], p_cal=h["pc"], p_avg=h["pa"], choice=h["ch"],
+                            status=st)
+        assert info.n_fwd == i.n_fwd and info.n_questions == nq
+        outs.append((bt, h))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for bt, h in outs:
+        ref = bt.reference()
+        assert torch.equal(h["o"], ref["o"].cpu())
+        if bt.nq:
+            assert torch.equal(h["pc"], ref["pc"].cpu())
+            assert torch.equal(h["ch"], ref["ch"].cpu())
+            _, qm = oplan.plan_forest(w.forest, leaf1=w.leaf1, leaf2=w.leaf2)
+            _, ref_pa, _ = ordo.decide(bt.logits, qm["r1"], qm["r2"], bt.n, bt.T, stride)
+            assert np.abs(h["pa"].numpy() - ref_pa).max() <= 1e-5
+        else:
+            assert float(h["pc"][0, 0]) == -1.0 and int(h["ch"][0]) == -9   # nothing to decide: untouched
+    rt.close()
+
+
+def test_runtime_host_capacity_checked(lib):
+    w = synth.workload(2)
+    bt = Batch(lib, w.forest, w.hq, w.hkv, w.d, w.seed, leaf1=w.leaf1, leaf2=w.leaf2)
+    rt = _rt(lib)
+    rt.attach_io(max_fwd=bt.info.n_fwd - 128, max_tot=bt.info.n_tot, hq=w.hq, hkv=w.hkv, d=w.d, stride=8,
+                 max_slots=bt.info.n_slots, max_questions=bt.nq)
+    h = [_pinned(x) for x in (bt.q, bt.k, bt.v, bt.logits, bt.n, bt.T)]
+    with pytest.raises(lib.TreeError) as e:
+        rt.step_host(bt.spec, h[0], h[1], h[2], bt.tab, bt.info.max_pos, logits=h[3], n_letters=h[4],
+                     temperature=h[5])
+    assert e.value.code == lib.TREE_ERR_INVALID_ARG
+    with pytest.raises(lib.TreeError) as e:
+        rt.attach_io(max_fwd=128, max_tot=128, hq=6, hkv=4, d=64)   # hq not a multiple of hkv
+    assert e.value.code == lib.TREE_ERR_INVALID_ARG
+    rt.close()
