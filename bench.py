@@ -173,16 +173,16 @@ class Batch:
         return 1 + 2 * len(self.chunks) + (1 if self.nq else 0)
 
 
-def measure_rope(lib, torch, B, stream, reps=40, warmup=None, keys_only=False):
+def measure_rope(lib, torch, B, stream, reps=40, warmup=None, keys_only=False, timing_forms=False):
     """tree_rope alone over the rotating input sets (Q and K, or K only): algorithmic GB/s."""
     w, i = B.w, B.info
     n_sets = len(B.sets)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
 
-    def run(s):
+    def run(s, st=None):
         for c in range(len(B.chunks)):
             lib.tree_rope(B.plan, B.pdev, c, None if keys_only else B.views[s][c][0], B.sets[s]["k"], w.hq, w.hkv,
-                          w.d, B.tab, i.max_pos, stream)
+                          w.d, B.tab, i.max_pos, stream if st is None else st)
     for s in range(n_sets if warmup is None else warmup):
         run(s % n_sets)
     ev[0].record(stream)
@@ -194,10 +194,13 @@ def measure_rope(lib, torch, B, stream, reps=40, warmup=None, keys_only=False):
     # read + write of every forward row rotated, plus its position
     heads = w.hkv if keys_only else w.hq + w.hkv
     nbytes = 2 * i.n_fwd * heads * w.d * 2 + 4 * i.n_fwd
-    return ms, nbytes
+    if not timing_forms:
+        return ms, nbytes
+    fns = [lambda st, x=x: run(x, st) for x in range(n_sets)]
+    return ms, nbytes, graph_ms(torch, fns, reps), single_call_us(torch, fns[0], stream)
 
 
-def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None, n_questions=65536):
+def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None, n_questions=65536, timing_forms=False):
     """readout_decide on n_questions (2-10 letters each) over rotating buffer sets: algorithmic GB/s."""
     b = synth.draw_readout_batch(n_questions)
     nq, stride = len(b["r1"]), b["stride"]
@@ -208,9 +211,9 @@ def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None, n_
                          T=torch.from_numpy(b["temperature"]).to(dev),
                          pc=torch.empty((nq, stride), device=dev), ch=torch.empty(nq, dtype=torch.int32, device=dev)))
 
-    def run(x):
+    def run(x, st=None):
         lib.readout_decide(x["logits"], stride, x["r1"], x["r2"], x["n"], x["T"], nq, x["pc"], None, x["ch"], None,
-                           stream)
+                           stream if st is None else st)
     for r in range(n_sets if warmup is None else warmup):
         run(sets[r % n_sets])
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -223,7 +226,52 @@ def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None, n_
     n = b["n_letters"].astype(np.int64)
     # logits of both orders, r1/r2/n/T, the zero-padded p_cal row, the choice
     nbytes = int((2 * n * 4).sum() + 16 * nq + 4 * stride * nq + 4 * nq)
-    return ms, nbytes
+    if not timing_forms:
+        return ms, nbytes
+    fns = [lambda st, x=x: run(x, st) for x in sets]
+    return ms, nbytes, graph_ms(torch, fns, reps), single_call_us(torch, fns[0], stream)
+
+
+def graph_ms(torch, fns, reps):
+    """Mean time of one call when the calls `fns` (launchers taking a stream, one per rotating input
+    set) run back to back from a captured CUDA graph, free of host launch overhead: ms."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for f in fns:
+            f(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        for f in fns:
+            f(cs)
+    g.replay()
+    torch.cuda.synchronize()
+    n = max(1, reps // len(fns))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    cur = torch.cuda.current_stream()
+    ev[0].record(cur)
+    for _ in range(n):
+        g.replay()
+    ev[1].record(cur)
+    torch.cuda.synchronize()
+    return ev[0].elapsed_time(ev[1]) / (n * len(fns))
+
+
+def single_call_us(torch, f, stream, n=21):
+    """Median device time of one call issued alone (the stream idle before it, launch latency included)."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ts = []
+    for _ in range(n):
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        f(stream)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        ts.append(ev[0].elapsed_time(ev[1]))
+    return statistics.median(ts) * 1e3
 
 
 def measure_h2d(torch, dev, stream, nbytes, reps=10):
@@ -452,11 +500,13 @@ def run_only(args):
         print(json.dumps(line), flush=True)
         return
     if args.only == "readout":
-        ms, nbytes = measure_readout(lib, torch, dev, stream, reps=args.steps, n_sets=args.sets or 16,
-                                     warmup=args.warmup, n_questions=args.questions)
+        ms, nbytes, gms, one_us = measure_readout(lib, torch, dev, stream, reps=args.steps, n_sets=args.sets or 16,
+                                                  warmup=args.warmup, n_questions=args.questions, timing_forms=True)
         gbs = nbytes / ms / 1e6
         line.update(workload=f"{args.questions:,} questions, 2-10 letters", us=round(ms * 1e3, 2), bytes=nbytes,
-                    achieved=round(gbs, 1), unit="GB/s", peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4))
+                    achieved=round(gbs, 1), unit="GB/s", peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4),
+                    graph_us=round(gms * 1e3, 2), graph_frac=round(nbytes / gms / 1e6 / peaks["hbm"], 4),
+                    single_call_us=round(one_us, 2))
     else:
         w = synth.workload(args.workload)
         B = Batch(lib, torch, w, dev, n_sets=args.sets or N_SETS, tiling=args.tiling)
@@ -471,17 +521,27 @@ def run_only(args):
                         peak=peaks["tc"], frac=round(tf / peaks["tc"], 4), gemms=r["gemms"],
                         weights="random init (no trained weights)")
         elif args.only == "rope":
-            ms, nbytes = measure_rope(lib, torch, B, stream, reps=args.steps, warmup=args.warmup,
-                                      keys_only=args.keys_only)
+            ms, nbytes, gms, one_us = measure_rope(lib, torch, B, stream, reps=args.steps, warmup=args.warmup,
+                                                   keys_only=args.keys_only, timing_forms=True)
             line["keys_only"] = args.keys_only
             gbs = nbytes / ms / 1e6
             line.update(us=round(ms * 1e3, 2), bytes=nbytes, achieved=round(gbs, 1), unit="GB/s",
-                        peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4))
+                        peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4), graph_us=round(gms * 1e3, 2),
+                        graph_frac=round(nbytes / gms / 1e6 / peaks["hbm"], 4), single_call_us=round(one_us, 2))
         else:
             ms = measure_attn(lib, torch, B, stream, reps=args.steps, warmup=args.warmup)
-            tf = 4.0 * w.d * w.hq * B.info.pairs / (ms / 1e3) / 1e12
-            line.update(us_per_forward=round(ms * 1e3, 2), chunks=len(B.chunks), visible_pairs=B.info.pairs,
-                        achieved=round(tf, 2), unit="TFLOP/s", peak=peaks["tc"], frac=round(tf / peaks["tc"], 4))
+            i = B.info
+            flops = 4.0 * w.d * w.hq * i.pairs
+            tf = flops / (ms / 1e3) / 1e12
+            # Q and O of every forward row, K and V of every key row, the plan image: each once
+            nbytes = 2 * i.n_fwd * w.hq * w.d * 2 + 2 * i.n_tot * w.hkv * w.d * 2 + i.dev_bytes
+            gbs = nbytes / ms / 1e6
+            ridge = peaks["tc"] * 1e12 / (peaks["hbm"] * 1e9)  # flop per byte where the two roofs meet
+            line.update(us_per_forward=round(ms * 1e3, 2), chunks=len(B.chunks), visible_pairs=i.pairs,
+                        achieved=round(tf, 2), unit="TFLOP/s", peak=peaks["tc"], frac=round(tf / peaks["tc"], 4),
+                        bytes=nbytes, flop_per_byte=round(flops / nbytes, 1), gbs=round(gbs, 1),
+                        hbm_frac=round(gbs / peaks["hbm"], 4),
+                        bound="tensor" if flops / nbytes >= ridge else "hbm")
     line["peak_source"] = peaks["src"]
     print(json.dumps(line), flush=True)
 
@@ -627,16 +687,19 @@ def run_gpu(args):
         "host_enqueue_ms_per_step": round(host_ms / args.steps, 4),
         "clocks": clk,
     }
-    rope_ms, rope_bytes = measure_rope(lib, torch, B, stream)
-    ro_ms, ro_bytes = measure_readout(lib, torch, dev, stream)
+    rope_ms, rope_bytes, rope_gms, rope_one = measure_rope(lib, torch, B, stream, timing_forms=True)
+    ro_ms, ro_bytes, ro_gms, ro_one = measure_readout(lib, torch, dev, stream, timing_forms=True)
     line["kernels"] = {
         "tree_rope": {"bound": "hbm", "us": round(rope_ms * 1e3, 2), "bytes": rope_bytes,
                       "achieved": round(rope_bytes / rope_ms / 1e6, 1), "peak": peaks["hbm"], "unit": "GB/s",
                       "frac": round(rope_bytes / rope_ms / 1e6 / peaks["hbm"], 4),
-                      "note": f"{N_SETS} rotating Q/K sets (> L2)"},
+                      "graph_us": round(rope_gms * 1e3, 2), "single_call_us": round(rope_one, 2),
+                      "note": f"{N_SETS} rotating Q/K sets (> L2); us: launches back to back on the stream, "
+                              "graph_us: the same from a CUDA graph, single_call_us: one launch on an idle stream"},
         "readout_decide_65536q": {"bound": "hbm", "us": round(ro_ms * 1e3, 2), "bytes": ro_bytes,
                                   "achieved": round(ro_bytes / ro_ms / 1e6, 1), "peak": peaks["hbm"],
                                   "unit": "GB/s", "frac": round(ro_bytes / ro_ms / 1e6 / peaks["hbm"], 4),
+                                  "graph_us": round(ro_gms * 1e3, 2), "single_call_us": round(ro_one, 2),
                                   "note": "65,536 questions, 2-10 letters, 16 rotating buffer sets (> L2)"},
         "tree_attn_fwd": {"bound": "tensor", "us": round(attn_launch_ms * 1e3, 2), "flops": flops_launch,
                           "achieved": round(achieved, 2), "peak": peaks["tc"], "unit": "TFLOP/s",
