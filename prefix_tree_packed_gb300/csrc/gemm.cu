@@ -215,12 +215,23 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     int tc = 0;
     for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++tc) {
       const int b = tc & 1;
-      if (!gwait_warp(b_af(b), (tc / 2) & 1, abort, a.status)) break;
-      fence_after();
       int tm, tn;
       tile_of(a, t, tm, tn);
       const int row = tm * GBM + 32 * qd + lane, n0 = tn * a.bn;
       const bool row_ok = row < a.m;
+      // the residual row is read before the accumulator is ready: its loads are all
+      // in flight while the tile's last MMAs run
+      uint4 res[BN / 8];
+      if (a.epi == TREE_GEMM_RESIDUAL) {
+        const __half *rrow = a.r + (size_t)row * a.n;
+#pragma unroll
+        for (int u = 0; u < BN / 8; ++u) {
+          const int c = n0 + 8 * u;
+          res[u] = (row_ok && c < a.n) ? *reinterpret_cast<const uint4 *>(rrow + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (!gwait_warp(b_af(b), (tc / 2) & 1, abort, a.status)) break;
+      fence_after();
       __half *crow = a.c + (size_t)row * a.n;
       const uint32_t acc = t_lane + (uint32_t)(b * BN);
       if (a.epi == TREE_GEMM_SWIGLU) {
@@ -244,7 +255,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           }
         }
       } else {
-        const __half *rrow = a.r ? a.r + (size_t)row * a.n : nullptr;
+#pragma unroll
         for (int ch = 0; ch < BN / 32; ++ch) {
           uint32_t x[32];
           tmem_ld32(acc + 32 * ch, x);
@@ -258,8 +269,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x[8 * v + e]);
             if (a.epi == TREE_GEMM_RESIDUAL) {
-              const uint4 rv = *reinterpret_cast<const uint4 *>(rrow + c);
-              const __half2 *rh = reinterpret_cast<const __half2 *>(&rv);
+              const __half2 *rh = reinterpret_cast<const __half2 *>(&res[4 * ch + v]);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float2 r2 = __half22float2(rh[e]);
