@@ -54,8 +54,8 @@ TREE_API int tree_gemm(const void *a, const void *b, void *c, const void *r, int
  * tree_gemm with the output tile width chosen by the caller: tile_n 256 (wide
  * tiles, for large m), 64 (narrow tiles: more of them, so a small m still
  * spreads the weight reads over every SM), or 0 (tree_gemm's choice: narrow
- * when m <= 2048 and wide tiles would be fewer than the SMs, else wide).  The width changes only the speed:
- * every output is the same f32 sum over k in the same order.
+ * for m <= 384, except with the SwiGLU epilogue, else wide).  The width changes
+ * only the speed: every output is the same f32 sum over k in the same order.
  */
 TREE_API int tree_gemm_ex(const void *a, const void *b, void *c, const void *r, int32_t m, int32_t n, int32_t k,
                           int32_t epi, int32_t tile_n, int32_t *status, tree_stream_t stream);

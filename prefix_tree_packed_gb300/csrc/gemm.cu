@@ -353,6 +353,13 @@ int launch_gemm(const void *a, const void *b, void *c, const void *r, int32_t m,
   return launch_status("tree_gemm");
 }
 
+// Narrow tiles for at most three row tiles (a single request, the readout rows):
+// there the weights' reads dominate and 64-column tiles spread them over more
+// SMs.  From four row tiles on, and for the SwiGLU projection at any m, wide
+// tiles measured faster (Llama-1B shapes: down at m = 300 32 vs 39 us narrow
+// first, at m = 600 60 vs 40 us wide first).
+bool narrow_tiles(int32_t m, int32_t epi) { return (m + GBM - 1) / GBM <= 3 && epi != TREE_GEMM_SWIGLU; }
+
 }  // namespace
 }  // namespace tree
 
@@ -370,13 +377,7 @@ extern "C" TREE_API int tree_gemm_ex(const void *a, const void *b, void *c, cons
   if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (r && !aligned16(r)))
     return fail(TREE_ERR_UNSUPPORTED, "tree_gemm: tensors must be 16-byte aligned");
   if (m == 0) return TREE_OK;
-  if (tile_n == 0) {
-    // wide tiles, unless m is small (the weights' reads dominate) and wide tiles would
-    // leave SMs without work
-    const int64_t wide = (int64_t)((m + GBM - 1) / GBM) * ((n + (epi == TREE_GEMM_SWIGLU ? 127 : 255)) /
-                                                           (epi == TREE_GEMM_SWIGLU ? 128 : 256));
-    tile_n = (m <= 2048 && wide < sm_count()) ? 64 : 256;
-  }
+  if (tile_n == 0) tile_n = narrow_tiles(m, epi) ? 64 : 256;
   const cudaStream_t s = as_stream(stream);
   return tile_n == 256 ? launch_gemm<256>(a, b, c, r, m, n, k, epi, status, s)
                        : launch_gemm<64>(a, b, c, r, m, n, k, epi, status, s);
@@ -399,9 +400,8 @@ extern "C" TREE_API int tree_gemm_qkv(const void *a, const void *wqkv, void *q, 
     return fail(TREE_ERR_UNSUPPORTED, "tree_gemm_qkv: tensors must be 16-byte aligned");
   if (m == 0) return TREE_OK;
   const int n = nq + 2 * nkv;
-  const int64_t wide = (int64_t)((m + GBM - 1) / GBM) * ((n + 255) / 256);
   const cudaStream_t s = as_stream(stream);
-  return (m <= 2048 && wide < sm_count())
+  return narrow_tiles(m, TREE_GEMM_STORE)
              ? launch_gemm<64>(a, wqkv, q, nullptr, m, n, kdim, kEpiQKV, status, s, nq, nkv, k, v)
              : launch_gemm<256>(a, wqkv, q, nullptr, m, n, kdim, kEpiQKV, status, s, nq, nkv, k, v);
 }
