@@ -68,7 +68,20 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_slots(const uint4 *s
   const int row = blockIdx.x * kGatherWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= m) return;
   const size_t s = (size_t)(slot_tok[row] - n_res);
-  for (int i = lane; i < vec_per_row; i += 32) dst[(size_t)row * vec_per_row + i] = src[s * vec_per_row + i];
+  // chunks of 8 loads per lane in flight before their stores (dst never overlaps src)
+  for (int i0 = 0; i0 < vec_per_row; i0 += 256) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + lane + 32 * u;
+      if (i < vec_per_row) v[u] = src[s * vec_per_row + i];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + lane + 32 * u;
+      if (i < vec_per_row) dst[(size_t)row * vec_per_row + i] = v[u];
+    }
+  }
 }
 
 int gather(const __half *src, int cols, const int32_t *slot_tok, int n_res, __half *dst, int m, cudaStream_t s) {

@@ -5,8 +5,9 @@
 //   y = f16( f16(x / sqrt(mean(x^2) + eps)) * w )
 //
 // One warp per row: a first pass sums the squares in f32 (8 values per lane
-// and load), a second re-reads the row (now in L1) and writes y.  HBM-bound:
-// x read once from memory, y written once.
+// and load), a second re-reads the row (now in L1) and writes y.  HBM-bound
+// for many rows (x read once from memory, y written once); for a few rows the
+// memory latency decides, so each pass issues its loads in chunks.
 
 #include "common.cuh"
 #include "sm103.cuh"
@@ -16,6 +17,7 @@ namespace tree {
 namespace {
 
 constexpr int kNormWarps = 8;
+constexpr int kChunk = 8;  // 16-byte loads in flight per lane
 
 __global__ void __launch_bounds__(kNormWarps * 32) rmsnorm_kernel(const __half *x,
                                                                    const __half *__restrict__ w,
@@ -27,15 +29,25 @@ __global__ void __launch_bounds__(kNormWarps * 32) rmsnorm_kernel(const __half *
   if (row >= rows) return;
   const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)row * cols);
   const int nv = cols / 8;
+  // chunks of up to kChunk 16-byte loads per lane are issued together, so a row
+  // costs one memory latency per chunk (two chunks at hidden 4096)
   float ss = 0.f;
-  for (int i = lane; i < nv; i += 32) {
-    const uint4 v = xr[i];
-    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+  for (int i0 = 0; i0 < nv; i0 += 32 * kChunk) {
+    uint4 v[kChunk];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __half22float2(h[e]);
-      ss = fmaf(f.x, f.x, ss);
-      ss = fmaf(f.y, f.y, ss);
+    for (int u = 0; u < kChunk; ++u) {
+      const int i = i0 + lane + 32 * u;
+      v[u] = i < nv ? xr[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      const __half2 *h = reinterpret_cast<const __half2 *>(&v[u]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h[e]);
+        ss = fmaf(f.x, f.x, ss);
+        ss = fmaf(f.y, f.y, ss);
+      }
     }
   }
 #pragma unroll
@@ -43,19 +55,33 @@ __global__ void __launch_bounds__(kNormWarps * 32) rmsnorm_kernel(const __half *
   const float inv = rsqrtf(ss / (float)cols + eps);
   const uint4 *wr = reinterpret_cast<const uint4 *>(w);
   uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)row * cols);
-  for (int i = lane; i < nv; i += 32) {
-    const uint4 v = xr[i], wv = wr[i];
-    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-    const __half2 *hw = reinterpret_cast<const __half2 *>(&wv);
-    uint4 out;
-    __half2 *ho = reinterpret_cast<__half2 *>(&out);
+  // y may be x: each lane stores only elements it has already loaded
+  for (int i0 = 0; i0 < nv; i0 += 32 * kChunk) {
+    uint4 v[kChunk], wv[kChunk];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __half22float2(h[e]);
-      const __half2 n = __floats2half2_rn(f.x * inv, f.y * inv);
-      ho[e] = __hmul2(n, hw[e]);
+    for (int u = 0; u < kChunk; ++u) {
+      const int i = i0 + lane + 32 * u;
+      if (i < nv) {
+        v[u] = xr[i];
+        wv[u] = wr[i];
+      }
     }
-    yr[i] = out;
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      const int i = i0 + lane + 32 * u;
+      if (i >= nv) continue;
+      const __half2 *h = reinterpret_cast<const __half2 *>(&v[u]);
+      const __half2 *hw = reinterpret_cast<const __half2 *>(&wv[u]);
+      uint4 out;
+      __half2 *ho = reinterpret_cast<__half2 *>(&out);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h[e]);
+        const __half2 n = __floats2half2_rn(f.x * inv, f.y * inv);
+        ho[e] = __hmul2(n, hw[e]);
+      }
+      yr[i] = out;
+    }
   }
 }
 
