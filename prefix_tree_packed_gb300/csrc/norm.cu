@@ -17,7 +17,8 @@ namespace tree {
 namespace {
 
 constexpr int kNormWarps = 8;
-constexpr int kChunk = 8;  // 16-byte loads in flight per lane
+constexpr int kChunk = 8;   // 16-byte loads in flight per lane, first pass (x from memory)
+constexpr int kChunk2 = 4;  // second pass (x again, now cached, and w): fewer registers
 
 __global__ void __launch_bounds__(kNormWarps * 32) rmsnorm_kernel(const __half *x,
                                                                    const __half *__restrict__ w,
@@ -56,10 +57,10 @@ __global__ void __launch_bounds__(kNormWarps * 32) rmsnorm_kernel(const __half *
   const uint4 *wr = reinterpret_cast<const uint4 *>(w);
   uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)row * cols);
   // y may be x: each lane stores only elements it has already loaded
-  for (int i0 = 0; i0 < nv; i0 += 32 * kChunk) {
-    uint4 v[kChunk], wv[kChunk];
+  for (int i0 = 0; i0 < nv; i0 += 32 * kChunk2) {
+    uint4 v[kChunk2], wv[kChunk2];
 #pragma unroll
-    for (int u = 0; u < kChunk; ++u) {
+    for (int u = 0; u < kChunk2; ++u) {
       const int i = i0 + lane + 32 * u;
       if (i < nv) {
         v[u] = xr[i];
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(kNormWarps * 32) rmsnorm_kernel(const __half *
       }
     }
 #pragma unroll
-    for (int u = 0; u < kChunk; ++u) {
+    for (int u = 0; u < kChunk2; ++u) {
       const int i = i0 + lane + 32 * u;
       if (i >= nv) continue;
       const __half2 *h = reinterpret_cast<const __half2 *>(&v[u]);
