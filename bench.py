@@ -10,15 +10,18 @@ theta 500000, 4-6 letters per question, T in {0.7, 1.0, 1.3}.
 
 Printed (rank 0, one JSON line): tokens/s of the whole job, the attention
 kernel's TFLOP/s against the measured tensor peak (roofline), an end-to-end
-figure with host<->device copies inside the timed region, SM clocks sampled
-during the timed region, and the CPU oracle timed on the host as a baseline.
+figure through tree_runtime_step_host (inputs from page-locked host memory,
+decisions back, every copy inside the timed region) beside the measured
+host-to-device link rate, SM clocks sampled during the timed region, RoPE and
+readout against HBM (back to back, from a CUDA graph, and one call alone), and
+the CPU oracle timed on the host as a baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl reference]
-  python bench.py --only attn|rope|readout [--workload N] [--steps K] [--warmup W] [--sets S]
+  python bench.py --only attn|rope|readout|layer|model [--workload N] [--steps K] [--warmup W] [--sets S]
 
---only times one kernel by itself (CUDA events, rotating input sets) and prints
-one JSON line for it; it is also the small, fixed command that profiler captures
-are taken on.
+--only times one kernel (or the Llama layer, or the whole decision forward) by
+itself (CUDA events, rotating input sets) and prints one JSON line for it; it is
+also the small, fixed command that profiler captures are taken on.
 """
 from __future__ import annotations
 
