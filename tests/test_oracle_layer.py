@@ -64,3 +64,42 @@ def test_letter_logits_special_case():
     got = ol.letter_logits(plan, y, wf, wl, eps=0.0)
     rows = y[[5, 1, 3]].astype(np.int64) * wf.astype(np.int64)
     np.testing.assert_array_equal(got, rows @ wl.astype(np.int64).T)
+
+
+def _chain_layer_inputs(n: int, hidden: int, hq: int, hkv: int, d: int, ffn: int):
+    import synth
+    from oracle import plan as oplan
+    forest = synth.Forest(np.array([-1], np.int32), np.array([n], np.int32), np.zeros(1, np.uint64),
+                          np.zeros(1, np.uint8))
+    plan, _ = oplan.plan_forest(forest)
+    w, x, rk, rv = synth.draw_layer(n, 0, hidden, hq, hkv, d, ffn, seed=11)
+    return plan, w, x, rk, rv
+
+
+def test_layer_residual_adds_pass_their_input_through_zero_projections():
+    # wo = 0: the attention block's residual add returns the layer input; wd = 0: the MLP's residual
+    # add returns the attention block's output h (which differs from the input when wo != 0)
+    hidden, hq, hkv, d, ffn = 32, 4, 2, 16, 48
+    plan, w, x, rk, rv = _chain_layer_inputs(20, hidden, hq, hkv, d, ffn)
+    _, _, _, _, _, h = ol.layer(plan, x, rk, rv, dict(w, wo=np.zeros_like(w["wo"])), hq, hkv, d, 500000.0)
+    np.testing.assert_array_equal(h, x)
+    y, _, _, _, _, h = ol.layer(plan, x, rk, rv, dict(w, wd=np.zeros_like(w["wd"])), hq, hkv, d, 500000.0)
+    assert not np.array_equal(h, x)
+    np.testing.assert_array_equal(y, h)
+
+
+def test_layer_with_zero_queries_averages_the_values():
+    # wq = 0: every score is 0, so on a chain token i's attention output is the plain mean of the
+    # value rows 0..i of its kv head (the values are the normalised input times wv, rounded to f16)
+    hidden, hq, hkv, d, ffn = 32, 4, 2, 16, 48
+    n = 24
+    plan, w, x, rk, rv = _chain_layer_inputs(n, hidden, hq, hkv, d, ffn)
+    w = dict(w, wq=np.zeros_like(w["wq"]))
+    _, q, _, v, o16, _ = ol.layer(plan, x, rk, rv, w, hq, hkv, d, 500000.0)
+    assert not np.any(q)
+    xn = ol.rmsnorm(x, w["w_in"], 1e-5).astype(np.float64)
+    vv = (xn @ w["wv"].astype(np.float64).T).astype(np.float16).astype(np.float64).reshape(n, hkv, d)
+    np.testing.assert_array_equal(v.astype(np.float64), vv)
+    mean = np.cumsum(vv, axis=0) / np.arange(1, n + 1)[:, None, None]
+    want = np.repeat(mean, hq // hkv, axis=1).reshape(n, hq * d)   # q head h reads kv head h // 2
+    np.testing.assert_allclose(o16.astype(np.float64), want, rtol=2 ** -10, atol=2 ** -24)
