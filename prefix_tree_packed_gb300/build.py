@@ -48,7 +48,7 @@ def _compile(src: str, cuda: str, verbose: bool) -> str:
         cmd = [os.path.join(cuda, "bin", "nvcc"), "-O3", "-std=c++17", *ARCH, "-lineinfo",
                "-Xcompiler", "-fPIC,-fvisibility=hidden", "-Xptxas", "-v" if verbose else "-O3", *inc, "-c", src, "-o", obj]
     else:
-        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall", *inc, "-c", src, "-o", obj]
+        cmd = ["g++", "-O3", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall", *inc, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"compile failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

@@ -458,12 +458,11 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   im[6] = (int32_t)P.slot_tok.size();
   im[7] = P.n_questions;
   int32_t *pos = im + P.off_pos, *send = im + P.off_send;
-  for (int32_t i = 0; i < nbc; ++i) {
-    const int32_t st = bstart[i], len = blen[i], p0 = bpos0[i], se = bsend[i];
-    for (int32_t t = 0; t < len; ++t) {
-      pos[st + t] = p0 + t;
-      send[st + t] = se;
-    }
+  for (int32_t i = 0; i < nbc; ++i) {  // two plain fills per block (each vectorises on its own)
+    const int32_t st = bstart[i], len = blen[i], p0 = bpos0[i];
+    int32_t *pp = pos + st;
+    for (int32_t t = 0; t < len; ++t) pp[t] = p0 + t;
+    std::fill(send + st, send + st + len, bsend[i]);
   }
   std::fill(send + P.n_tot, send + n_send, 0);
   for (size_t t = 0; t < P.qt_row0.size(); ++t) {
@@ -485,21 +484,38 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   std::copy(P.slot_tok.begin(), P.slot_tok.end(), im + P.off_slot_tok);
   std::copy(P.r1.begin(), P.r1.end(), im + P.off_r1);
   std::copy(P.r2.begin(), P.r2.end(), im + P.off_r2);
-  // run tables of the key tiles
+  // run tables of the key tiles: maximal runs of equal send.  A tile's keys fall
+  // into a few block segments of constant send (padding past the last token:
+  // send 0), so the runs are built segment by segment.
   std::fill(im + P.off_runs, im + P.off_runs + (size_t)n_kvt * kRunWords, 0);
-  for (int32_t t = 0; t < n_kvt; ++t) {
-    int32_t *tb = im + P.off_runs + (size_t)t * kRunWords;
-    const int32_t *sd = send + (size_t)t * kTile;
-    int32_t n = 0;
-    for (int32_t c = 0; c < kTile; ++c) {
-      if (c == 0 || sd[c] != sd[c - 1]) {
-        if (n < kMaxRuns) tb[4 + n] = sd[c];
-        ++n;
-      }
-      if (n <= kMaxRuns) tb[20 + 4 * (n - 1) + c / 32] |= (int32_t)(1u << (c % 32));
+  {
+    int32_t b = 0;  // first block that ends after the tile's first key
+    for (int32_t t = 0; t < n_kvt; ++t) {
+      int32_t *tb = im + P.off_runs + (size_t)t * kRunWords;
+      const int32_t j0 = t * kTile, j1 = j0 + kTile;
+      while (b < nbc && bstart[b] + blen[b] <= j0) ++b;
+      int32_t n = 0, last = 0;
+      auto segment = [&](int32_t lo, int32_t hi, int32_t value) {  // keys [lo, hi) of the tile
+        if (n == 0 || value != last) {
+          if (n < kMaxRuns) tb[4 + n] = value;
+          ++n;
+          last = value;
+        }
+        if (n > kMaxRuns) return;
+        int32_t *bits = tb + 20 + 4 * (n - 1);
+        for (int32_t c = lo - j0; c < hi - j0;) {  // set bits c .. (word end or hi) at once
+          const int32_t wd = c >> 5, e = std::min(hi - j0, (wd + 1) << 5);
+          const uint32_t lo_bit = (uint32_t)(c & 31), cnt = (uint32_t)(e - c);
+          bits[wd] |= (int32_t)((cnt == 32 ? 0xffffffffu : ((1u << cnt) - 1u)) << lo_bit);
+          c = e;
+        }
+      };
+      for (int32_t i = b; i < nbc && bstart[i] < j1; ++i)
+        segment(std::max(j0, bstart[i]), std::min(j1, bstart[i] + blen[i]), bsend[i]);
+      if (j1 > P.n_tot) segment(std::max(j0, P.n_tot), j1, 0);
+      tb[0] = n;
+      if (n > kMaxRuns) std::fill(tb + 4, tb + kRunWords, 0);  // only the count is meaningful
     }
-    tb[0] = n;
-    if (n > kMaxRuns) std::fill(tb + 4, tb + kRunWords, 0);  // only the count is meaningful
   }
   // zero the alignment gaps so the image is fully defined
   auto zero_gap = [&](size_t from, size_t to) { std::fill(im + from, im + to, 0); };
