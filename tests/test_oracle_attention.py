@@ -97,6 +97,36 @@ def test_result_does_not_depend_on_batch_neighbours():
     np.testing.assert_allclose(op[dst], oa[src], rtol=0, atol=1e-13)
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_sibling_order_does_not_change_any_token(seed):
+    # the same tree given with its children in another input order packs in another order; every
+    # token, identified by (input block, offset), keeps its Q/K/V and must keep its output
+    rng = np.random.default_rng(300 + seed)
+    parent = [-1, 0, 0, 0, 1, 1, 2, 3, 3]
+    length = [int(x) for x in rng.integers(1, 9, len(parent))]
+    # new input index -> old: every sibling group reversed, then random orders
+    order = [0, 3, 2, 1, 5, 4, 6, 8, 7] if seed == 0 else [0] + [int(x) + 1 for x in rng.permutation(len(parent) - 1)]
+    new_of = {old: new for new, old in enumerate(order)}
+    parent2 = [-1 if parent[o] < 0 else new_of[parent[o]] for o in order]
+    length2 = [length[o] for o in order]
+    pa, _ = oplan.make_plan(parent, length, np.zeros(len(parent), np.uint64), [0] * len(parent))
+    pb, _ = oplan.make_plan(parent2, length2, np.zeros(len(parent), np.uint64), [0] * len(parent))
+    qa, ka, va = _rand_qkv(pa, 2, 1, 16, 400 + seed)
+
+    def tokens(p, blk):  # packed indices of input block blk's tokens
+        start = int(p.blk_start[p.block_map[blk]])
+        return np.arange(start, start + int(p.blk_len[p.block_map[blk]]))
+    ia = np.concatenate([tokens(pa, o) for o in order])
+    ib = np.concatenate([tokens(pb, n) for n in range(len(order))])
+    if seed == 0:
+        assert not np.array_equal(ia, ib)   # the packed order does change
+    qb, kb, vb = (np.empty_like(x) for x in (qa, ka, va))
+    qb[ib], kb[ib], vb[ib] = qa[ia], ka[ia], va[ia]
+    oa = oatt.attend_paths(pa, qa, ka, va)
+    ob = oatt.attend_paths(pb, qb, kb, vb)
+    np.testing.assert_allclose(ob[ib], oa[ia], rtol=0, atol=1e-13)
+
+
 def test_one_token_block_sees_its_ancestors_and_itself():
     p, _ = oplan.make_plan([-1, 0, 0, 2], [5, 4, 3, 1], np.zeros(4, np.uint64), [0] * 4)
     q, k, v = _rand_qkv(p, 1, 1, 8, 13)
