@@ -203,10 +203,16 @@ def measure_rope(lib, torch, B, stream, reps=40, warmup=None, keys_only=False, t
     return ms, nbytes, graph_ms(torch, fns, reps), single_call_us(torch, fns[0], stream)
 
 
-def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None, n_questions=65536, timing_forms=False):
-    """readout_decide on n_questions (2-10 letters each) over rotating buffer sets: algorithmic GB/s."""
+def measure_readout(lib, torch, dev, stream, reps=64, n_sets=None, warmup=None, n_questions=65536, timing_forms=False):
+    """readout_decide on n_questions (2-10 letters each) over rotating buffer sets: algorithmic GB/s.
+
+    n_sets None: enough sets that their buffers span three times the L2 cache (at least 2)."""
     b = synth.draw_readout_batch(n_questions)
     nq, stride = len(b["r1"]), b["stride"]
+    set_bytes = 4 * (b["logits"].size + nq * stride) + 4 * 5 * nq   # logits, p_cal; r1, r2, n, T, choice
+    if n_sets is None:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        n_sets = max(2, -(-3 * l2 // set_bytes))
     sets = []
     for _ in range(n_sets):
         sets.append(dict(logits=torch.from_numpy(b["logits"]).to(dev), r1=torch.from_numpy(b["r1"]).to(dev),
@@ -232,7 +238,7 @@ def measure_readout(lib, torch, dev, stream, reps=64, n_sets=16, warmup=None, n_
     if not timing_forms:
         return ms, nbytes
     fns = [lambda st, x=x: run(x, st) for x in sets]
-    return ms, nbytes, graph_ms(torch, fns, reps), single_call_us(torch, fns[0], stream)
+    return ms, nbytes, graph_ms(torch, fns, reps), single_call_us(torch, fns[0], stream), (n_sets, n_sets * set_bytes)
 
 
 def graph_ms(torch, fns, reps):
@@ -503,10 +509,12 @@ def run_only(args):
         print(json.dumps(line), flush=True)
         return
     if args.only == "readout":
-        ms, nbytes, gms, one_us = measure_readout(lib, torch, dev, stream, reps=args.steps, n_sets=args.sets or 16,
-                                                  warmup=args.warmup, n_questions=args.questions, timing_forms=True)
+        ms, nbytes, gms, one_us, rot = measure_readout(lib, torch, dev, stream, reps=args.steps,
+                                                       n_sets=args.sets or None, warmup=args.warmup,
+                                                       n_questions=args.questions, timing_forms=True)
         gbs = nbytes / ms / 1e6
-        line.update(workload=f"{args.questions:,} questions, 2-10 letters", us=round(ms * 1e3, 2), bytes=nbytes,
+        line.update(workload=f"{args.questions:,} questions, 2-10 letters", sets=rot[0],
+                    rotating_mb=round(rot[1] / 1e6, 1), us=round(ms * 1e3, 2), bytes=nbytes,
                     achieved=round(gbs, 1), unit="GB/s", peak=peaks["hbm"], frac=round(gbs / peaks["hbm"], 4),
                     graph_us=round(gms * 1e3, 2), graph_frac=round(nbytes / gms / 1e6 / peaks["hbm"], 4),
                     single_call_us=round(one_us, 2))
@@ -691,19 +699,23 @@ def run_gpu(args):
         "clocks": clk,
     }
     rope_ms, rope_bytes, rope_gms, rope_one = measure_rope(lib, torch, B, stream, timing_forms=True)
-    ro_ms, ro_bytes, ro_gms, ro_one = measure_readout(lib, torch, dev, stream, timing_forms=True)
+    ro_ms, ro_bytes, ro_gms, ro_one, ro_rot = measure_readout(lib, torch, dev, stream, timing_forms=True)
+    rot_mb = N_SETS * (2 * i.n_fwd * w.hq * w.d * 2 + 2 * i.n_tot * w.hkv * w.d * 2) / 1e6  # Q, O, K, V per set
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     line["kernels"] = {
         "tree_rope": {"bound": "hbm", "us": round(rope_ms * 1e3, 2), "bytes": rope_bytes,
                       "achieved": round(rope_bytes / rope_ms / 1e6, 1), "peak": peaks["hbm"], "unit": "GB/s",
                       "frac": round(rope_bytes / rope_ms / 1e6 / peaks["hbm"], 4),
                       "graph_us": round(rope_gms * 1e3, 2), "single_call_us": round(rope_one, 2),
-                      "note": f"{N_SETS} rotating Q/K sets (> L2); us: launches back to back on the stream, "
+                      "note": f"{N_SETS} rotating Q/K/V/O sets ({rot_mb:.0f} MB, {rot_mb * 1e6 / l2_bytes:.1f} x L2); "
+                              "us: launches back to back on the stream, "
                               "graph_us: the same from a CUDA graph, single_call_us: one launch on an idle stream"},
         "readout_decide_65536q": {"bound": "hbm", "us": round(ro_ms * 1e3, 2), "bytes": ro_bytes,
                                   "achieved": round(ro_bytes / ro_ms / 1e6, 1), "peak": peaks["hbm"],
                                   "unit": "GB/s", "frac": round(ro_bytes / ro_ms / 1e6 / peaks["hbm"], 4),
                                   "graph_us": round(ro_gms * 1e3, 2), "single_call_us": round(ro_one, 2),
-                                  "note": "65,536 questions, 2-10 letters, 16 rotating buffer sets (> L2)"},
+                                  "note": f"65,536 questions, 2-10 letters, {ro_rot[0]} rotating buffer sets "
+                                          f"({ro_rot[1] / 1e6:.0f} MB, {ro_rot[1] / l2_bytes:.1f} x L2)"},
         "tree_attn_fwd": {"bound": "tensor", "us": round(attn_launch_ms * 1e3, 2), "flops": flops_launch,
                           "achieved": round(achieved, 2), "peak": peaks["tc"], "unit": "TFLOP/s",
                           "frac": round(achieved / peaks["tc"], 4)},
