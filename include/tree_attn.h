@@ -135,7 +135,13 @@ typedef struct tree_plan tree_plan_t;
  */
 TREE_API int tree_pack_plan(const tree_spec_t *spec, const tree_plan_opts_t *opts, tree_plan_t **out);
 
-/* Free a plan (NULL is accepted). */
+/*
+ * Free a plan (NULL is accepted).  The largest host buffers of the plans freed
+ * on a thread (device image, gathered keys, their run tables) are kept for the
+ * next tree_pack_plan on that thread, so a caller planning batch after batch
+ * does not pay for fresh memory each time; the thread holds at most the
+ * buffers of the largest plan it has freed, released when it exits.
+ */
 TREE_API int tree_plan_free(tree_plan_t *plan);
 
 typedef struct {

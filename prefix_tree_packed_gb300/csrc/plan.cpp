@@ -46,6 +46,26 @@ constexpr int32_t kTile = 128;
 
 size_t align4(size_t words) { return (words + 3) & ~size_t(3); }
 
+// Bits [lo, hi) of a little-endian multi-word bit set, a word at a time.
+void set_bits(int32_t *w, int32_t lo, int32_t hi) {
+  while (lo < hi) {
+    const int32_t k = lo >> 5, e = std::min(hi, (k + 1) << 5);
+    const uint32_t n = (uint32_t)(e - lo);
+    w[k] |= (int32_t)((n == 32 ? 0xffffffffu : ((1u << n) - 1u)) << (lo & 31));
+    lo = e;
+  }
+}
+
+// Bits [0, n) of a multi-word bit set all set.
+bool all_bits(const int32_t *w, int32_t n) {
+  for (int32_t k = 0; (k << 5) < n; ++k) {
+    const int32_t m = std::min(32, n - (k << 5));
+    const uint32_t want = m == 32 ? 0xffffffffu : ((1u << m) - 1u);
+    if (((uint32_t)w[k] & want) != want) return false;
+  }
+  return true;
+}
+
 int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_row, int32_t tiling, Plan &P) {
   const int32_t nb = s.n_blocks;
   P.n_input_blocks = nb;
@@ -320,7 +340,7 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
         int32_t *rows = P.vruns.data() + (size_t)e * kVRunWords + 4;
         const int32_t r_lo = std::max(i0, bstart[b]), r_hi = std::min(i1, bstart[b] + blen[b]);
         const int32_t first = std::max(r_lo, bstart[b] + (t * kTile - bpos0[b]));
-        for (int32_t i = first; i < r_hi; ++i) rows[(i - i0) >> 5] |= (int32_t)(1u << ((i - i0) & 31));
+        set_bits(rows, first - i0, r_hi - i0);
       }
       // entries of this range: contiguous (slot c holds packed key j0 + c: one tiled load)
       // and full (every row of the tile is served by it and sees every slot: no mask)
@@ -331,7 +351,7 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
         const bool contig = run[0] == 1 && run[8] == 0 && run[9] == kTile - 1;
         bool full = contig && vk[kTile - 1] <= i0;
         if (full) {
-          for (int32_t i = i0; i < i1 && full; ++i) full = (run[4 + ((i - i0) >> 5)] >> ((i - i0) & 31)) & 1;
+          full = all_bits(run + 4, i1 - i0);  // every row of the tile is served by it
           full = full && run[11] > i1 - 1;
         }
         // a full contiguous entry needs neither its gather list nor its run table: it names
@@ -351,6 +371,27 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   P.qt_ent1.reserve(n_qt_est);
   P.qt_order.reserve(n_qt_est);
   P.ent.reserve((size_t)n_qt_est * 8);
+  if (tiling == 1) {
+    // an upper bound on the entries (per query tile: position ranges x blocks with rows in
+    // it), so the gather lists and run tables are allocated once
+    size_t bound = 0;
+    for (int32_t c = 0; c < P.n_chunks; ++c) {
+      const int32_t q0 = P.n_res + c * max_fwd, q1 = std::min(q0 + max_fwd, P.n_tot);
+      for (int32_t i0 = q0; i0 < q1; i0 += kTile) {
+        const int32_t i1 = std::min(i0 + kTile, q1);
+        int32_t nblk = 0, tmax = 0;
+        for (int32_t b = block_of(i0); b < nbc && bstart[b] < i1; ++b) {
+          if (bstart[b] + blen[b] <= i0) continue;
+          ++nblk;
+          tmax = std::max(tmax, (bpos0[b] + (std::min(i1, bstart[b] + blen[b]) - 1 - bstart[b])) / kTile);
+        }
+        bound += (size_t)(tmax + 1) * nblk;
+      }
+    }
+    P.ent.reserve(P.ent.size() + bound);
+    P.vkeys.reserve(bound * kTile);
+    P.vruns.reserve(bound * kVRunWords);
+  }
   std::vector<int32_t> ord;
   for (int32_t c = 0; c < P.n_chunks; ++c) {
     const int32_t q0 = P.n_res + c * max_fwd, q1 = std::min(q0 + max_fwd, P.n_tot);
@@ -535,6 +576,33 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
   return TREE_OK;
 }
 
+// The largest buffers of the plans freed on this thread, kept for the next plan
+// built here: a runtime plans batch after batch, and fresh multi-megabyte
+// buffers would cost a page fault per page every time.
+struct Spare {
+  std::vector<int32_t> image, vkeys, vruns;
+};
+thread_local Spare g_spare;
+
+void keep_larger(std::vector<int32_t> &spare, std::vector<int32_t> &v) {
+  if (v.capacity() > spare.capacity()) spare.swap(v);
+}
+
+void take_spare(Plan &P) {
+  P.image.swap(g_spare.image);
+  P.vkeys.swap(g_spare.vkeys);
+  P.vruns.swap(g_spare.vruns);
+  P.image.clear();
+  P.vkeys.clear();
+  P.vruns.clear();
+}
+
+void give_spare(Plan &P) {
+  keep_larger(g_spare.image, P.image);
+  keep_larger(g_spare.vkeys, P.vkeys);
+  keep_larger(g_spare.vruns, P.vruns);
+}
+
 }  // namespace
 }  // namespace tree
 
@@ -566,8 +634,10 @@ int tree_pack_plan(const tree_spec_t *spec, const tree_plan_opts_t *opts, tree_p
     return tree::fail(TREE_ERR_UNSUPPORTED, "tiling by position needs max_depth <= %d", tree::kMaxRuns);
   auto *pl = new (std::nothrow) tree_plan;
   if (!pl) return tree::fail(TREE_ERR_INVALID_ARG, "out of host memory");
+  tree::take_spare(pl->p);
   const int rc = tree::build(*spec, max_fwd, max_depth, max_row, tiling, pl->p);
   if (rc != TREE_OK) {
+    tree::give_spare(pl->p);
     delete pl;
     return rc;
   }
@@ -576,6 +646,7 @@ int tree_pack_plan(const tree_spec_t *spec, const tree_plan_opts_t *opts, tree_p
 }
 
 int tree_plan_free(tree_plan_t *plan) {
+  if (plan) tree::give_spare(plan->p);
   delete plan;
   return TREE_OK;
 }
