@@ -34,13 +34,21 @@ struct Request {
 };
 
 // Prefix trie over prompts.  Nodes are created in first-seen order, so a
-// parent always precedes its children.
+// parent always precedes its children.  Row sizes (tokens per root, resident
+// blocks included), rows above the limit and resident roots are kept up to
+// date, and a trial addition can be undone: every change it makes is a node
+// appended at the end, a child count of an earlier node, a map entry keyed by
+// the new node's own (parent, key, length), or a row total.
 struct Trie {
-  std::vector<int32_t> parent, length, resident;
+  std::vector<int32_t> parent, length, resident, n_children, root;
   std::vector<uint64_t> key;
-  std::vector<int32_t> n_children;
+  std::vector<int64_t> row;  // per node: tokens of the row it roots (roots only)
   std::map<std::tuple<int32_t, uint64_t, int32_t>, int32_t> child;  // (parent, key, length) -> node
   int64_t cost = 0;
+  int64_t max_row = INT64_MAX;
+  int32_t res_roots = 0, over_rows = 0;
+
+  size_t size() const { return parent.size(); }
 
   // Walk/extend the path of one prompt; returns its last node.
   int32_t add(const tree_block_t *b, int32_t n, const std::unordered_set<uint64_t> &res_keys) {
@@ -59,12 +67,34 @@ struct Trie {
       key.push_back(b[i].key);
       resident.push_back(res ? 1 : 0);
       n_children.push_back(0);
-      if (p >= 0) ++n_children[p];
+      root.push_back(p < 0 ? node : root[(size_t)p]);
+      row.push_back(0);
+      if (p >= 0) ++n_children[(size_t)p];
       if (b[i].key != 0) child.emplace(k, node);
       if (!res) cost += b[i].length;
+      if (p < 0 && res) ++res_roots;
+      int64_t &rw = row[(size_t)root[(size_t)node]];
+      if (rw <= max_row && rw + b[i].length > max_row) ++over_rows;
+      rw += b[i].length;
       p = node;
     }
     return p;
+  }
+
+  // Back to the state with n0 nodes and the given cost.
+  void undo(size_t n0, int64_t cost0) {
+    for (size_t n = size(); n-- > n0;) {
+      if (key[n] != 0) child.erase(std::make_tuple(parent[n], key[n], length[n]));
+      if (parent[n] >= 0) --n_children[(size_t)parent[n]];
+      int64_t &rw = row[(size_t)root[n]];
+      if (rw > max_row && rw - length[n] <= max_row) --over_rows;
+      rw -= length[n];
+      if (parent[n] < 0 && resident[n]) --res_roots;
+    }
+    for (auto *v : {&parent, &length, &resident, &n_children, &root}) v->resize(n0);
+    key.resize(n0);
+    row.resize(n0);
+    cost = cost0;
   }
 };
 
@@ -76,6 +106,7 @@ struct tree_queue {
   std::vector<uint64_t> resident_keys;
   std::unordered_set<uint64_t> res_set;
   std::vector<tree::Request> lane[2];  // 0 short, 1 long
+  std::unordered_set<int64_t> ids;      // ids of the queued requests
   uint64_t next_seq = 0;
 };
 
@@ -97,6 +128,7 @@ namespace {
 // row outgrows max_row, or a second resident root appears.
 bool add_request(Trie &t, const Request &r, const tree_queue &q, std::vector<int32_t> &readout,
                  std::vector<int32_t> &leaf1, std::vector<int32_t> &leaf2) {
+  t.max_row = q.opts.max_row;
   std::vector<int32_t> last(r.prompt_blocks.size());
   size_t off = 0;
   for (size_t p = 0; p < r.prompt_blocks.size(); ++p) {
@@ -111,18 +143,7 @@ bool add_request(Trie &t, const Request &r, const tree_queue &q, std::vector<int
   }
   for (int32_t n : readout)
     if (t.n_children[(size_t)n] != 0) return false;
-  // row sizes and resident roots
-  std::vector<int64_t> row(t.parent.size(), 0);
-  int32_t res_roots = 0;
-  for (size_t n = 0; n < t.parent.size(); ++n) {
-    int32_t root = (int32_t)n;
-    while (t.parent[(size_t)root] >= 0) root = t.parent[(size_t)root];
-    row[(size_t)root] += t.length[n];
-    if (t.parent[n] < 0 && t.resident[n]) ++res_roots;
-  }
-  for (int64_t v : row)
-    if (v > q.opts.max_row) return false;
-  return res_roots <= 1;
+  return t.over_rows == 0 && t.res_roots <= 1;
 }
 
 // Schedule order of a lane at time now: highest priority first (HRRN) or
@@ -190,9 +211,7 @@ extern "C" TREE_API int tree_queue_push(tree_queue_t *q, const tree_request_t *r
   if (r->n_prompts < 1 || !r->prompt_blocks || !r->blocks || r->n_questions < 0 ||
       (r->n_questions > 0 && (!r->q_prompt1 || !r->q_prompt2)))
     return fail(TREE_ERR_INVALID_ARG, "tree_queue_push: bad counts or NULL arrays");
-  for (const auto &lane : q->lane)
-    for (const auto &x : lane)
-      if (x.id == r->id) return fail(TREE_ERR_INVALID_ARG, "tree_queue_push: id %lld already queued", (long long)r->id);
+  if (q->ids.count(r->id)) return fail(TREE_ERR_INVALID_ARG, "tree_queue_push: id %lld already queued", (long long)r->id);
   Request req;
   req.id = r->id;
   req.arrival = r->arrival_ms;
@@ -234,6 +253,7 @@ extern "C" TREE_API int tree_queue_push(tree_queue_t *q, const tree_request_t *r
   req.seq = q->next_seq++;
   const int lane = (q->opts.long_tokens > 0 && req.cost > q->opts.long_tokens) ? 1 : 0;
   if (cost_out) *cost_out = req.cost;
+  q->ids.insert(req.id);
   q->lane[lane].push_back(std::move(req));
   return ok();
 }
@@ -244,6 +264,7 @@ extern "C" TREE_API int tree_queue_cancel(tree_queue_t *q, int64_t id) {
     for (size_t i = 0; i < lane.size(); ++i)
       if (lane[i].id == id) {
         lane.erase(lane.begin() + (std::ptrdiff_t)i);
+        q->ids.erase(id);
         return ok();
       }
   return fail(TREE_ERR_INVALID_ARG, "tree_queue_cancel: id %lld is not queued", (long long)id);
@@ -273,13 +294,16 @@ extern "C" TREE_API int tree_queue_pop(tree_queue_t *q, double now_ms, tree_batc
       add_request(t, r, *q, readout, leaf1, leaf2);  // the first request is always taken (checked at push)
     } else {
       if (lane == 1) break;  // a long request runs alone
-      Trie t2 = t;
-      std::vector<int32_t> ro2 = readout, a2 = leaf1, b2 = leaf2;
-      if (!add_request(t2, r, *q, ro2, a2, b2) || t2.cost > q->opts.max_batch_tokens) continue;
-      t = std::move(t2);
-      readout = std::move(ro2);
-      leaf1 = std::move(a2);
-      leaf2 = std::move(b2);
+      // try it in place; a request that does not fit is undone
+      const size_t n0 = t.size(), r0 = readout.size(), l0 = leaf1.size();
+      const int64_t c0 = t.cost;
+      if (!add_request(t, r, *q, readout, leaf1, leaf2) || t.cost > q->opts.max_batch_tokens) {
+        t.undo(n0, c0);
+        readout.resize(r0);
+        leaf1.resize(l0);
+        leaf2.resize(l0);
+        continue;
+      }
     }
     taken.push_back(order[k]);
     q0.push_back((int32_t)leaf1.size());
@@ -287,7 +311,10 @@ extern "C" TREE_API int tree_queue_pop(tree_queue_t *q, double now_ms, tree_batc
   auto *b = new tree_batch;
   b->lane = lane;
   b->cost = t.cost;
-  for (size_t i : taken) b->ids.push_back(reqs[i].id);
+  for (size_t i : taken) {
+    b->ids.push_back(reqs[i].id);
+    q->ids.erase(reqs[i].id);
+  }
   b->q0 = q0;
   // the resident root (at most one) goes first, so that its tokens lead the
   // packed row; every other block keeps its first-seen place (parents first)
