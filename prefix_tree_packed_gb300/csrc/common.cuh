@@ -27,6 +27,10 @@ inline cudaStream_t as_stream(tree_stream_t s) { return reinterpret_cast<cudaStr
 // Number of SMs of the current device (cached per process; GB300 has 152).
 int sm_count();
 
+// Raise kernel `fn`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (device, kernel).
+int set_max_dynamic_smem(const void *fn, int bytes, const char *who);
+
 // 2-D TMA map over a row-major [rows, cols] f16 matrix: box_rows x 64-column
 // boxes (128-byte rows), 128-byte swizzle, zero fill outside the matrix
 // (box_rows 1: the map of tile::gather4 loads).  `who` names the caller in

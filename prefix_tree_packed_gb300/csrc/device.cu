@@ -1,6 +1,10 @@
 // Per-device facts and tensor maps the launchers need.
 #include <cudaTypedefs.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "common.cuh"
 
 namespace tree {
@@ -15,6 +19,22 @@ int sm_count() {
     cached[dev] = n;
   }
   return cached[dev];
+}
+
+int set_max_dynamic_smem(const void *fn, int bytes, const char *who) {
+  // a kernel attribute belongs to one device: a process that launches on a
+  // second device sets it again there
+  static std::mutex mu;
+  static std::set<std::pair<int, const void *>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "%s: cudaGetDevice: %s", who, cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({dev, fn})) return TREE_OK;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+  done.insert({dev, fn});
+  return TREE_OK;
 }
 
 namespace {

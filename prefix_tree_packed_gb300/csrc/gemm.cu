@@ -320,15 +320,10 @@ int launch_gemm(const void *a, const void *b, void *c, const void *r, int32_t m,
                 int32_t *status, cudaStream_t s, int32_t n1 = 0, int32_t n2 = 0, void *c2 = nullptr,
                 void *c3 = nullptr) {
   using Cf = GCfg<BN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
-    if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_gemm: %s", cudaGetErrorString(e));
-    attr_set = true;
-  }
+  int rc = set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc<BN>), (int)Cf::SMEM, "tree_gemm");
+  if (rc) return rc;
   const int nb_rows = epi == TREE_GEMM_SWIGLU ? 2 * n : n;
   CUtensorMap ma, mb;
-  int rc;
   if ((rc = make_map(&ma, a, k, m, "tree_gemm")) || (rc = make_map(&mb, b, k, nb_rows, "tree_gemm", BN / 2))) return rc;
   GemmArgs g;
   g.m = m;

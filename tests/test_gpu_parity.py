@@ -250,8 +250,21 @@ def test_rope_keys_only(lib):
 
 # ---------------------------------------------------------------- attention
 
+def _boundary_rows(p):
+    """Forward rows on either side of every chunk seam and of every block start and end:
+    the rows where the visible key set changes."""
+    rows = set()
+    for c in range(p.n_chunks):
+        a, b = int(p.chunk_q0[c]) - p.n_res, int(p.chunk_q1[c]) - p.n_res
+        rows.update((a, a + 1, b - 2, b - 1))
+    for b in range(p.n_blocks):
+        s, e = int(p.blk_start[b]), int(p.blk_start[b] + p.blk_len[b])
+        rows.update(t - p.n_res for t in (s, s + 1, e - 2, e - 1))
+    return sorted(r for r in rows if 0 <= r < p.n_fwd)
+
+
 def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per_chunk=48, lse=True,
-                dynamic=True, tiling=0):
+                dynamic=True, tiling=0, extra_rows=()):
     r = Run(lib, forest, max_fwd, tiling=tiling)
     work = torch.zeros(2, dtype=torch.int32, device="cuda") if dynamic else None
     p = r.oplan
@@ -285,7 +298,7 @@ def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per
         for c in range(p.n_chunks):
             a, b = int(p.chunk_q0[c]) - p.n_res, int(p.chunk_q1[c]) - p.n_res
             rows += [a, b - 1] + list(rng.integers(a, b, rows_per_chunk - 2))
-        rows = np.array(rows)
+        rows = np.unique(np.array(rows + list(extra_rows), dtype=np.int64))
         ref = oatt.attend_rows(p, qr, kr, v, rows)
         err = np.abs(got[rows] - ref)
         assert err.max() <= ATOL_O, f"max err {err.max()}"
@@ -305,8 +318,38 @@ def test_attention_workloads_full(lib, n, tiling):
 
 @pytest.mark.parametrize("tiling", [0, 1])
 def test_attention_long_row_four_chunks_sampled(lib, tiling):
+    """The 32,768-token row in four chunks, on random rows of each chunk plus every row beside a
+    chunk seam or a block boundary (the question and option blocks of the last chunk)."""
     w = synth.workload(4)
-    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=False, rows_per_chunk=40, tiling=tiling)
+    p, _ = oplan.plan_forest(w.forest, max_fwd=w.max_fwd)
+    seams = _boundary_rows(p)
+    assert len(seams) == 76   # 4 per chunk seam and per block edge, shared ones counted once
+    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=False, rows_per_chunk=40, tiling=tiling,
+                extra_rows=seams)
+
+
+@pytest.mark.parametrize("tiling", [0, 1])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (6, 2), (32, 32)])
+def test_attention_odd_head_ratio_d128(lib, hq, hkv, tiling):
+    """At head dim 128 an odd number of q heads per kv head runs the kernel instance that takes one
+    q head per work item (one softmax warpgroup, its epilogue deferred behind the next item's first
+    tile, P over S in tensor memory): the mixed rows of the Llama-8B-shaped workload, in full."""
+    w = synth.workload(3)
+    _attn_check(lib, w.forest, hq, hkv, 128, w.seed + hq, w.max_fwd, full=True, tiling=tiling)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_attention_random_forests_odd_ratio_d128(lib, seed):
+    rng = np.random.default_rng(900 + seed)
+    f = synth.random_forest(rng, n_roots=int(rng.integers(1, 4)), max_blocks=int(rng.integers(3, 30)),
+                            max_len=int(rng.integers(1, 300)), dup_prob=0.2, resident_root=bool(seed % 2))
+    try:
+        oplan.plan_forest(f, max_fwd=256)
+    except oplan.PlanError:
+        pytest.skip("forest has no forward tokens")
+    hq, hkv = [(3, 3), (6, 2), (5, 1)][seed % 3]
+    _attn_check(lib, f, hq, hkv, 128, seed, max_fwd=int(rng.choice([128, 256, 8192])), dynamic=bool(seed % 2),
+                tiling=seed % 2)
 
 
 @pytest.mark.parametrize("seed", range(8))
