@@ -331,8 +331,10 @@ TREE_API int tree_attn_fwd(const tree_plan_t *plan, const void *plan_dev, int32_
  * call clears its chunk's counter on `stream` before the launch.  Calls for
  * the same chunk index that may run at the same time on the GPU (different
  * streams, several plans) share that counter and race: serialise them.
- * The first call on each device looks up the array's device address; make that
- * first call before any stream capture begins.  Nothing is allocated.
+ * The first call on each device (and the first after that device's context
+ * has been replaced, by cudaDeviceReset for instance) looks up the array's
+ * device address; make that first call before any stream capture begins.
+ * Nothing is allocated.
  */
 TREE_API int tree_attn_fwd_noalloc(const tree_plan_t *plan, const void *plan_dev, int32_t chunk, const void *q,
                                    const void *k, const void *v, void *o, float *lse,

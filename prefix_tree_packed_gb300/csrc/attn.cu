@@ -40,6 +40,8 @@
 // caller's status word, and the CTA winds down: pending copies and MMAs are
 // awaited (bounded), tensor memory is freed, and the kernel returns.
 
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <mutex>
 
@@ -833,17 +835,12 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
               float *lse, int hq, int hkv, float scale, int32_t *work, int32_t self_test, int32_t *status,
               cudaStream_t s) {
   using C = Cfg<D, NH>;
-  static bool attr_set[2] = {false, false};
   const bool gather = P.tiling == 1;
   auto kern = gather ? tree_attn_tc<D, NH, true> : tree_attn_tc<D, NH, false>;
-  if (!attr_set[gather]) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd: %s", cudaGetErrorString(e));
-    attr_set[gather] = true;
-  }
+  int rc = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), (int)C::SMEM, "tree_attn_fwd");
+  if (rc) return rc;
   const int32_t q0 = P.chunk_q0[chunk], nq = P.chunk_q1[chunk] - q0;
   CUtensorMap mq, mk, mv, mo, mkg, mvg;
-  int rc;
   if ((rc = make_map(&mq, q, (int64_t)hq * D, nq, "tree_attn_fwd")) ||
       (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
       (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
@@ -924,25 +921,58 @@ constexpr int kNoAllocChunks = 256;
 static __device__ __align__(256) int32_t g_noalloc_work[2 * kNoAllocChunks];
 
 constexpr int kMaxDevices = 64;
-int32_t *g_noalloc_ptr[kMaxDevices] = {nullptr};
+struct NoAllocSlot {
+  unsigned long long ctx_id;  // context the address belongs to (0: none yet)
+  int32_t *ptr;
+};
+NoAllocSlot g_noalloc_slot[kMaxDevices] = {};
 std::mutex g_noalloc_mutex;
 
-// Device address of the array on the current device, looked up once per device.
+// Unique id of the calling thread's current CUDA context, 0 if there is none
+// (ids are never reused within a process, unlike context handles).
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the array in the current context.  Looked up on the
+// first call on a device and again whenever the device's context has changed
+// since (after cudaDeviceReset, say, the old address belongs to a context
+// that no longer exists).
 int noalloc_counters(int32_t **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices)
     return fail(TREE_ERR_UNSUPPORTED, "tree_attn_fwd_noalloc: device %d beyond %d", dev, kMaxDevices);
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
+  NoAllocSlot &slot = g_noalloc_slot[dev];
+  if (ctx == 0 || slot.ctx_id != ctx || !slot.ptr) {
     int32_t *ptr = nullptr;
     e = cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr), g_noalloc_work);
     if (e != cudaSuccess || !ptr)
       return fail(TREE_ERR_CUDA, "tree_attn_fwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    g_noalloc_ptr[dev] = ptr;
+    slot.ptr = ptr;
+    slot.ctx_id = current_context_id();  // the lookup has made the device's context current
   }
-  *out = g_noalloc_ptr[dev];
+  *out = slot.ptr;
   return TREE_OK;
 }
 
