@@ -263,9 +263,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   };
 
   if (warp >= 4 * NH) {
-    // (the position-tiled kernels keep the launch budget: with the split, their gathering
-    // producer at d = 128 gave wrong tiles; both groups skip it, so the budget stays balanced)
-    if (NH == 2 && !G) regs_dec<C::SERVICE_REGS>();
+    if (NH == 2) regs_dec<C::SERVICE_REGS>();
     if (warp == C::PROD_WARP) {
       // ---------------------------------------------------------- producer (whole warp, one lane issues)
       if (elect_one()) {
@@ -565,7 +563,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    if (NH == 2 && !G) regs_inc<C::SOFTMAX_REGS>();
+    if (NH == 2) regs_inc<C::SOFTMAX_REGS>();
     const int h = warp >> 2;
     const int r = 32 * (warp & 3) + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
