@@ -547,9 +547,10 @@ def run_only(args):
             # Q and O of every forward row, K and V of every key row, the plan image: each once
             nbytes = 2 * i.n_fwd * w.hq * w.d * 2 + 2 * i.n_tot * w.hkv * w.d * 2 + i.dev_bytes
             gbs = nbytes / ms / 1e6
-            ridge = peaks["tc"] * 1e12 / (peaks["hbm"] * 1e9)  # flop per byte where the two roofs meet
+            ridge = peaks["tc_burst"] * 1e12 / (peaks["hbm"] * 1e9)  # flop per byte where the two roofs meet
             line.update(us_per_forward=round(ms * 1e3, 2), chunks=len(B.chunks), visible_pairs=i.pairs,
-                        achieved=round(tf, 2), unit="TFLOP/s", peak=peaks["tc"], frac=round(tf / peaks["tc"], 4),
+                        achieved=round(tf, 2), unit="TFLOP/s", peak=peaks["tc_burst"],
+                        frac=round(tf / peaks["tc_burst"], 4), frac_of_sustained=round(tf / peaks["tc"], 4),
                         bytes=nbytes, flop_per_byte=round(flops / nbytes, 1), gbs=round(gbs, 1),
                         hbm_frac=round(gbs / peaks["hbm"], 4),
                         bound="tensor" if flops / nbytes >= ridge else "hbm")
@@ -557,11 +558,127 @@ def run_only(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ every workload
+
+def oracle_sample(w, budget_s: float, seed: int = 0):
+    """The oracle (plan, f64 RoPE, per-row attention, readout) on random forward rows of workload w,
+    in growing batches until budget_s of host time is spent: forward rows per second.  Rows are
+    drawn uniformly from the forward, so the rate extrapolates to the whole batch."""
+    from oracle import plan as oplan
+    p, _ = oplan.plan_forest(w.forest, max_fwd=w.max_fwd)
+    if p.n_fwd <= 128:
+        t = time.perf_counter()
+        n, reps = 0, 0
+        while reps == 0 or (time.perf_counter() - t < budget_s and reps < 50):
+            n += _oracle_step(w)
+            reps += 1
+        dt = time.perf_counter() - t
+        return {"tokens_per_s": round(n / dt, 2), "rows": int(n), "seconds": round(dt, 2), "cores": _threads(),
+                "sample": f"{reps} x all {p.n_fwd} forward rows"}
+    rng = np.random.default_rng(seed)
+    t = time.perf_counter()
+    n, batch = 0, 4
+    while True:
+        rows = np.sort(rng.choice(p.n_fwd, min(batch, p.n_fwd), replace=False))
+        n += _oracle_step(w, rows)
+        if time.perf_counter() - t >= budget_s:
+            break
+        batch = min(2 * batch, 256)
+    dt = time.perf_counter() - t
+    return {"tokens_per_s": round(n / dt, 2), "rows": int(n), "seconds": round(dt, 2), "cores": _threads(),
+            "sample": f"{n} random forward rows of {p.n_fwd} (with the keys of their prompts); rate per row "
+                      f"extrapolates to the batch"}
+
+
+def measure_configs(lib, torch, dev, stream, peaks, oracle_s: float, numbers=(1, 2, 3, 4, 5)):
+    """tree_attn_fwd (and tree_rope) on every workload, each over rotating input sets larger than L2
+    where the workload allows, with the oracle's rate on a sample of the same workload beside it."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    ridge = peaks["tc_burst"] * 1e12 / (peaks["hbm"] * 1e9)
+    out = {}
+    for n in numbers:
+        w = synth.workload(n)
+        plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd)
+        i = plan.info
+        set_bytes = 2 * i.n_fwd * w.hq * w.d * 2 + 2 * i.n_tot * w.hkv * w.d * 2
+        n_sets = int(min(8, max(2, -(-3 * l2 // set_bytes))))
+        B = Batch(lib, torch, w, dev, n_sets=n_sets)
+        flops = 4.0 * w.d * w.hq * i.pairs
+        # attention bytes: Q and O of every forward row, K and V of every key row, the plan image
+        nbytes = set_bytes + i.dev_bytes
+        probe = measure_attn(lib, torch, B, stream, reps=2, warmup=3)
+        reps = int(min(2000, max(5, 0.25 / max(probe * 1e-3, 1e-6))))
+        ms = measure_attn(lib, torch, B, stream, reps=reps, warmup=3)
+        tf = flops / (ms / 1e3) / 1e12
+        gbs = nbytes / ms / 1e6
+        bound = "tensor" if flops / nbytes >= ridge else "hbm"
+        r_ms, r_bytes = measure_rope(lib, torch, B, stream, reps=max(20, reps // 4))
+        r_gbs = r_bytes / r_ms / 1e6
+        e = {"forward_tokens": i.n_fwd, "resident_tokens": i.n_res, "chunks": i.n_chunks,
+             "heads": f"{w.hq}/{w.hkv}", "head_dim": w.d, "visible_pairs_per_head": int(i.pairs),
+             "rotating_sets": n_sets, "rotating_mb": round(n_sets * set_bytes / 1e6, 1),
+             "tree_attn_fwd": {"us_per_forward": round(ms * 1e3, 2), "launches": i.n_chunks, "reps": reps,
+                               "tokens_per_s": round(i.n_fwd / (ms / 1e3), 1), "flops": flops,
+                               "tflops": round(tf, 2), "frac_of_burst": round(tf / peaks["tc_burst"], 4),
+                               "bytes": int(nbytes), "gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm"], 4),
+                               "flop_per_byte": round(flops / nbytes, 1), "bound": bound},
+             "tree_rope": {"us": round(r_ms * 1e3, 2), "bytes": int(r_bytes), "gbs": round(r_gbs, 1),
+                           "hbm_frac": round(r_gbs / peaks["hbm"], 4)}}
+        e["roofline_frac"] = e["tree_attn_fwd"]["frac_of_burst" if bound == "tensor" else "hbm_frac"]
+        del B
+        torch.cuda.empty_cache()
+        if oracle_s > 0:
+            e["oracle"] = oracle_sample(w, oracle_s, seed=n)
+            e["oracle"]["kind"] = "oracle"
+        out[w.name] = e
+    return out
+
+
 # ------------------------------------------------------------------ ranks (one GPU each)
 
-def rank_workload(n: int, rank: int) -> synth.Workload:
-    """Each rank packs and runs its own batch (rows are independent: no data exchange)."""
-    return synth.workload(n, seed=n + 101 * rank)
+def job_batch(n: int, world: int):
+    """The whole job's batch: `world` copies of workload n's rows (copy c's letters and temperatures
+    drawn with seed n + 101 c), the resident template shared.  Returns the workload of copy 0 and
+    the batch as (parent, length, key, resident, leaf1, leaf2, n_letters, temperature)."""
+    copies = [synth.workload(n, seed=n + 101 * c) for c in range(world)]
+    w0 = copies[0]
+    f, nb = w0.forest, w0.forest.n_blocks
+    res = f.resident.astype(bool)
+    parent = np.concatenate([np.where(f.parent >= 0, f.parent + c * nb, -1) for c in range(world)]).astype(np.int32)
+    # keys of copied rows must not make them merge with the other copies; the template's may
+    key = np.concatenate([np.where(res | (f.key == 0), f.key, f.key + (np.uint64(c) << np.uint64(40)))
+                          for c in range(world)]).astype(np.uint64)
+    batch = dict(parent=parent, length=np.tile(f.length, world), key=key, resident=np.tile(f.resident, world))
+    if w0.leaf1 is not None:
+        batch.update(leaf1=np.concatenate([w0.leaf1 + c * nb for c in range(world)]).astype(np.int32),
+                     leaf2=np.concatenate([w0.leaf2 + c * nb for c in range(world)]).astype(np.int32),
+                     n_letters=np.concatenate([c.n_letters for c in copies]).astype(np.int32),
+                     temperature=np.concatenate([c.temperature for c in copies]).astype(np.float32))
+    return w0, batch
+
+
+def rank_workload(n: int, rank: int, world: int = 1):
+    """This rank's share of the job's batch: its rows as split by tree_shard_rows (visible pairs,
+    longest first), the resident template kept by every rank.  Rows are independent trees, so no
+    data moves between ranks; decisions are gathered on the host afterwards.
+
+    Returns (workload, question_index): the share as a workload (inputs seeded per rank) and the
+    job-wide index of each of its questions."""
+    import prefix_tree_packed_gb300 as lib
+    w0, b = job_batch(n, world)
+    spec = lib.Spec(b["parent"], b["length"], b["key"], b["resident"], b.get("leaf1"), b.get("leaf2"),
+                    max_fwd=w0.max_fwd)
+    block_rank, question_rank, _ = lib.shard_rows(spec, world)
+    sel = lib.shard_select(spec, block_rank, question_rank, rank)
+    qi = sel["question_index"]
+    has_q = "leaf1" in b and len(qi) > 0
+    w = synth.Workload(n, w0.name, synth.Forest(sel["parent"], sel["length"], sel["key"], sel["resident"]),
+                       hq=w0.hq, hkv=w0.hkv, d=w0.d, theta=w0.theta, seed=n + 101 * rank,
+                       leaf1=sel["leaf1"] if has_q else None, leaf2=sel["leaf2"] if has_q else None,
+                       n_letters=b["n_letters"][qi] if has_q else None,
+                       temperature=b["temperature"][qi] if has_q else None,
+                       logit_sigma=w0.logit_sigma, letter_stride=w0.letter_stride, max_fwd=w0.max_fwd)
+    return w, qi
 
 
 def max_over_ranks(dist, values, device):
@@ -574,8 +691,32 @@ def max_over_ranks(dist, values, device):
 
 
 def job_value(tokens_per_step: int, world: int, steps: int, ms: float) -> float:
-    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    """Whole-job tokens/s when every rank runs tokens_per_step: all ranks' tokens over the slowest
+    rank's time."""
     return tokens_per_step * world * steps / (ms / 1e3)
+
+
+def job_tokens(dist, n_fwd: int, device) -> int:
+    """Forward tokens of one job step: the sum over ranks of their shares."""
+    import torch
+    t = torch.tensor([n_fwd], dtype=torch.int64, device=device)
+    if dist is not None:
+        dist.all_reduce(t)
+    return int(t.item())
+
+
+def gather_decisions(dist, world: int, q_index, choices):
+    """Every rank's (job-wide question index, choice) pairs, assembled on the host: one choice per
+    question of the job, or None where a question was not answered."""
+    parts = [(np.asarray(q_index), np.asarray(choices))]
+    if dist is not None:
+        parts = [None] * world
+        dist.all_gather_object(parts, (np.asarray(q_index), np.asarray(choices)))
+    n = sum(len(q) for q, _ in parts)
+    out = np.full(n, -2, np.int32)
+    for q, c in parts:
+        out[q] = c
+    return out
 
 
 def run_gpu(args):
@@ -592,8 +733,8 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     import prefix_tree_packed_gb300 as lib
 
-    # every rank packs and runs its own batch: rows are independent, no data exchange
-    w = rank_workload(args.workload, rank)
+    # every rank plans and runs its share of the job's rows: rows are independent, no data exchange
+    w, q_index = rank_workload(args.workload, rank, world)
     B = Batch(lib, torch, w, dev)
     i = B.info
     stream = torch.cuda.current_stream()
@@ -660,11 +801,14 @@ def run_gpu(args):
     assert int(B.status.item()) == 0, "device status word set"
     link_gbs = measure_h2d(torch, dev, stream, int(h2d))
 
+    # ---- decisions of the last step gathered on the host (outside the timed regions)
+    decisions = gather_decisions(dist, world, q_index, out_ch.numpy() if B.nq else np.zeros(0, np.int32))
+
     # ---- max over ranks
     total_ms, e2e_ms = max_over_ranks(dist, [total_ms, e2e_ms], dev)
-    toks_step = i.n_fwd
-    value = job_value(toks_step, world, args.steps, total_ms)
-    e2e_value = job_value(toks_step, world, args.steps, e2e_ms)
+    toks_step = job_tokens(dist, i.n_fwd, dev)
+    value = toks_step * args.steps / (total_ms / 1e3)
+    e2e_value = toks_step * args.steps / (e2e_ms / 1e3)
 
     peaks = _peaks()
     flops = 4.0 * w.d * w.hq * i.pairs                      # QK^T + PV on visible pairs only
@@ -683,17 +827,24 @@ def run_gpu(args):
                    "rows": 8 if args.workload == 2 else None, "q_heads": w.hq, "kv_heads": w.hkv,
                    "head_dim": w.d, "visible_pairs_per_head": i.pairs, "chunks": len(B.chunks),
                    "questions": B.nq, "l2": f"{N_SETS} rotating input sets (> L2)",
-                   "step": "tree_runtime_step: plan (host) + plan transfer + rope + attention + readout, one kernel chain", "parallelism": f"dp{world} (rows)"},
+                   "step": "tree_runtime_step: plan (host) + plan transfer + rope + attention + readout, one kernel chain",
+                   "parallelism": f"dp{world} (the job's {world} x 8 rows split by visible pairs; template on "
+                                  f"every rank; decisions gathered on the host)"},
         "tflops_attention": round(achieved, 2),
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tc"], "unit": "TFLOP/s",
-                     "frac": round(achieved / peaks["tc"], 4), "traffic": traffic,
-                     "kernel": "tree_attn_fwd", "peak_source": f"{peaks['src']} bf16 sustained x 1 (f16 = bf16 rate)",
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tc_burst"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["tc_burst"], 4), "traffic": traffic,
+                     "kernel": "tree_attn_fwd",
+                     "peak_source": f"{peaks['src']} bf16 burst x 1 (f16 = bf16 rate; the launch is timed in a "
+                                    f"region of milliseconds at full clock)",
+                     "frac_of_sustained": round(achieved / peaks["tc"], 4),
                      "launch_ms": round(attn_launch_ms, 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4),
                 "call": "tree_runtime_step_host (page-locked host inputs, decisions back to the host)",
                 "h2d_link_gbs": round(link_gbs, 1),
                 "frac_of_link": round(h2d / (e2e_ms / args.steps * 1e6) / link_gbs, 4)},
+        "decisions": {"questions": int(len(decisions)), "answered": int((decisions >= 0).sum()),
+                      "gathered_from_ranks": world},
         "gpu_launches": B.launches_per_step() * args.steps,
         "host_enqueue_ms_per_step": round(host_ms / args.steps, 4),
         "clocks": clk,
@@ -717,9 +868,12 @@ def run_gpu(args):
                                   "note": f"65,536 questions, 2-10 letters, {ro_rot[0]} rotating buffer sets "
                                           f"({ro_rot[1] / 1e6:.0f} MB, {ro_rot[1] / l2_bytes:.1f} x L2)"},
         "tree_attn_fwd": {"bound": "tensor", "us": round(attn_launch_ms * 1e3, 2), "flops": flops_launch,
-                          "achieved": round(achieved, 2), "peak": peaks["tc"], "unit": "TFLOP/s",
-                          "frac": round(achieved / peaks["tc"], 4)},
+                          "achieved": round(achieved, 2), "peak": peaks["tc_burst"], "unit": "TFLOP/s",
+                          "frac": round(achieved / peaks["tc_burst"], 4)},
     }
+    if rank == 0 and not args.no_configs:
+        line["configs"] = measure_configs(lib, torch, dev, stream, peaks,
+                                          0.0 if (world > 1 or args.no_cpu_baseline) else args.oracle_budget)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if rank == 0:
@@ -831,6 +985,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload kernel and oracle figures")
+    ap.add_argument("--oracle-budget", type=float, default=4.0, help="host seconds of oracle per workload")
     ap.add_argument("--only", choices=["attn", "rope", "readout", "layer", "model"], default=None)
     ap.add_argument("--layers", type=int, default=16, help="layers for --only model (Llama-1B: 16)")
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets for --only (0: default)")

@@ -341,6 +341,59 @@ TREE_API int tree_attn_fwd_noalloc(const tree_plan_t *plan, const void *plan_dev
                                    const tree_attn_params_t *params, int32_t *status, tree_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Rows over several GPUs (host only)                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Rows of one batch shared out over n_ranks GPUs.  A query sees only its own
+ * prompt ("01 / Request path: Batch and prefix tree"; "03 / Packing: Attention
+ * over tree blocks"), so each GPU can plan and run a share of the rows with no
+ * data exchanged; every GPU keeps the resident blocks (the template, "03 /
+ * Packing: Shared state computed once"), and decisions are gathered on the host.
+ *
+ * A row is the subtree of a non-resident block whose parent is resident or
+ * absent, after identical siblings merge (rows that merge stay one).  Rows
+ * joined by a question (its two leaves in different rows) form one unit.  A
+ * unit costs its visible (query, key) pairs per head (a query at position p
+ * sees p + 1 keys).  Units are assigned longest first (ties: first in packed
+ * order) to the rank with the least cost so far (ties: lowest rank).
+ *
+ *   spec, opts     the batch, as for tree_pack_plan (opts->tiling is ignored)
+ *   block_rank     out, host int32 [spec->n_blocks]: the rank of every input
+ *                  block, -1 for resident blocks (kept by every rank)
+ *   question_rank  out, host int32 [spec->n_questions]: the rank answering it
+ *   rank_pairs     out, host int64 [n_ranks] or NULL: visible pairs per head
+ * Errors: those of tree_pack_plan; TREE_ERR_INVALID_ARG for n_ranks < 1 or a
+ * question whose leaf is a resident block.
+ */
+TREE_API int tree_shard_rows(const tree_spec_t *spec, const tree_plan_opts_t *opts, int32_t n_ranks,
+                             int32_t *block_rank, int32_t *question_rank, int64_t *rank_pairs);
+
+/* One rank's share of a batch, written by tree_shard_select into caller arrays
+ * of (at least) spec->n_blocks and spec->n_questions entries. */
+typedef struct {
+  int32_t n_blocks;         /* out: blocks kept, in input order */
+  int32_t *parent;          /* [n_blocks] parent among the kept blocks, -1 for a root */
+  int32_t *length;          /* [n_blocks] */
+  uint64_t *key;            /* [n_blocks] or NULL; 0 where the spec has no keys */
+  uint8_t *resident;        /* [n_blocks] or NULL; 0 where the spec has none */
+  int32_t *block_index;     /* [n_blocks] input block of each kept block */
+  int32_t n_questions;      /* out: questions kept, in input order */
+  int32_t *leaf1, *leaf2;   /* [n_questions] their leaves among the kept blocks */
+  int32_t *question_index;  /* [n_questions] input question of each kept one */
+} tree_shard_t;
+
+/*
+ * The blocks and questions of `rank` (as tree_shard_rows assigned them) as a
+ * forest of their own, blocks and questions in input order: planning it packs
+ * the rank's rows in the same order as in the whole batch.  Host only.
+ * Errors: TREE_ERR_INVALID_ARG (NULL arrays; a kept block whose parent is not
+ * kept; a question whose leaves are not kept).
+ */
+TREE_API int tree_shard_select(const tree_spec_t *spec, const int32_t *block_rank, const int32_t *question_rank,
+                               int32_t rank, tree_shard_t *out);
+
+/* ------------------------------------------------------------------------ */
 /* Letter readout and calibration                                            */
 /* ------------------------------------------------------------------------ */
 

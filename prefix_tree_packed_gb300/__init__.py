@@ -35,7 +35,7 @@ EXPORTS = (
     "tree_plan_chunk", "tree_plan_tables", "tree_plan_upload", "tree_plan_upload_staged", "tree_rope_table",
     "tree_rope",
     "tree_attn_fwd", "tree_attn_fwd_noalloc", "readout_decide", "tree_runtime_create", "tree_runtime_destroy",
-    "tree_runtime_step", "tree_runtime_attach_io", "tree_runtime_step_host",
+    "tree_runtime_step", "tree_runtime_attach_io", "tree_runtime_step_host", "tree_shard_rows", "tree_shard_select",
     # include/tree_queue.h
     "tree_queue_default_opts", "tree_queue_create", "tree_queue_destroy", "tree_queue_push", "tree_queue_cancel",
     "tree_queue_info", "tree_queue_pop", "tree_batch_view", "tree_batch_free",
@@ -131,6 +131,12 @@ class _View(C.Structure):
                                                      ("runs", _i32p), ("vkeys", _i32p), ("vruns", _i32p)]
 
 
+class _Shard(C.Structure):
+    _fields_ = [("n_blocks", C.c_int32), ("parent", C.c_void_p), ("length", C.c_void_p), ("key", C.c_void_p),
+                ("resident", C.c_void_p), ("block_index", C.c_void_p), ("n_questions", C.c_int32),
+                ("leaf1", C.c_void_p), ("leaf2", C.c_void_p), ("question_index", C.c_void_p)]
+
+
 class AttnParams(C.Structure):
     _fields_ = [("hq", C.c_int32), ("hkv", C.c_int32), ("d", C.c_int32), ("scale", C.c_float),
                 ("work", C.c_void_p), ("self_test", C.c_int32)]
@@ -176,6 +182,8 @@ _lib.tree_attn_fwd.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp, C.P
                                _vp, _vp]
 _lib.tree_attn_fwd_noalloc.argtypes = [_vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp, C.POINTER(AttnParams),
                                        _vp, _vp]
+_lib.tree_shard_rows.argtypes = [C.POINTER(_Spec), C.POINTER(_Opts), C.c_int32, _vp, _vp, _vp]
+_lib.tree_shard_select.argtypes = [C.POINTER(_Spec), _vp, _vp, C.c_int32, C.POINTER(_Shard)]
 _lib.readout_decide.argtypes = [_vp, C.c_int32, _vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, _vp, _vp, _vp]
 _lib.tree_runtime_create.argtypes = [C.c_size_t, C.c_int32, C.POINTER(_vp)]
 _lib.tree_runtime_destroy.argtypes = [_vp]
@@ -219,7 +227,7 @@ for _f in ("tree_gemm", "tree_gemm_ex", "tree_gemm_qkv", "tree_rmsnorm", "tree_l
     getattr(_lib, _f).restype = C.c_int
 for _f in ("tree_pack_plan", "tree_plan_free", "tree_plan_query", "tree_plan_chunk", "tree_plan_tables",
            "tree_plan_upload", "tree_plan_upload_staged", "tree_rope_table", "tree_rope", "tree_attn_fwd", "tree_attn_fwd_noalloc",
-           "readout_decide"):
+           "readout_decide", "tree_shard_rows", "tree_shard_select"):
     getattr(_lib, _f).restype = C.c_int
 
 
@@ -281,6 +289,37 @@ class Spec:
     @classmethod
     def from_forest(cls, forest, **kw):
         return cls(forest.parent, forest.length, forest.key, forest.resident, **kw)
+
+
+def shard_rows(spec: Spec, n_ranks: int):
+    """tree_shard_rows: (block_rank [n_blocks], question_rank [n_questions], rank_pairs [n_ranks])."""
+    nb, nq = spec.spec.n_blocks, spec.spec.n_questions
+    block_rank = np.empty(nb, np.int32)
+    question_rank = np.empty(max(nq, 1), np.int32)
+    pairs = np.empty(n_ranks, np.int64)
+    _check(_lib.tree_shard_rows(C.byref(spec.spec), C.byref(spec.opts), n_ranks, block_rank.ctypes.data,
+                                question_rank.ctypes.data, pairs.ctypes.data))
+    return block_rank, question_rank[:nq], pairs
+
+
+def shard_select(spec: Spec, block_rank, question_rank, rank: int) -> dict:
+    """tree_shard_select: the rank's blocks and questions as arrays (parent, length, key, resident,
+    block_index, leaf1, leaf2, question_index), in input order."""
+    nb, nq = spec.spec.n_blocks, spec.spec.n_questions
+    br = np.ascontiguousarray(block_rank, np.int32)
+    qr = np.ascontiguousarray(question_rank, np.int32) if nq else np.zeros(1, np.int32)
+    out = dict(parent=np.empty(nb, np.int32), length=np.empty(nb, np.int32), key=np.empty(nb, np.uint64),
+               resident=np.empty(nb, np.uint8), block_index=np.empty(nb, np.int32),
+               leaf1=np.empty(max(nq, 1), np.int32), leaf2=np.empty(max(nq, 1), np.int32),
+               question_index=np.empty(max(nq, 1), np.int32))
+    sh = _Shard(0, *(out[k].ctypes.data for k in ("parent", "length", "key", "resident", "block_index")), 0,
+                *(out[k].ctypes.data for k in ("leaf1", "leaf2", "question_index")))
+    _check(_lib.tree_shard_select(C.byref(spec.spec), br.ctypes.data, qr.ctypes.data, rank, C.byref(sh)))
+    for k in ("parent", "length", "key", "resident", "block_index"):
+        out[k] = out[k][:sh.n_blocks]
+    for k in ("leaf1", "leaf2", "question_index"):
+        out[k] = out[k][:sh.n_questions]
+    return out
 
 
 def gemm(a, b, c, m: int, n: int, k: int, epi: int = GEMM_STORE, r=None, status=None, stream=None, tile_n: int = 0):

@@ -1,8 +1,9 @@
 """The N > 1 path of bench.py on CPU: two gloo ranks, no GPU.
 
-Each rank plans its own seeded batch with the library's planner (checked against the
-oracle planner) and the only collective is the max over ranks of the timings; the
-reference arm runs on rank 0 alone.
+The job's batch (two copies of the Llama-1B-shaped rows) is split by rows over the ranks
+(tree_shard_rows); each rank plans its share with the library's planner (checked against the
+oracle planner), the collectives are the max over ranks of the timings, the sum of the ranks'
+tokens and the gather of the decisions on the host; the reference arm runs on rank 0 alone.
 """
 import os
 import socket
@@ -33,7 +34,7 @@ def _rank_main(rank, world, port, out):
     from oracle import plan as oplan
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        w = bench.rank_workload(2, rank)
+        w, qi = bench.rank_workload(2, rank, world)
         plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, leaf1=w.leaf1, leaf2=w.leaf2)
         ref, qm = oplan.plan_forest(w.forest, max_fwd=w.max_fwd, leaf1=w.leaf1, leaf2=w.leaf2)
         t = plan.tables()
@@ -42,9 +43,11 @@ def _rank_main(rank, world, port, out):
         q, _, _ = synth.draw_qkv(8, 8, w.hq, w.hkv, w.d, w.seed)
         # fake timings: the slower rank decides the job's time
         ms = bench.max_over_ranks(dist, [10.0 + rank, 20.0 - rank], "cpu")
+        toks = bench.job_tokens(dist, plan.info.n_fwd, "cpu")
+        dec = bench.gather_decisions(dist, world, qi, 1000 + qi)   # stand-in choices: the question's index
         gathered = [None] * world
         dist.all_gather_object(gathered, (float(q.astype(np.float64).sum()), ok, plan.info.n_fwd))
-        out.put((rank, ms, gathered))
+        out.put((rank, ms, gathered, toks, dec, len(qi)))
     finally:
         dist.destroy_process_group()
 
@@ -61,12 +64,15 @@ def test_two_ranks_plan_their_own_batches_and_reduce_timings():
         p.join(timeout=60)
         assert p.exitcode == 0
     res.sort()
-    for rank, ms, gathered in res:
+    for rank, ms, gathered, toks, dec, nq in res:
         assert ms == [11.0, 20.0]                       # max over ranks, elementwise
         (s0, ok0, n0), (s1, ok1, n1) = gathered
         assert ok0 and ok1                              # each rank's native plan equals the oracle's
         assert s0 != s1                                 # different inputs on each rank
-        assert n0 == n1 == 8192
+        assert n0 == n1 == 8192                         # 16 equal rows: 8 per rank
+        assert toks == 16384
+        assert nq == 32
+        assert np.array_equal(dec, 1000 + np.arange(64))   # every question answered once, in job order
     sys.path.insert(0, ROOT)
     import bench
     # whole-job throughput: both ranks' tokens over the slowest rank's time
