@@ -338,6 +338,18 @@ def test_attention_odd_head_ratio_d128(lib, hq, hkv, tiling):
     _attn_check(lib, w.forest, hq, hkv, 128, w.seed + hq, w.max_fwd, full=True, tiling=tiling)
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (16, 2), (8, 4), (12, 2), (6, 6)])
+def test_attention_d64_head_ratios(lib, hq, hkv):
+    """Head dim 64 takes a kernel instance by the q/kv head ratio: an even ratio runs two q heads per
+    work item (32/8, 16/2, 8/4, 12/2, with one or more pairs per kv head), an odd one a head per item
+    (6/6).  The Llama-1B-shaped rows in full, and random forests in chunks."""
+    w = synth.workload(2)
+    _attn_check(lib, w.forest, hq, hkv, 64, 40 + hq, w.max_fwd, full=True)
+    rng = np.random.default_rng(hq * 10 + hkv)
+    f = synth.random_forest(rng, n_roots=3, max_blocks=25, max_len=150, dup_prob=0.2, resident_root=True)
+    _attn_check(lib, f, hq, hkv, 64, 3, max_fwd=256, full=True, dynamic=False)
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_attention_random_forests_odd_ratio_d128(lib, seed):
     rng = np.random.default_rng(900 + seed)
