@@ -122,12 +122,12 @@ class Batch:
     plan buffers alternating so that the host plans step s+1 while the GPU runs step s.
     """
 
-    def __init__(self, lib, torch, w: synth.Workload, dev, n_sets=N_SETS, tiling=0):
+    def __init__(self, lib, torch, w: synth.Workload, dev, n_sets=N_SETS, tiling=0, pack_heads=0):
         self.lib, self.torch, self.w, self.dev = lib, torch, w, dev
         kw = dict(leaf1=w.leaf1, leaf2=w.leaf2) if w.leaf1 is not None else {}
         self.kw = kw
-        self.spec = lib.Spec.from_forest(w.forest, max_fwd=w.max_fwd, tiling=tiling, **kw)
-        self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, tiling=tiling, **kw)
+        self.spec = lib.Spec.from_forest(w.forest, max_fwd=w.max_fwd, tiling=tiling, pack_heads=pack_heads, **kw)
+        self.plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, tiling=tiling, pack_heads=pack_heads, **kw)
         i = self.plan.info
         self.info = i
         self.rt = lib.Runtime(i.dev_bytes + 4096, max(i.n_chunks, 1))
@@ -520,9 +520,9 @@ def run_only(args):
                     single_call_us=round(one_us, 2))
     else:
         w = synth.workload(args.workload)
-        B = Batch(lib, torch, w, dev, n_sets=args.sets or N_SETS, tiling=args.tiling)
+        B = Batch(lib, torch, w, dev, n_sets=args.sets or N_SETS, tiling=args.tiling, pack_heads=args.pack)
         B.plan.upload(B.pdev, B.info.dev_bytes, stream)
-        line.update(workload=w.name, sets=len(B.sets), tiling=args.tiling)
+        line.update(workload=w.name, sets=len(B.sets), tiling=args.tiling, pack_heads=B.info.pack_heads)
         if args.only == "layer":
             r = measure_layer(lib, torch, w, dev, stream, args.steps, args.warmup)
             tf = r["flops"] / (r["ms"] / 1e3) / 1e12
@@ -629,6 +629,30 @@ def measure_configs(lib, torch, dev, stream, peaks, oracle_s: float, numbers=(1,
         e["roofline_frac"] = e["tree_attn_fwd"]["frac_of_burst" if bound == "tensor" else "hbm_frac"]
         del B
         torch.cuda.empty_cache()
+        # gathered key tiles with the q heads of a kv head packed into one MMA tile (tiling 2), timed
+        # where they cut the MMA tiles visited: per kv head a packed entry meets each of the R q
+        # heads, a gathered one the two halves of its query tile
+        R = w.hq // w.hkv
+        if R in (2, 4, 8):
+            g_plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, tiling=2, pack_heads=R)
+            if g_plan.info.n_entries * 2 < 0.8 * i.n_entries * R:
+                Bg = Batch(lib, torch, w, dev, n_sets=n_sets, tiling=2, pack_heads=R)
+                gms = measure_attn(lib, torch, Bg, stream, reps=reps, warmup=3)
+                gbs_g = (set_bytes + Bg.info.dev_bytes) / gms / 1e6
+                tf_g = flops / (gms / 1e3) / 1e12
+                e["tree_attn_fwd_gathered"] = {
+                    "plan": f"tiling 2, pack_heads {R}", "us_per_forward": round(gms * 1e3, 2),
+                    "mma_tile_pairs_per_kv_head": int(g_plan.info.n_entries * 2),
+                    "packed_mma_tile_pairs_per_kv_head": int(i.n_entries * R),
+                    "tokens_per_s": round(i.n_fwd / (gms / 1e3), 1), "tflops": round(tf_g, 2),
+                    "frac_of_burst": round(tf_g / peaks["tc_burst"], 4), "gbs": round(gbs_g, 1),
+                    "hbm_frac": round(gbs_g / peaks["hbm"], 4)}
+                g_frac = e["tree_attn_fwd_gathered"]["frac_of_burst" if bound == "tensor" else "hbm_frac"]
+                if g_frac > e["roofline_frac"]:
+                    e["roofline_frac"] = g_frac
+                    e["roofline_from"] = "tree_attn_fwd_gathered"
+                del Bg
+                torch.cuda.empty_cache()
         if oracle_s > 0:
             e["oracle"] = oracle_sample(w, oracle_s, seed=n)
             e["oracle"]["kind"] = "oracle"
@@ -994,8 +1018,11 @@ def main():
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets for --only (0: default)")
     ap.add_argument("--questions", type=int, default=65536, help="questions for --only readout")
     ap.add_argument("--keys-only", action="store_true", help="--only rope: rotate the keys alone")
-    ap.add_argument("--tiling", type=int, default=0, choices=[0, 1],
-                    help="--only attn: key tiles of 128 packed keys (0) or by position (1, batch-invariant)")
+    ap.add_argument("--tiling", type=int, default=0, choices=[0, 1, 2],
+                    help="--only attn: key tiles of 128 packed keys (0), by position (1, batch-invariant) or "
+                         "gathered (2: the keys some query of the tile sees)")
+    ap.add_argument("--pack", type=int, default=0, choices=[0, 1, 2, 4, 8],
+                    help="--only attn with --tiling 2: q heads packed into one MMA tile (the q/kv head ratio)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

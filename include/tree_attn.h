@@ -112,7 +112,14 @@ typedef struct {
                         1 = by position: each query sees its keys in tiles of 128 positions of
                         its own prompt (key at position p in slot p % 128, tiles in increasing
                         position), so its result does not depend on the other prompts of the
-                        batch ("05 / Reproducibility": attention tiled by position) */
+                        batch ("05 / Reproducibility": attention tiled by position);
+                        2 = gathered: the keys that some query of the tile sees, in packed
+                        order, 128 to a tile (no tile spent on keys nobody in the query tile
+                        sees: for batches of short prompts under a shared template) */
+  int32_t pack_heads; /* q heads packed into one 128-row MMA tile with tiling 2 [1]: 1, 2, 4 or 8.
+                        With R > 1 a query tile holds 256 / R tokens, attended as two MMA tiles
+                        of R heads x 128 / R tokens that share each gathered K/V tile; the
+                        attention then needs hq / hkv == R. */
 } tree_plan_opts_t;
 
 typedef struct tree_plan tree_plan_t;
@@ -156,7 +163,7 @@ typedef struct {
   int32_t n_slots;       /* readout slots */
   int32_t n_questions;
   int32_t max_fwd;
-  int32_t bm, bn;        /* query / key tile rows (128 / 128) */
+  int32_t bm, bn;        /* query tile tokens (128; 256 / pack_heads with packed heads) / key tile rows (128) */
   int32_t max_pos;       /* 1 + largest position: rows needed in the RoPE table */
   int64_t pairs;         /* visible (query, key) pairs over all forward tokens */
   size_t dev_bytes;      /* size of the device image (tree_plan_upload) */
@@ -164,7 +171,8 @@ typedef struct {
   size_t off_pos, off_send, off_qtile, off_ent, off_order, off_chunk, off_slot_tok, off_r1, off_r2;
   size_t off_runs;       /* run tables of the key tiles (see tree_plan_host_view_t.runs) */
   int32_t tiling;        /* as in tree_plan_opts_t */
-  size_t off_vkeys, off_vruns; /* tiling 1: per entry its 128 gathered keys and its run table */
+  size_t off_vkeys, off_vruns; /* tiling 1, 2: per entry its 128 gathered keys and its run table */
+  int32_t pack_heads;    /* as in tree_plan_opts_t (1 when not packed) */
 } tree_plan_info_t;
 
 TREE_API int tree_plan_query(const tree_plan_t *plan, tree_plan_info_t *info);
@@ -201,7 +209,7 @@ typedef struct {
                            send, words 20 + 4r .. 23 + 4r its keys as a 128-bit mask (key c of the
                            tile is bit c % 32 of word c / 32); all else 0.  A query i sees the keys
                            of run r, apart from keys after i, iff i < send of r. */
-  /* tiling 1 only (else NULL).  Entry e of the tile lists is a virtual key tile.  ent[e] =
+  /* tiling 1 and 2 (else NULL).  Entry e of the tile lists is a virtual key tile.  ent[e] =
      (e << 2) | contiguous << 1 | 1 (contiguous: its slots hold the consecutive packed keys
      vkeys[128 e] + c), or (j0 << 2) | 2 when every row of the query tile takes this range from it
      and sees every slot, slot c holding key j0 + c (no mask: a packed key tile).  Per entry: vkeys[128 e + c] = the packed key in slot c (0 for an empty slot, which no query
@@ -209,7 +217,10 @@ typedef struct {
      the query tile's rows that take their keys of this position range from this entry, then per
      run r words 8 + 4r .. 11 + 4r = {first slot c0, last slot c1, packed key j0 in c0, its send}:
      the run's slots hold the consecutive keys j0 + (c - c0) of one block.  Query i of an
-     assigned row sees slot c of run r iff c - c0 <= i - j0 and j0 <= i < send. */
+     assigned row sees slot c of run r iff c - c0 <= i - j0 and j0 <= i < send.  With tiling 2
+     every row of the query tile is assigned to every entry of its list, an entry holds at most
+     16 runs, and "contiguous" means that all 128 slots hold consecutive keys (it may have
+     several runs). */
   const int32_t *vkeys, *vruns;
 } tree_plan_host_view_t;
 
@@ -413,6 +424,11 @@ TREE_API int tree_shard_select(const tree_spec_t *spec, const int32_t *block_ran
  *               of 1..min(stride,255) or some T <= 0 (that question's
  *               outputs are zero, choice -1)
  * All arithmetic in f32.  n_q == 0 is a no-op.
+ * The kernel is a programmatic dependent launch: for strides up to 32 it reads
+ * r1, r2, n_letters and temperature before the kernel ahead of it in the
+ * stream has finished (the logits only after), so a kernel that lets its
+ * dependents launch early (griddepcontrol.launch_dependents) must not write
+ * them; the library's own kernels never do.
  */
 TREE_API int readout_decide(const float *logits, int32_t stride, const int32_t *r1, const int32_t *r2,
                    const int32_t *n_letters, const float *temperature, int32_t n_q, float *p_cal,

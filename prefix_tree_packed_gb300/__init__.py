@@ -102,7 +102,8 @@ class LayerWeights(C.Structure):
 
 
 class _Opts(C.Structure):
-    _fields_ = [("max_fwd", C.c_int32), ("max_depth", C.c_int32), ("max_row", C.c_int32), ("tiling", C.c_int32)]
+    _fields_ = [("max_fwd", C.c_int32), ("max_depth", C.c_int32), ("max_row", C.c_int32), ("tiling", C.c_int32),
+                ("pack_heads", C.c_int32)]
 
 
 class PlanInfo(C.Structure):
@@ -112,7 +113,7 @@ class PlanInfo(C.Structure):
         ("pairs", C.c_int64), ("dev_bytes", C.c_size_t)] + [(n, C.c_size_t) for n in (
         "off_pos", "off_send", "off_qtile", "off_ent", "off_order", "off_chunk", "off_slot_tok",
         "off_r1", "off_r2", "off_runs")] + [("tiling", C.c_int32), ("off_vkeys", C.c_size_t),
-                                            ("off_vruns", C.c_size_t)]
+                                            ("off_vruns", C.c_size_t), ("pack_heads", C.c_int32)]
 
 
 class ChunkInfo(C.Structure):
@@ -260,7 +261,7 @@ class Spec:
     """A batch's forest as the planner reads it (arrays kept alive, struct built once)."""
 
     def __init__(self, parent, length, key=None, resident=None, leaf1=None, leaf2=None,
-                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0, tiling: int = 0):
+                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0, tiling: int = 0, pack_heads: int = 0):
         self._keep = []
         par = np.ascontiguousarray(parent, np.int32)
         ln = np.ascontiguousarray(length, np.int32)
@@ -284,7 +285,7 @@ class Spec:
             self.spec.leaf1 = l1.ctypes.data_as(_i32p)
             self.spec.leaf2 = l2.ctypes.data_as(_i32p)
             self._keep += [l1, l2]
-        self.opts = _Opts(max_fwd, max_depth, max_row, tiling)
+        self.opts = _Opts(max_fwd, max_depth, max_row, tiling, pack_heads)
 
     @classmethod
     def from_forest(cls, forest, **kw):
@@ -560,7 +561,7 @@ class Plan:
     """A packed batch: owns the library's host plan (``tree_pack_plan``)."""
 
     def __init__(self, parent, length, key=None, resident=None, leaf1=None, leaf2=None,
-                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0, tiling: int = 0):
+                 max_fwd: int = 0, max_depth: int = 0, max_row: int = 0, tiling: int = 0, pack_heads: int = 0):
         self._keep = []
         par = np.ascontiguousarray(parent, np.int32)
         ln = np.ascontiguousarray(length, np.int32)
@@ -584,7 +585,7 @@ class Plan:
             spec.leaf1 = l1.ctypes.data_as(_i32p)
             spec.leaf2 = l2.ctypes.data_as(_i32p)
             self._keep += [l1, l2]
-        opts = _Opts(max_fwd, max_depth, max_row, tiling)
+        opts = _Opts(max_fwd, max_depth, max_row, tiling, pack_heads)
         h = _vp()
         _check(_lib.tree_pack_plan(C.byref(spec), C.byref(opts), C.byref(h)))
         self._keep = []
@@ -630,7 +631,7 @@ class Plan:
         out["image"] = np.ctypeslib.as_array(C.cast(v.image, C.POINTER(C.c_uint8)),
                                              shape=(v.image_bytes,)).copy()
         out["runs"] = np.ctypeslib.as_array(v.runs, shape=(n_kvt, 84)).copy()
-        if i.tiling == 1 and i.n_entries > 0:
+        if i.tiling != 0 and i.n_entries > 0:
             out["vkeys"] = np.ctypeslib.as_array(v.vkeys, shape=(i.n_entries, 128)).copy()
             out["vruns"] = np.ctypeslib.as_array(v.vruns, shape=(i.n_entries, 72)).copy()
         return out

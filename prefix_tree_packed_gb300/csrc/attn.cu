@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 #include "attn_common.cuh"
@@ -112,11 +113,16 @@ struct Bars {
 // every barrier phase follows that count (or the item count for per-item
 // barriers), so the producer and MMA warps run ahead into the next item while
 // the softmax warps finish the current one.
-template <int D, int NH, bool G>
+// HP (packed heads, with gathered key tiles): the item is a query tile of 2 x tpm
+// tokens and one kv head; MMA tile h holds tokens [row0 + h tpm, row0 + (h+1) tpm)
+// of all ratio = 128 / tpm q heads (row r: head h0 + r / tpm, token r % tpm), so
+// the item's K/V tiles serve every q head of the kv head at once.
+template <int D, int NH, bool G, bool HP>
 __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     tree_attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
-                 const __grid_constant__ CUtensorMap mkg, const __grid_constant__ CUtensorMap mvg, const AttnArgs a) {
+                 const __grid_constant__ CUtensorMap mkg, const __grid_constant__ CUtensorMap mvg,
+                 const __grid_constant__ BoxMaps bm, const AttnArgs a) {
   using C = Cfg<D, NH>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
@@ -214,6 +220,28 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         ok = wait_bar(smem_u32(&bars.never), 0, abort, a.status, true, kSelfTestNs);
         ok = __all_sync(0xffffffffu, ok);
       }
+      // the Q tile(s) of item `qi` into buffer qb
+      auto issue_q = [&](int qb, const Item &qi) {
+        if (elect_one()) {
+          mbar_expect_tx(b_qf(qb), C::Q_BYTES);
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+#pragma unroll
+            for (int c = 0; c < C::CB; ++c) {
+              const uint32_t dst = s_base + C::Q_OFF + qb * C::Q_BYTES + (h * C::CB + c) * BOX_BYTES;
+              if (HP) {
+                // tpm rows of each q head, one box each (tpm >= 16: every sub-box starts on a
+                // 1024-byte swizzle period, so the tile is laid out as one 128-row box)
+                for (int hh = 0; hh < a.ratio; ++hh)
+                  tma_load_2d(dst + hh * a.tpm * 128, &mq, (qi.h0 + hh) * D + 64 * c,
+                              qi.qt.row0 - a.q0 + h * a.tpm, b_qf(qb));
+              } else {
+                tma_load_2d(dst, &mq, (qi.h0 + h) * D + 64 * c, qi.qt.row0 - a.q0, b_qf(qb));
+              }
+            }
+        }
+        __syncwarp();
+      };
       while (ok) {
         // claim the next item and publish it in the ring (a value >= n_items ends the list)
         const int slot = fetched % kRing;
@@ -227,7 +255,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         Item it{};
         int e0 = 0;
         if (w < a.n_items) {
-          it = item_at<NH>(a, w);
+          it = item_at<NH, HP>(a, w);
           if (it.n > 0) e0 = __ldg(a.ent + it.qt.ent0);
         }
         if (lane == 0) {
@@ -250,16 +278,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         if (it.n <= 0) continue;  // (a plan never makes one: every query tile sees its own rows)
         const int b = j % C::QBUF;
         if (j >= C::QBUF && !(ok = wait_bar_warp(b_qe(b), ((j / C::QBUF) - 1) & 1, abort, a.status))) break;
-        if (elect_one()) {
-          mbar_expect_tx(b_qf(b), C::Q_BYTES);
-#pragma unroll
-          for (int h = 0; h < NH; ++h)
-#pragma unroll
-            for (int c = 0; c < C::CB; ++c)
-              tma_load_2d(s_base + C::Q_OFF + b * C::Q_BYTES + (h * C::CB + c) * BOX_BYTES, &mq,
-                          (it.h0 + h) * D + 64 * c, it.qt.row0 - a.q0, b_qf(b));
-        }
-        __syncwarp();
+        issue_q(b, it);
         for (int i = 0; i < it.n; ++i, ++t) {
           const int st = t % C::STAGES;
           if (t >= C::STAGES && !(ok = wait_bar_warp(b_e(st), ((t / C::STAGES) - 1) & 1, abort, a.status))) break;
@@ -285,6 +304,50 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
               continue;
             }
             const int e = ev >> 2;
+            if (a.boxes && !(ev & 2)) {
+              // gathered tile (tiling 2): lane r loads the slots of run r, widened to whole
+              // groups of 8 rows, as tiled boxes of 8, 16, 32, 64 or 128 rows.  A stretch of
+              // consecutive keys starts at a multiple of 8 slots, so every box lands on a
+              // 1024-byte swizzle period; where two runs of one stretch share a group of 8 both
+              // write the same keys there, and rows past a stretch (keys of other blocks, or the
+              // fill value past the last key) go to slots no run covers.
+              const int32_t *vr = a.vruns + (size_t)e * kVRunWords;
+              const int R = __ldg(vr);
+              int4 run = make_int4(0, -1, 0, 0);
+              if (lane < R) run = __ldg(reinterpret_cast<const int4 *>(vr + 8) + lane);
+              // the last run loads through slot 127: every slot then holds finite keys and
+              // values (an unloaded V row could hold NaN, and 0 * NaN would reach O)
+              const int s0 = run.x & ~7;
+              const int nr = lane < R ? (lane == R - 1 ? 127 : (run.y | 7)) - s0 + 1 : 0;
+              const uint32_t kb = __reduce_add_sync(0xffffffffu, (uint32_t)nr) * 128u * C::CB;
+              const uint32_t v_bar = C::KV_ONE ? b_k(st) : b_v(st);
+              if (lane == 0) {
+                mbar_expect_tx(b_k(st), (C::KV_ONE ? 2 : 1) * kb + kVRunWords * 4);
+                bulk_load(s_base + C::RUNS_OFF + st * 512, vr, kVRunWords * 4, b_k(st));
+                if (!C::KV_ONE) mbar_expect_tx(v_bar, kb);
+              }
+              __syncwarp();
+              if (nr > 0) {
+                int y = run.z - (run.x - s0), slot = s0;
+#pragma unroll
+                for (int lg = 4; lg >= 0; --lg) {  // boxes of 8 << lg rows
+                  if (!(((nr >> 3) >> lg) & 1)) continue;
+                  const CUtensorMap *km = lg == 4 ? &mk : &bm.k[lg], *vm = lg == 4 ? &mv : &bm.v[lg];
+#pragma unroll
+                  for (int c = 0; c < C::CB; ++c)
+                    tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES + slot * 128, km, it.g * D + 64 * c,
+                                y, b_k(st));
+#pragma unroll
+                  for (int c = 0; c < C::CB; ++c)
+                    tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES + slot * 128, vm, it.g * D + 64 * c,
+                                y, v_bar);
+                  slot += 8 << lg;
+                  y += 8 << lg;
+                }
+              }
+              __syncwarp();
+              continue;
+            }
             const int4 rows = __ldg(reinterpret_cast<const int4 *>(a.vkeys + (size_t)e * BN) + lane);
             const int jc = __shfl_sync(0xffffffffu, rows.x, 0);  // slot 0's key
             const uint32_t v_bar = C::KV_ONE ? b_k(st) : b_v(st);
@@ -548,13 +611,22 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
         fence_async_shared();
         mbar_arrive(b_osq(h));
         if (r == 0 && wait_bar(b_osq(h), use & 1, abort, a.status)) {
-          tma_store_2d(&mo, (pit.h0 + h) * D + 64 * c, pit.qt.row0 - a.q0, stage);
+          if (HP) {
+            // rows past the query tile are clipped by the store (they lie past the chunk);
+            // a half that starts past it stores nothing
+            if (pit.qt.row0 + h * a.tpm < pit.qt.row1)
+              for (int hh = 0; hh < a.ratio; ++hh)
+                tma_store_2d(&mo, (pit.h0 + hh) * D + 64 * c, pit.qt.row0 - a.q0 + h * a.tpm,
+                             stage + hh * a.tpm * 128);
+          } else {
+            tma_store_2d(&mo, (pit.h0 + h) * D + 64 * c, pit.qt.row0 - a.q0, stage);
+          }
           bulk_commit();
         }
       }
       if (a.lse && piq < pit.qt.row1) {
         const float mu = (pm == -INFINITY) ? 0.f : pm;
-        a.lse[(size_t)(piq - a.q0) * a.hq + pit.h0 + h] = (mu + __log2f(pl)) * 0.69314718055994531f;
+        a.lse[(size_t)(piq - a.q0) * a.hq + pit.h0 + (HP ? r / a.tpm : h)] = (mu + __log2f(pl)) * 0.69314718055994531f;
       }
       pend = false;
       return true;
@@ -568,7 +640,9 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
       mbar_arrive(b_ie(slot));
       if (w >= a.n_items) break;
       if (it.n <= 0) continue;
-      const int iq = it.qt.row0 + r;
+      // this thread's row of the query tile: its token, and (packed heads) its q head's rows
+      const int srow = HP ? h * a.tpm + (r & (a.tpm - 1)) : r;
+      const int iq = it.qt.row0 + srow;
       float m = -INFINITY, l = 0.f;
       for (int i = 0; i < it.n; ++i, ++T) {
         const int st = T % C::STAGES;
@@ -599,7 +673,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
           // an assigned row sees slot c of run r iff c - c0 <= iq - j0 and j0 <= iq < send
           const int32_t *tb = sRuns + st * 128;
           uint32_t mw[4] = {0u, 0u, 0u, 0u};
-          if ((tb[4 + (r >> 5)] >> (r & 31)) & 1) {
+          if ((tb[4 + (srow >> 5)] >> (srow & 31)) & 1) {
             const int R = tb[0];
 #pragma unroll
             for (int rr = 0; rr < kMaxRuns; ++rr) {
@@ -759,19 +833,31 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
               float *lse, int hq, int hkv, float scale, int32_t *work, int32_t self_test, int32_t *status,
               cudaStream_t s) {
   using C = Cfg<D, NH>;
-  const bool gather = P.tiling == 1;
-  auto kern = gather ? tree_attn_tc<D, NH, true> : tree_attn_tc<D, NH, false>;
+  const bool gather = P.tiling != 0;
+  // packed heads (NH == 2 only): tokens per MMA tile, the Q and O boxes' height
+  const bool hp = NH == 2 && P.pack_heads > 1;
+  const int tpm = hp ? BN / P.pack_heads : BN;
+  auto kern = gather ? tree_attn_tc<D, NH, true, false> : tree_attn_tc<D, NH, false, false>;
+  if constexpr (NH == 2)
+    if (hp) kern = tree_attn_tc<D, NH, true, true>;
   int rc = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), (int)C::SMEM, "tree_attn_fwd");
   if (rc) return rc;
   const int32_t q0 = P.chunk_q0[chunk], nq = P.chunk_q1[chunk] - q0;
   CUtensorMap mq, mk, mv, mo, mkg, mvg;
-  if ((rc = make_map(&mq, q, (int64_t)hq * D, nq, "tree_attn_fwd")) ||
+  BoxMaps bm;
+  std::memset(&bm, 0, sizeof bm);
+  if ((rc = make_map(&mq, q, (int64_t)hq * D, nq, "tree_attn_fwd", tpm)) ||
       (rc = make_map(&mk, k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
       (rc = make_map(&mv, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd")) ||
       (rc = make_map(&mkg, k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", 1)) ||
       (rc = make_map(&mvg, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", 1)) ||
-      (rc = make_map(&mo, o, (int64_t)hq * D, nq, "tree_attn_fwd")))
+      (rc = make_map(&mo, o, (int64_t)hq * D, nq, "tree_attn_fwd", tpm)))
     return rc;
+  if (P.tiling == 2)
+    for (int lg = 0; lg < 4; ++lg)
+      if ((rc = make_map(&bm.k[lg], k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", 8 << lg)) ||
+          (rc = make_map(&bm.v[lg], v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", 8 << lg)))
+        return rc;
   AttnArgs a;
   a.send = img + P.off_send;
   a.runs = img + P.off_runs;
@@ -792,11 +878,13 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
   a.scale_log2 = scale * 1.4426950408889634f;
   a.self_test = self_test;
   const int tiles = P.chunk_t1[chunk] - P.chunk_t0[chunk];
-  a.n_items = tiles * hkv * (a.ratio / NH);
+  a.tpm = tpm;
+  a.boxes = P.tiling == 2;
+  a.n_items = tiles * hkv * (hp ? 1 : a.ratio / NH);
   a.work = work;
   if (a.n_items == 0) return TREE_OK;
   const dim3 grid((unsigned)std::min(a.n_items, sm_count()));
-  const cudaError_t e = launch_dependent(kern, grid, dim3(C::THREADS), C::SMEM, s, mq, mk, mv, mo, mkg, mvg, a);
+  const cudaError_t e = launch_dependent(kern, grid, dim3(C::THREADS), C::SMEM, s, mq, mk, mv, mo, mkg, mvg, bm, a);
   if (e != cudaSuccess) return fail(TREE_ERR_CUDA, "tree_attn_fwd: launch failed: %s", cudaGetErrorString(e));
   return launch_status("tree_attn_fwd");
 }
@@ -824,6 +912,9 @@ extern "C" TREE_API int tree_attn_fwd(const tree_plan_t *plan, const void *plan_
   const int32_t *img = reinterpret_cast<const int32_t *>(plan_dev);
   const cudaStream_t s = as_stream(stream);
   const bool pair = (hq / hkv) % 2 == 0;
+  if (P.pack_heads > 1 && hq / hkv != P.pack_heads)
+    return fail(TREE_ERR_UNSUPPORTED, "tree_attn_fwd: the plan packs %d q heads per kv head, the launch has %d / %d",
+                P.pack_heads, hq, hkv);
   if (d == 64)
     return pair ? launch_tc<64, 2>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, params->self_test, status, s)
                 : launch_tc<64, 1>(P, img, chunk, q, k, v, o, lse, hq, hkv, scale, params->work, params->self_test, status, s);

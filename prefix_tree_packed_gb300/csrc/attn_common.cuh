@@ -32,6 +32,13 @@ struct AttnArgs {
   int32_t *work;    // {next item, finished CTAs} or nullptr for the round-robin schedule
   float scale_log2;
   int32_t self_test;  // the timeout self-test (see tree_attn_params_t)
+  int32_t tpm;        // packed heads: tokens per 128-row MMA tile (128 / q heads per kv head)
+  int32_t boxes;      // gathered tiles (tiling 2): runs load as tiled boxes of 8k rows, not row by row
+};
+
+// Tiling 2: maps of K and V with boxes of 8, 16, 32 and 64 rows (64 columns).
+struct BoxMaps {
+  CUtensorMap k[4], v[4];
 };
 
 constexpr int kRing = 4;  // items handed from the producer to the MMA and softmax warps
@@ -73,9 +80,11 @@ struct Item {
   int g;   // kv head
 };
 
-template <int NH>
+// With packed heads (HP) an item is a query tile and one kv head, and h0 is the
+// first of all ratio q heads that read it (the MMA tiles hold every q head).
+template <int NH, bool HP = false>
 TREE_DEV Item item_at(const AttnArgs &a, int w) {
-  const int groups = a.ratio / NH;
+  const int groups = HP ? 1 : a.ratio / NH;
   const int per_tile = a.hkv * groups;
   const int rank = w / per_tile;
   const int rem = w - rank * per_tile;

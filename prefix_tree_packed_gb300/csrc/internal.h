@@ -33,6 +33,7 @@ struct Plan {
          off_slot_tok = 0, off_r1 = 0, off_r2 = 0, off_runs = 0;  // in int32 words
   // tiling by position: per entry its gathered keys and run table (see tree_plan_host_view_t)
   int32_t tiling = 0;
+  int32_t pack_heads = 1;  // q heads per 128-row MMA tile (1: one head per tile)
   std::vector<int32_t> vkeys, vruns;
   size_t off_vkeys = 0, off_vruns = 0;
 };

@@ -66,11 +66,16 @@ bool all_bits(const int32_t *w, int32_t n) {
   return true;
 }
 
-int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_row, int32_t tiling, Plan &P) {
+int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_row, int32_t tiling,
+          int32_t pack_heads, Plan &P) {
   const int32_t nb = s.n_blocks;
   P.n_input_blocks = nb;
   P.max_fwd = max_fwd;
   P.tiling = tiling;
+  P.pack_heads = pack_heads > 1 ? pack_heads : 1;
+  // with R q heads packed per 128-row MMA tile, a query tile is two such tiles of 128 / R tokens
+  P.bm = P.pack_heads > 1 ? 2 * (kTile / P.pack_heads) : kTile;
+  const int32_t bm = P.bm;
   // ---- validation of the input forest
   for (int32_t b = 0; b < nb; ++b) {
     const int32_t p = s.parent[b];
@@ -361,10 +366,77 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
     }
   };
 
+  // ---- gathered key tiles (tiling 2).  A query sees every key of its ancestor
+  // blocks and the keys of its own block up to itself, so the keys that some
+  // query of the tile [i0, i1) sees are: each block with rows in the tile up to
+  // its last row there, and the whole of every ancestor of those blocks.  They
+  // fill entries of 128 slots in packed order, a run per piece of a block
+  // (consecutive keys, one subtree end), at most kMaxRuns runs per entry.  A
+  // run whose first key does not follow the previous run's last starts at a
+  // slot that is a multiple of 8, so that the kernel loads each stretch of
+  // consecutive keys as tiled boxes of 8k rows (the rows past a stretch's end
+  // land in slots no run covers).
+  std::vector<std::pair<int32_t, int32_t>> gathered;  // (block, key end), then merged per block
+  auto add_gathered_tiles = [&](int32_t i0, int32_t i1) {
+    gathered.clear();
+    for (int32_t b = block_of(i0); b < nbc && bstart[b] < i1; ++b) {
+      if (bstart[b] + blen[b] <= i0) continue;
+      gathered.emplace_back(b, std::min(i1, bstart[b] + blen[b]));
+      for (int32_t x = P.blk_parent[b]; x >= 0; x = P.blk_parent[x]) gathered.emplace_back(x, bstart[x] + blen[x]);
+    }
+    std::sort(gathered.begin(), gathered.end());
+    int32_t e = -1, slot = kTile, nrun = kMaxRuns;
+    size_t kb = 0, rb = 0;
+    auto finish = [&]() {  // contiguous: every slot holds key (slot 0's key) + c; full: no mask at all
+      if (e < 0) return;
+      const int32_t *vk = P.vkeys.data() + kb, *run = P.vruns.data() + rb;
+      bool contig = slot == kTile && run[0] > 0;
+      for (int32_t c = 1; c < kTile && contig; ++c) contig = vk[c] == vk[0] + c;
+      bool full = contig && vk[kTile - 1] <= i0;
+      for (int32_t r = 0; r < run[0] && full; ++r) full = run[8 + 4 * r + 3] > i1 - 1;
+      P.ent[(size_t)e] = full ? ((vk[0] << 2) | 2) : ((e << 2) | (contig ? 2 : 0) | 1);
+    };
+    for (size_t g = 0; g < gathered.size(); ++g) {
+      const int32_t blk = gathered[g].first;
+      int32_t end = gathered[g].second;
+      while (g + 1 < gathered.size() && gathered[g + 1].first == blk) end = std::max(end, gathered[++g].second);
+      int32_t j = bstart[blk];
+      while (j < end) {
+        if (nrun > 0 && slot < kTile) {
+          const int32_t *prev = P.vruns.data() + rb + 8 + 4 * (nrun - 1);
+          if (prev[2] + (prev[1] - prev[0]) + 1 != j) slot = (slot + 7) & ~7;  // a new stretch of keys
+        }
+        if (slot >= kTile || nrun == kMaxRuns) {
+          finish();
+          e = (int32_t)P.ent.size();
+          P.ent.push_back(0);
+          kb = P.vkeys.size();
+          rb = P.vruns.size();
+          P.vkeys.resize(kb + kTile, 0);
+          P.vruns.resize(rb + kVRunWords, 0);
+          set_bits(P.vruns.data() + rb + 4, 0, i1 - i0);  // every row of the tile takes every entry
+          slot = 0;
+          nrun = 0;
+        }
+        const int32_t n = std::min(end - j, kTile - slot);
+        for (int32_t c = 0; c < n; ++c) P.vkeys[kb + slot + c] = j + c;
+        int32_t *run = P.vruns.data() + rb + 8 + 4 * nrun;
+        run[0] = slot;
+        run[1] = slot + n - 1;
+        run[2] = j;
+        run[3] = bsend[blk];
+        P.vruns[rb] = ++nrun;
+        slot += n;
+        j += n;
+      }
+    }
+    finish();
+  };
+
   // ---- chunks, query tiles, tile lists
   const int32_t n_fwd = P.n_tot - P.n_res;
   P.n_chunks = (n_fwd + max_fwd - 1) / max_fwd;
-  const int32_t n_qt_est = (n_fwd + kTile - 1) / kTile + P.n_chunks;
+  const int32_t n_qt_est = (n_fwd + bm - 1) / bm + P.n_chunks;
   P.qt_row0.reserve(n_qt_est);
   P.qt_row1.reserve(n_qt_est);
   P.qt_ent0.reserve(n_qt_est);
@@ -400,13 +472,18 @@ int build(const tree_spec_t &s, int32_t max_fwd, int32_t max_depth, int32_t max_
     P.chunk_t0.push_back((int32_t)P.qt_row0.size());
     P.chunk_pairs.push_back(pairs_in(q0, q1));
     const int32_t e_begin = (int32_t)P.ent.size();
-    for (int32_t i0 = q0; i0 < q1; i0 += kTile) {
-      const int32_t i1 = std::min(i0 + kTile, q1);
+    for (int32_t i0 = q0; i0 < q1; i0 += bm) {
+      const int32_t i1 = std::min(i0 + bm, q1);
       P.qt_row0.push_back(i0);
       P.qt_row1.push_back(i1);
       P.qt_ent0.push_back((int32_t)P.ent.size());
       if (tiling == 1) {
         add_position_tiles(i0, i1);
+        P.qt_ent1.push_back((int32_t)P.ent.size());
+        continue;
+      }
+      if (tiling == 2) {
+        add_gathered_tiles(i0, i1);
         P.qt_ent1.push_back((int32_t)P.ent.size());
         continue;
       }
@@ -610,7 +687,7 @@ extern "C" {
 
 const char *tree_last_error(void) { return tree::g_err.c_str(); }
 
-int tree_version(void) { return 100; }
+int tree_version(void) { return 101; }
 
 int tree_pack_plan(const tree_spec_t *spec, const tree_plan_opts_t *opts, tree_plan_t **out) {
   if (!spec || !out) return tree::fail(TREE_ERR_INVALID_ARG, "tree_pack_plan: NULL spec or out");
@@ -619,23 +696,28 @@ int tree_pack_plan(const tree_spec_t *spec, const tree_plan_opts_t *opts, tree_p
     return tree::fail(TREE_ERR_INVALID_ARG, "tree_pack_plan: empty forest or NULL parent/length");
   if (spec->n_questions < 0 || (spec->n_questions > 0 && (!spec->leaf1 || !spec->leaf2)))
     return tree::fail(TREE_ERR_INVALID_ARG, "tree_pack_plan: bad question arrays");
-  int32_t max_fwd = 8192, max_depth = 8, max_row = 32768, tiling = 0;
+  int32_t max_fwd = 8192, max_depth = 8, max_row = 32768, tiling = 0, pack_heads = 0;
   if (opts) {
     if (opts->max_fwd) max_fwd = opts->max_fwd;
     if (opts->max_depth) max_depth = opts->max_depth;
     if (opts->max_row) max_row = opts->max_row;
     tiling = opts->tiling;
+    pack_heads = opts->pack_heads;
   }
   if (max_fwd <= 0 || max_fwd % 128 != 0)
     return tree::fail(TREE_ERR_UNSUPPORTED, "max_fwd %d is not a positive multiple of 128", max_fwd);
   if (max_depth <= 0 || max_row <= 0) return tree::fail(TREE_ERR_INVALID_ARG, "bad limits");
-  if (tiling != 0 && tiling != 1) return tree::fail(TREE_ERR_INVALID_ARG, "tiling %d is neither 0 nor 1", tiling);
+  if (tiling < 0 || tiling > 2) return tree::fail(TREE_ERR_INVALID_ARG, "tiling %d is not 0, 1 or 2", tiling);
+  if (pack_heads < 0 || pack_heads > 8 || (pack_heads & (pack_heads - 1)))
+    return tree::fail(TREE_ERR_INVALID_ARG, "pack_heads %d is not 0, 1, 2, 4 or 8", pack_heads);
+  if (pack_heads > 1 && tiling != 2)
+    return tree::fail(TREE_ERR_UNSUPPORTED, "pack_heads %d needs gathered key tiles (tiling 2)", pack_heads);
   if (tiling == 1 && max_depth > tree::kMaxRuns)
     return tree::fail(TREE_ERR_UNSUPPORTED, "tiling by position needs max_depth <= %d", tree::kMaxRuns);
   auto *pl = new (std::nothrow) tree_plan;
   if (!pl) return tree::fail(TREE_ERR_INVALID_ARG, "out of host memory");
   tree::take_spare(pl->p);
-  const int rc = tree::build(*spec, max_fwd, max_depth, max_row, tiling, pl->p);
+  const int rc = tree::build(*spec, max_fwd, max_depth, max_row, tiling, pack_heads, pl->p);
   if (rc != TREE_OK) {
     tree::give_spare(pl->p);
     delete pl;
@@ -684,6 +766,7 @@ int tree_plan_query(const tree_plan_t *plan, tree_plan_info_t *info) {
   info->tiling = P.tiling;
   info->off_vkeys = P.off_vkeys * 4;
   info->off_vruns = P.off_vruns * 4;
+  info->pack_heads = P.pack_heads;
   return TREE_OK;
 }
 
@@ -716,8 +799,8 @@ int tree_plan_tables(const tree_plan_t *plan, tree_plan_host_view_t *v) {
   v->pos = P.image.data() + P.off_pos;
   v->send = P.image.data() + P.off_send;
   v->runs = P.image.data() + P.off_runs;
-  v->vkeys = P.tiling == 1 ? P.image.data() + P.off_vkeys : nullptr;
-  v->vruns = P.tiling == 1 ? P.image.data() + P.off_vruns : nullptr;
+  v->vkeys = P.tiling != 0 ? P.image.data() + P.off_vkeys : nullptr;
+  v->vruns = P.tiling != 0 ? P.image.data() + P.off_vruns : nullptr;
   v->chunk_q0 = P.chunk_q0.data();
   v->chunk_q1 = P.chunk_q1.data();
   v->chunk_t0 = P.chunk_t0.data();

@@ -195,8 +195,6 @@ __global__ void __launch_bounds__(kTileWarps * 32) readout_tile_kernel(
     int32_t *__restrict__ status, int vec_out) {
   static_assert(V == 1 || (V == 2 && EXACT && K % 2 == 0), "letter pairs need an even, compile-time stride");
   extern __shared__ float tile_smem[];
-  sm103::griddep_wait();    // the logits may come from the kernel before this one in the stream
-  sm103::griddep_launch();  // the next kernel may launch (it waits for this one if it reads its results)
   const int S = EXACT ? K : stride_rt;
   const int pitch = S | 1;
   constexpr int NP = EXACT ? K / V : K;  // gather passes (runtime stride: the first S of K)
@@ -212,6 +210,10 @@ __global__ void __launch_bounds__(kTileWarps * 32) readout_tile_kernel(
     return EXACT ? (int)((uint32_t)g / (uint32_t)(K / V)) : (int)(((uint32_t)g * magic) >> 16);
   };
 
+  // The question records are read before waiting for the kernel ahead in the
+  // stream (only the logits come from it), so their memory latency overlaps
+  // that kernel's tail; a caller's kernel that lets dependents launch early must
+  // not write them (the library's kernels never do).
   int my_n = 0;
   float T = 1.f;
   int4 m = make_int4(0, 0, 0, 0);
@@ -221,6 +223,8 @@ __global__ void __launch_bounds__(kTileWarps * 32) readout_tile_kernel(
     my_n = nl[q0 + lane];
     T = temp[q0 + lane];
   }
+  sm103::griddep_wait();    // the logits may come from the kernel before this one in the stream
+  sm103::griddep_launch();  // the next kernel may launch (it waits for this one if it reads its results)
   const bool bad = lane < nv && (my_n < 1 || my_n > S || my_n > 255 || !(T > 0.f));
   m.z = (lane < nv && !bad) ? my_n : 0;  // letters to load
   meta[lane] = m;

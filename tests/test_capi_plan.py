@@ -313,4 +313,105 @@ def test_position_tiling_workload1_and_alone_equals_packed(lib):
         assert run[0] >= 1
     assert lib.Plan([-1], [10], tiling=1).info.n_entries == 1
     with pytest.raises(lib.TreeError):
-        lib.Plan([-1], [10], tiling=2)
+        lib.Plan([-1], [10], tiling=3)
+
+
+# ---------------------------------------------------------------- gathered key tiles
+
+def _check_gathered_tiling(plan, mask, bm):
+    """Every row of a query tile takes exactly its visible keys from the tile's gathered
+    entries, each once; an entry holds keys nobody in the tile sees only in slots no run covers."""
+    t_ = plan.tables()
+    i = plan.info
+    assert i.tiling == 2 and i.bm == bm
+    send = t_["send"]
+    r0s, r1s = t_["qt_row0"], t_["qt_row1"]
+    # query tiles of bm tokens cover every forward row once, chunk by chunk
+    rows = np.concatenate([np.arange(a, b) for a, b in zip(r0s, r1s)])
+    np.testing.assert_array_equal(np.sort(rows), np.arange(i.n_res, i.n_tot))
+    assert all(b - a <= bm for a, b in zip(r0s, r1s))
+    per_row = _position_tiles_of(plan, t_)
+    vk, vr = t_["vkeys"], t_["vruns"]
+    for q in range(i.n_qtiles):
+        r0, r1 = int(r0s[q]), int(r1s[q])
+        prev = -1
+        union = set()
+        for e in range(int(t_["qt_ent0"][q]), int(t_["qt_ent1"][q])):
+            run = vr[e]
+            n = int(run[0])
+            assert 1 <= n <= 16
+            # every row of the tile is assigned to every entry
+            assert all((int(run[4 + (x >> 5)]) >> (x & 31)) & 1 for x in range(r1 - r0))
+            for rr in range(n):
+                c0, c1, j0, se = (int(x) for x in run[8 + 4 * rr: 12 + 4 * rr])
+                assert c0 <= c1 and j0 > prev          # keys ascend through the tile's entries
+                if rr == 0 or j0 != prev + 1:          # a stretch of consecutive keys starts on 8 slots
+                    assert c0 % 8 == 0
+                else:                                  # else it continues the run before, slot by slot
+                    assert c0 == int(run[8 + 4 * (rr - 1) + 1]) + 1
+                prev = j0 + c1 - c0
+                assert (send[j0:prev + 1] == se).all()  # one subtree end: one block's piece
+                union.update(range(j0, prev + 1))
+        want = set()
+        for iq in range(r0, r1):
+            want |= set(np.nonzero(mask[iq])[0].tolist())
+        assert union == want, q                         # no key that nobody in the tile sees
+    for iq in range(i.n_res, i.n_tot):
+        got = []
+        for _, seen in per_row.get(iq, []):
+            got += list(seen.values())
+        assert len(got) == len(set(got))                # each key once
+        assert set(got) == set(np.nonzero(mask[iq])[0].tolist()), iq
+
+
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("pack", [1, 4])
+def test_gathered_tiling_random_forests(lib, seed, pack):
+    rng = np.random.default_rng(1300 + seed)
+    f = synth.random_forest(rng, n_roots=int(rng.integers(1, 4)), max_blocks=int(rng.integers(4, 40)),
+                            max_len=[3, 9, 60, 200][seed % 4], resident_root=bool(seed % 2))
+    try:
+        ref, _ = oplan.plan_forest(f, max_fwd=1024)
+    except oplan.PlanError:
+        pytest.skip("forest has no forward tokens")
+    plan = lib.Plan.from_forest(f, max_fwd=1024, tiling=2, pack_heads=pack)
+    assert plan.info.pack_heads == pack
+    t0 = lib.Plan.from_forest(f, max_fwd=1024).tables()
+    np.testing.assert_array_equal(plan.tables()["pos"], t0["pos"])  # same packing
+    _check_gathered_tiling(plan, oplan.brute_mask(ref), 256 // pack if pack > 1 else 128)
+
+
+@pytest.mark.parametrize("pack", [2, 8])
+def test_gathered_tiling_many_tiny_blocks(lib, pack):
+    # a bush of one-token leaves: more than 16 blocks reach into one query tile, so entries split at 16 runs
+    parent = [-1] + [0] * 300
+    length = [40] + [1] * 300
+    f = synth.Forest(np.array(parent, np.int32), np.array(length, np.int32), np.arange(1, 302, dtype=np.uint64),
+                     np.zeros(301, np.uint8))
+    ref, _ = oplan.plan_forest(f, max_fwd=8192)
+    plan = lib.Plan.from_forest(f, tiling=2, pack_heads=pack)
+    _check_gathered_tiling(plan, oplan.brute_mask(ref), 256 // pack)
+
+
+def test_gathered_tiling_small_leaves_one_entry_per_tile(lib):
+    # many short prompts under a shared template: with four heads packed, each 64-token query tile
+    # sees the template and at most 64 + 23 keys of its own leaves: one gathered tile
+    w = synth.workload(5)
+    plan = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd, tiling=2, pack_heads=4)
+    i = plan.info
+    assert i.bm == 64 and i.n_entries == i.n_qtiles
+    packed = lib.Plan.from_forest(w.forest, max_fwd=w.max_fwd).info
+    # the same visible pairs for a third of the MMA tiles: per kv head, a packed entry is met by
+    # each of the 4 q heads, a gathered one by the tile's two halves (4 heads x 32 tokens each)
+    assert i.pairs == packed.pairs
+    assert i.n_entries * 2 * 2.5 < packed.n_entries * 4
+
+
+def test_gathered_tiling_options_checked(lib):
+    with pytest.raises(lib.TreeError):
+        lib.Plan([-1], [10], tiling=2, pack_heads=3)
+    with pytest.raises(lib.TreeError):
+        lib.Plan([-1], [10], tiling=0, pack_heads=4)
+    with pytest.raises(lib.TreeError):
+        lib.Plan([-1], [10], tiling=1, pack_heads=2)
+    assert lib.Plan([-1], [10], tiling=2, pack_heads=1).info.bm == 128

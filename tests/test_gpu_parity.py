@@ -38,10 +38,10 @@ def _dev(x):
 class Run:
     """A plan on the device plus helpers to call the library."""
 
-    def __init__(self, lib, forest, max_fwd=8192, leaf1=None, leaf2=None, tiling=0):
+    def __init__(self, lib, forest, max_fwd=8192, leaf1=None, leaf2=None, tiling=0, pack_heads=0):
         self.lib = lib
         kw = dict(leaf1=leaf1, leaf2=leaf2) if leaf1 is not None else {}
-        self.plan = lib.Plan.from_forest(forest, max_fwd=max_fwd, tiling=tiling, **kw)
+        self.plan = lib.Plan.from_forest(forest, max_fwd=max_fwd, tiling=tiling, pack_heads=pack_heads, **kw)
         self.oplan, self.oq = oplan.plan_forest(forest, max_fwd=max_fwd, **kw)
         i = self.plan.info
         self.dev = torch.empty(i.dev_bytes, dtype=torch.uint8, device="cuda")
@@ -264,8 +264,8 @@ def _boundary_rows(p):
 
 
 def _attn_check(lib, forest, hq, hkv, d, seed, max_fwd=8192, full=True, rows_per_chunk=48, lse=True,
-                dynamic=True, tiling=0, extra_rows=()):
-    r = Run(lib, forest, max_fwd, tiling=tiling)
+                dynamic=True, tiling=0, extra_rows=(), pack_heads=0):
+    r = Run(lib, forest, max_fwd, tiling=tiling, pack_heads=pack_heads)
     work = torch.zeros(2, dtype=torch.int32, device="cuda") if dynamic else None
     p = r.oplan
     q, k, v = synth.draw_qkv(p.n_fwd, p.n_tot, hq, hkv, d, seed)
@@ -376,6 +376,54 @@ def test_attention_random_forests(lib, seed):
     hq, hkv, d = [(4, 4, 64), (8, 2, 128), (4, 1, 64), (6, 3, 128)][seed % 4]
     _attn_check(lib, f, hq, hkv, d, seed, max_fwd=int(rng.choice([128, 256, 8192])), dynamic=bool(seed % 2),
                 tiling=seed // 4)
+
+
+# ---------------------------------------------------------------- gathered key tiles, packed heads
+
+@pytest.mark.parametrize("pack", [0, 4])
+@pytest.mark.parametrize("n", [1, 2, 3, 5])
+def test_attention_gathered_workloads_full(lib, n, pack):
+    """Gathered key tiles (tiling 2), alone and with the four q heads of a kv head packed into each
+    MMA tile (32 tokens x 4 heads, two such tiles per item sharing its K/V tiles): every workload in
+    full.  The tiny tree has one q head per kv head, so it is never packed."""
+    w = synth.workload(n)
+    if pack and w.hq // w.hkv != pack:
+        pytest.skip("the workload's q/kv head ratio is not the packing")
+    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=True, tiling=2, pack_heads=pack)
+
+
+def test_attention_gathered_long_row_sampled(lib):
+    w = synth.workload(4)
+    p, _ = oplan.plan_forest(w.forest, max_fwd=w.max_fwd)
+    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=False, rows_per_chunk=40, tiling=2,
+                pack_heads=4, extra_rows=_boundary_rows(p))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_attention_gathered_random_forests(lib, seed):
+    """Random forests in chunks; packings of 2, 4 and 8 heads (MMA tiles of 64, 32 and 16 tokens per
+    head) at head dims 64 and 128, and unpacked gathered tiles with one or two heads per item."""
+    rng = np.random.default_rng(1700 + seed)
+    f = synth.random_forest(rng, n_roots=int(rng.integers(1, 5)), max_blocks=int(rng.integers(3, 60)),
+                            max_len=int(rng.choice([4, 20, 150])), dup_prob=0.2, resident_root=bool(seed % 2))
+    try:
+        oplan.plan_forest(f, max_fwd=256)
+    except oplan.PlanError:
+        pytest.skip("forest has no forward tokens")
+    hq, hkv, d, pack = [(8, 2, 64, 4), (8, 4, 128, 2), (16, 2, 64, 8), (4, 4, 64, 0), (3, 3, 128, 0),
+                        (32, 8, 128, 4), (16, 8, 64, 2), (16, 2, 128, 8), (6, 2, 64, 0), (8, 1, 128, 8)][seed]
+    _attn_check(lib, f, hq, hkv, d, seed, max_fwd=int(rng.choice([128, 256, 8192])), dynamic=bool(seed % 3),
+                tiling=2, pack_heads=pack)
+
+
+def test_attention_packing_must_match_head_ratio(lib):
+    w = synth.workload(5)
+    r = Run(lib, w.forest, w.max_fwd, tiling=2, pack_heads=2)
+    p = r.oplan
+    q = torch.zeros((p.n_fwd, 32, 128), dtype=torch.float16, device="cuda")
+    kv = torch.zeros((p.n_tot, 8, 128), dtype=torch.float16, device="cuda")
+    with pytest.raises(lib.TreeError):
+        r.attn(q, kv, kv, 32, 8, 128, 0)
 
 
 @pytest.mark.parametrize("n", [2, 5])
