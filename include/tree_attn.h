@@ -116,10 +116,11 @@ typedef struct {
                         2 = gathered: the keys that some query of the tile sees, in packed
                         order, 128 to a tile (no tile spent on keys nobody in the query tile
                         sees: for batches of short prompts under a shared template) */
-  int32_t pack_heads; /* q heads packed into one 128-row MMA tile with tiling 2 [1]: 1, 2, 4 or 8.
-                        With R > 1 a query tile holds 256 / R tokens, attended as two MMA tiles
-                        of R heads x 128 / R tokens that share each gathered K/V tile; the
-                        attention then needs hq / hkv == R. */
+  int32_t pack_heads; /* q heads packed into one 128-row MMA tile with tiling 1 or 2 [1]: 1, 2, 4
+                        or 8.  With R > 1 a query tile holds 256 / R tokens, attended as two MMA
+                        tiles of R heads x 128 / R tokens that share each K/V tile; the attention
+                        then needs hq / hkv == R.  With tiling 1 each query still takes its keys
+                        in the same tiles, slots and order, so results stay batch-invariant. */
 } tree_plan_opts_t;
 
 typedef struct tree_plan tree_plan_t;

@@ -710,8 +710,9 @@ int tree_pack_plan(const tree_spec_t *spec, const tree_plan_opts_t *opts, tree_p
   if (tiling < 0 || tiling > 2) return tree::fail(TREE_ERR_INVALID_ARG, "tiling %d is not 0, 1 or 2", tiling);
   if (pack_heads < 0 || pack_heads > 8 || (pack_heads & (pack_heads - 1)))
     return tree::fail(TREE_ERR_INVALID_ARG, "pack_heads %d is not 0, 1, 2, 4 or 8", pack_heads);
-  if (pack_heads > 1 && tiling != 2)
-    return tree::fail(TREE_ERR_UNSUPPORTED, "pack_heads %d needs gathered key tiles (tiling 2)", pack_heads);
+  if (pack_heads > 1 && tiling == 0)
+    return tree::fail(TREE_ERR_UNSUPPORTED, "pack_heads %d needs key tiles by position or gathered (tiling 1, 2)",
+                      pack_heads);
   if (tiling == 1 && max_depth > tree::kMaxRuns)
     return tree::fail(TREE_ERR_UNSUPPORTED, "tiling by position needs max_depth <= %d", tree::kMaxRuns);
   auto *pl = new (std::nothrow) tree_plan;

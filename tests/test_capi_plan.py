@@ -412,6 +412,21 @@ def test_gathered_tiling_options_checked(lib):
         lib.Plan([-1], [10], tiling=2, pack_heads=3)
     with pytest.raises(lib.TreeError):
         lib.Plan([-1], [10], tiling=0, pack_heads=4)
-    with pytest.raises(lib.TreeError):
-        lib.Plan([-1], [10], tiling=1, pack_heads=2)
+    assert lib.Plan([-1], [10], tiling=1, pack_heads=2).info.bm == 128
     assert lib.Plan([-1], [10], tiling=2, pack_heads=1).info.bm == 128
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_position_tiling_packed_heads_random_forests(lib, seed):
+    # query tiles of 256 / R tokens; every row still takes its keys per position range from one entry
+    rng = np.random.default_rng(1900 + seed)
+    f = synth.random_forest(rng, n_roots=int(rng.integers(1, 4)), max_blocks=int(rng.integers(4, 40)),
+                            max_len=[3, 9, 60, 200][seed % 4], resident_root=bool(seed % 2))
+    try:
+        ref, _ = oplan.plan_forest(f, max_fwd=8192)
+    except oplan.PlanError:
+        pytest.skip("forest has no forward tokens")
+    R = [2, 4, 8, 4][seed]
+    plan = lib.Plan.from_forest(f, max_fwd=8192, tiling=1, pack_heads=R)
+    assert plan.info.bm == 256 // R and plan.info.pack_heads == R
+    _check_position_tiling(plan, oplan.brute_mask(ref))

@@ -81,9 +81,11 @@ def test_attention_bitwise_alone_batch_tree(lib, d, hq, hkv, template):
     kp = rng.standard_normal((n_prompt, hkv, d)).astype(np.float16)
     vp = rng.standard_normal((n_prompt, hkv, d)).astype(np.float16)
     outs = {}
+    pack = hq // hkv   # the q heads of a kv head in one MMA tile (tiling 1 with packed heads)
     for name, forest, blocks in (("alone", alone, chain), ("batch", batch, prompt)):
-        for tiling in (0, 1):
-            plan = lib.Plan.from_forest(forest, tiling=tiling)
+        for tiling in (0, 1, "1p"):
+            plan = lib.Plan.from_forest(forest, tiling=1 if tiling == "1p" else tiling,
+                                        pack_heads=pack if tiling == "1p" else 0)
             i = plan.info
             tok = _token_index(plan, blocks)
             # every other token gets its own random values
@@ -109,6 +111,10 @@ def test_attention_bitwise_alone_batch_tree(lib, d, hq, hkv, template):
     assert np.array_equal(outs[("alone", 1)].view(np.uint16), outs[("batch", 1)].view(np.uint16))
     # alone, both tilings see the same tiles (packed index = position)
     assert np.array_equal(outs[("alone", 0)].view(np.uint16), outs[("alone", 1)].view(np.uint16))
+    # with the q heads packed into the MMA tiles: the same keys in the same slots and order per row,
+    # each row of an MMA tile summed on its own, so again bit-identical
+    assert np.array_equal(outs[("alone", "1p")].view(np.uint16), outs[("batch", "1p")].view(np.uint16))
+    assert np.array_equal(outs[("alone", "1p")].view(np.uint16), outs[("alone", 1)].view(np.uint16))
 
 
 def test_model_logits_bitwise_alone_batch_tree(lib):

@@ -392,6 +392,27 @@ def test_attention_gathered_workloads_full(lib, n, pack):
     _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=True, tiling=2, pack_heads=pack)
 
 
+@pytest.mark.parametrize("n", [2, 3, 5])
+def test_attention_position_tiled_packed_heads_full(lib, n):
+    """Tiling by position with the four q heads of a kv head packed into each MMA tile."""
+    w = synth.workload(n)
+    _attn_check(lib, w.forest, w.hq, w.hkv, w.d, w.seed, w.max_fwd, full=True, tiling=1, pack_heads=w.hq // w.hkv)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_attention_position_tiled_packed_heads_random_forests(lib, seed):
+    rng = np.random.default_rng(2100 + seed)
+    f = synth.random_forest(rng, n_roots=int(rng.integers(1, 4)), max_blocks=int(rng.integers(3, 40)),
+                            max_len=int(rng.choice([4, 30, 150])), dup_prob=0.2, resident_root=bool(seed % 2))
+    try:
+        oplan.plan_forest(f, max_fwd=256)
+    except oplan.PlanError:
+        pytest.skip("forest has no forward tokens")
+    hq, hkv, d = [(8, 2, 64), (8, 4, 128), (16, 2, 64), (32, 8, 128)][seed]
+    _attn_check(lib, f, hq, hkv, d, seed, max_fwd=int(rng.choice([128, 256, 8192])), dynamic=bool(seed % 2),
+                tiling=1, pack_heads=hq // hkv)
+
+
 def test_attention_gathered_long_row_sampled(lib):
     w = synth.workload(4)
     p, _ = oplan.plan_forest(w.forest, max_fwd=w.max_fwd)
