@@ -367,14 +367,37 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
                   tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES, &mv, it.g * D + 64 * c, jc, v_bar);
               }
             } else {
+              // Lanes 2g and 2g+1 hold the 8 slots of group g.  A group whose slots hold
+              // consecutive keys, or no key at all (slot keys 0), loads as one tiled box of 8
+              // rows (from its first key, or rows 0-7) that lands on its 1024-byte swizzle
+              // period; only the groups where block pieces meet are gathered row by row.
+              const bool c4 = rows.y == rows.x + 1 && rows.z == rows.x + 2 && rows.w == rows.x + 3;
+              const bool z4 = (rows.x | rows.y | rows.z | rows.w) == 0;
+              const int nb_first = __shfl_xor_sync(0xffffffffu, rows.x, 1);
+              const bool nb_c4 = __shfl_xor_sync(0xffffffffu, c4, 1), nb_z4 = __shfl_xor_sync(0xffffffffu, z4, 1);
+              const bool g_box = (z4 && nb_z4) ||
+                                 (c4 && nb_c4 && ((lane & 1) ? rows.x == nb_first + 4 : nb_first == rows.x + 4));
+              if (g_box) {
+                if (!(lane & 1)) {
 #pragma unroll
-              for (int c = 0; c < C::CB; ++c)
-                tma_gather4(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mkg, it.g * D + 64 * c,
-                            rows, b_k(st));
+                  for (int c = 0; c < C::CB; ++c)
+                    tma_load_2d(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &bm.k[0],
+                                it.g * D + 64 * c, rows.x, b_k(st));
 #pragma unroll
-              for (int c = 0; c < C::CB; ++c)
-                tma_gather4(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mvg, it.g * D + 64 * c,
-                            rows, v_bar);
+                  for (int c = 0; c < C::CB; ++c)
+                    tma_load_2d(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &bm.v[0],
+                                it.g * D + 64 * c, rows.x, v_bar);
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < C::CB; ++c)
+                  tma_gather4(s_base + C::K_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mkg, it.g * D + 64 * c,
+                              rows, b_k(st));
+#pragma unroll
+                for (int c = 0; c < C::CB; ++c)
+                  tma_gather4(s_base + C::V_OFF + (st * C::CB + c) * BOX_BYTES + lane * 512, &mvg, it.g * D + 64 * c,
+                              rows, v_bar);
+              }
             }
             __syncwarp();
             continue;
@@ -853,7 +876,7 @@ int launch_tc(const Plan &P, const int32_t *img, int chunk, const void *q, const
       (rc = make_map(&mvg, v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", 1)) ||
       (rc = make_map(&mo, o, (int64_t)hq * D, nq, "tree_attn_fwd", tpm)))
     return rc;
-  if (P.tiling == 2)
+  if (P.tiling != 0)
     for (int lg = 0; lg < 4; ++lg)
       if ((rc = make_map(&bm.k[lg], k, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", 8 << lg)) ||
           (rc = make_map(&bm.v[lg], v, (int64_t)hkv * D, P.n_tot, "tree_attn_fwd", 8 << lg)))
