@@ -127,6 +127,36 @@ def test_readout_65536_questions(lib):
     _check_readout(lib, b["logits"], b["r1"], b["r2"], b["n_letters"], b["temperature"], b["stride"])
 
 
+@pytest.mark.parametrize("with_avg", [False, True])
+def test_readout_262144_questions_sampled(lib, with_avg):
+    """A batch of 262,144 questions (8,192 tiles, more than one wave of resident warps): sampled
+    questions against the oracle, every question of the first and last tiles and a stretch across
+    the middle included; with and without p_avg."""
+    b = synth.draw_readout_batch(262144, seed=9)
+    nq, stride = len(b["r1"]), b["stride"]
+    pc = torch.full((nq, stride), -7.0, device="cuda")
+    pa = torch.full((nq, stride), -7.0, device="cuda") if with_avg else None
+    ch = torch.full((nq,), -9, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.readout_decide(_dev(b["logits"]), stride, _dev(b["r1"]), _dev(b["r2"]), _dev(b["n_letters"]),
+                       _dev(b["temperature"]), nq, pc, pa, ch, st, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rng = np.random.default_rng(3)
+    qs = np.unique(np.concatenate([np.arange(64), np.arange(nq - 64, nq), np.arange(131000, 131400),
+                                   rng.choice(nq, 4000, replace=False)]))
+    ref_pc, ref_pa, _ = ordo.decide(b["logits"], b["r1"][qs], b["r2"][qs], b["n_letters"][qs],
+                                    b["temperature"][qs], stride)
+    assert np.abs(pc.cpu().numpy()[qs] - ref_pc).max() <= ATOL_P
+    if with_avg:
+        assert np.abs(pa.cpu().numpy()[qs] - ref_pa).max() <= ATOL_P
+    got = ch.cpu().numpy()[qs]
+    want = ordo.choice_f32(b["logits"], b["r1"][qs], b["r2"][qs], b["n_letters"][qs])
+    for k in np.nonzero(got != want)[0]:
+        top = np.sort(ref_pa[k])[::-1]
+        assert top[0] - top[1] < 1e-6 and abs(ref_pa[k, got[k]] - top[0]) < 1e-6
+
+
 @pytest.mark.parametrize("stride,nmax", [(1, 1), (3, 2), (10, 10), (16, 16), (17, 17), (31, 20), (32, 32), (33, 33),
                                          (40, 33), (255, 255), (300, 255)])
 def test_readout_sizes(lib, stride, nmax):
