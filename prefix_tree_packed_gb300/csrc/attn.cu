@@ -85,9 +85,14 @@ struct Cfg {
   static constexpr uint32_t O_COL = PSEP ? 128 * NH + 64 * NH : 128 * NH;
   static constexpr uint32_t TMEM_USED = O_COL + D * NH;
   static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
-  // 12 warps launch at 168 registers (3 per SM sub-partition of 16384); setmaxnreg moves them
-  static constexpr int SOFTMAX_REGS = 208;       // 2 x 208 + 88 = 504 <= 512 per sub-partition
+  // 12 warps launch at 168 registers (3 per SM sub-partition of 16384); setmaxnreg moves them.
+  // An increase draws only on what the block launched with, so the warpgroups' shares must
+  // add up to no more than that: a larger sum makes setmaxnreg.inc wait forever.
+  static constexpr int LAUNCH_REGS = 168;
+  static constexpr int SOFTMAX_REGS = 208;
   static constexpr int SERVICE_REGS = 88;
+  static_assert(NH != 2 || 128 * (NH * SOFTMAX_REGS + SERVICE_REGS) <= THREADS * LAUNCH_REGS,
+                "register split exceeds the block's launch allotment");
 };
 
 
