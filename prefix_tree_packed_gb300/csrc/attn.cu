@@ -21,13 +21,13 @@
 //       keeps a running max and sum in the log2 domain, writes P (f16) to
 //       tensor memory, and rescales O in tensor memory only when the running
 //       max grows by more than 2^8 (rare); at the end normalises O and stores
-//       it.  These warps raise their register budget to 208 (setmaxnreg).
+//       it.  At d = 64 these warps raise their register budget to 208 (setmaxnreg).
 //   producer warp: TMA loads of the Q tiles and of K, V (plus the 128 subtree
 //       ends of the key tile) into a ring of shared-memory stages.
 //   MMA warp: one thread issues tcgen05.mma: S_h = Q_h K^T (A, B in shared
 //       memory, 128 x 128 x d) and O_h += P_h V (A = P_h in tensor memory,
 //       B = V in shared memory, 128 x d x 128), each followed by a commit to an
-//       mbarrier.  The producer/MMA warpgroup lowers its budget to 88 registers.
+//       mbarrier.  At d = 64 the producer/MMA warpgroup lowers its budget to 88 registers.
 // Tensor memory (512 columns for two heads):
 //   d = 64 : S_h at 128h, P_h at 256 + 64h, O_h at 384 + 64h.  S_h is free as
 //            soon as the softmax has read it, so S_h(i+1) is computed while the
@@ -85,13 +85,17 @@ struct Cfg {
   static constexpr uint32_t O_COL = PSEP ? 128 * NH + 64 * NH : 128 * NH;
   static constexpr uint32_t TMEM_USED = O_COL + D * NH;
   static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
-  // 12 warps launch at 168 registers (3 per SM sub-partition of 16384); setmaxnreg moves them.
-  // An increase draws only on what the block launched with, so the warpgroups' shares must
-  // add up to no more than that: a larger sum makes setmaxnreg.inc wait forever.
+  // 12 warps launch at 168 registers (3 per SM sub-partition of 16384); at d = 64 setmaxnreg
+  // moves them from the producer/MMA warpgroup to the softmax warpgroups.  An increase draws
+  // only on what the block launched with, so the shares must add up to no more than that: a
+  // larger sum makes setmaxnreg.inc wait forever.  The d = 128 instances keep 168 in every
+  // warp: under a split, some of them computed wrong results, and which one did changed with
+  // the shares (208/88, 200/104) and the number of MMA warps.
+  static constexpr bool SPLIT = NH == 2 && D == 64;
   static constexpr int LAUNCH_REGS = 168;
   static constexpr int SOFTMAX_REGS = 208;
   static constexpr int SERVICE_REGS = 88;
-  static_assert(NH != 2 || 128 * (NH * SOFTMAX_REGS + SERVICE_REGS) <= THREADS * LAUNCH_REGS,
+  static_assert(!SPLIT || 128 * (NH * SOFTMAX_REGS + SERVICE_REGS) <= THREADS * LAUNCH_REGS,
                 "register split exceeds the block's launch allotment");
 };
 
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
   };
 
   if (warp >= 4 * NH) {
-    if (NH == 2) regs_dec<C::SERVICE_REGS>();
+    if (C::SPLIT) regs_dec<C::SERVICE_REGS>();
     if (warp == C::PROD_WARP) {
       // ---------------------------------------------------------- producer (whole warp, one lane issues)
       if (elect_one()) {
@@ -580,7 +584,7 @@ __global__ void __launch_bounds__(Cfg<D, NH>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    if (NH == 2) regs_inc<C::SOFTMAX_REGS>();
+    if (C::SPLIT) regs_inc<C::SOFTMAX_REGS>();
     const int h = warp >> 2;
     const int r = 32 * (warp & 3) + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
