@@ -49,7 +49,7 @@ N_SETS = 4  # rotating input sets: 4 x ~81 MB > 129 MB L2
 # DRAM bytes per attention launch from one ncu capture, valid only for the
 # kernel source it was taken on (sha256 of csrc/attn.cu, first 16 hex digits).
 ATTN_TRAFFIC = {(2, "95cf95238ad36d73"): 53639424, (2, "5196ae79ce41ba40"): 53936896,
-                (2, "bf00683af88959fd"): 52984576}
+                (2, "bf00683af88959fd"): 52984576, (2, "02ab9c012a8bcad5"): 53109760}
 
 
 def _peaks():
